@@ -1,0 +1,520 @@
+"""Benchmark of the GDN token-mixing path on GB300.
+
+Default workload (N=1): varlen prefill bf16 — 8 sequences with lengths drawn
+uniformly from [1, 2048], q/k 16 heads and v 32 heads of 128 (C = 8192),
+conv width 4, half the sequences carrying an initial conv_state and state,
+exact 64-token chunks. One step = one layer's pass of the whole prefill path:
+gdn_conv_fwd (conv + SiLU + q/k L2 norm) then gdn_delta_prefill (chunked
+delta rule + z-gated RMSNorm), through the C ABI.
+
+metric: GDN tokens/s per layer (whole job: tokens of all ranks / max time).
+Other workloads (--workload): tiny-f32, long-prefill-bf16, spec-verify-bf16
+(36 verify launches + 1 batched commit per window), decode-bf16 (36 layers,
+T = 1, every token accepted).
+
+Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference];
+for N > 1 under torch.distributed.run, one rank per GPU, replicas of the same
+workload (the path shards by sequence with no exchange: weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_deltanet_linear_12_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "GDN tokens/sec per layer and achieved HBM GB/s vs GB300 peak (1 GPU)"
+L2_BYTES = 129 * 1024 * 1024
+D = 128
+
+
+# ----------------------------------------------------------------------------- accounting
+def prefill_conv_bytes(n_tok, C, n_seq_init, n_seq, es=2):
+    """Algorithmic HBM bytes of gdn_conv_fwd: read x, write y, conv_w once,
+    conv_state read for sequences with an initial state, written for all."""
+    return 2 * n_tok * C * es + C * 4 * es + (n_seq_init + n_seq) * 3 * C * es
+
+
+def prefill_delta_bytes(n_tok, C, Hv, n_seq_init, n_seq, es=2):
+    """Algorithmic HBM bytes of gdn_delta_prefill: read qkv, z, alpha, beta,
+    write out; state read (initial) and written (final) per sequence."""
+    HvD = Hv * D
+    return (n_tok * (C * es + 2 * HvD * es + 2 * Hv * 4)
+            + (n_seq_init + n_seq) * Hv * D * D * 4)
+
+
+def prefill_delta_flops(n_tok, Hv):
+    """Algorithmic FLOPs of the chunked form per token-head: five 64x64x128
+    intra-chunk products (k.k, q.k, Tinv-applied values and keys, scores x
+    deltas) = 81,920 FLOP and three 64x128x128 state products = 98,304 FLOP."""
+    return n_tok * Hv * (5 * 64 * 128 * 2 + 3 * 128 * 128 * 2)
+
+
+def state_bytes_per_layer(Hv, C, dv=D, dk=D, conv_rows=3, state_es=4, conv_es=4):
+    """Bytes of one layer's recurrent state plus conv_state for one sequence."""
+    return Hv * dv * dk * state_es + C * conv_rows * conv_es
+
+
+def fp32_alu_peak_tflops(sm_mhz, n_sm=152, lanes=128):
+    """FP32 FMA peak: SMs x FP32 lanes per SM x 2 FLOP x clock."""
+    return n_sm * lanes * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+class PrefillWorkload:
+    """One layer's varlen prefill; inputs resident on the device."""
+
+    def __init__(self, name, torch, G, device):
+        self.name, self.torch, self.G, self.dev = name, torch, G, device
+        inp = syn.workload_prefill(name)
+        self.inp = inp
+        self.act = torch.bfloat16 if inp["act"] == "bf16" else torch.float32
+        t = lambda a: self._dev(a)
+        self.x = t(inp["x"])
+        self.y = torch.empty_like(self.x)
+        self.conv_w = t(inp["conv_w"])
+        self.cs0 = t(inp["conv_state"])
+        self.cs = self.cs0.clone()
+        self.S0 = t(inp["state"])
+        self.S = self.S0.clone()
+        self.alpha, self.beta, self.z = t(inp["alpha"]), t(inp["beta"]), t(inp["z"])
+        self.norm_w = t(inp["norm_w"])
+        self.slot, self.cu = t(inp["slot_idx"]), t(inp["cu_seqlens"])
+        self.hic, self.his = t(inp["has_init_conv"]), t(inp["has_init_state"])
+        self.out = torch.empty(inp["n_tok"], inp["Hv"] * D, dtype=self.act, device=device)
+        self.cfg = G.make_config(inp["Hk"], inp["Hv"], self.act, self.S.shape[0])
+        self.tokens = int(inp["n_tok"])
+        es = 2 if inp["act"] == "bf16" else 4
+        n_init_c = int(inp["has_init_conv"].sum())
+        n_init_s = int(inp["has_init_state"].sum())
+        self.bytes = {"conv": prefill_conv_bytes(self.tokens, inp["C"], n_init_c, inp["n_seq"], es),
+                      "prefill": prefill_delta_bytes(self.tokens, inp["C"], inp["Hv"], n_init_s,
+                                                     inp["n_seq"], es)}
+        self.flops = {"prefill": prefill_delta_flops(self.tokens, inp["Hv"])}
+        self.launches_per_step = 2
+
+    def _dev(self, a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return self.torch.from_numpy(a.view(np.int16)).to(self.dev).view(self.torch.bfloat16)
+        return self.torch.from_numpy(a).to(self.dev)
+
+    def reset(self):
+        self.cs.copy_(self.cs0)
+        self.S.copy_(self.S0)
+
+    def step(self, ev=None):
+        G = self.G
+        if ev:
+            ev[0].record()
+        G.gdn_conv_fwd(self.cfg, self.x, self.y, self.conv_w, self.cs, self.slot, self.cu, self.hic)
+        if ev:
+            ev[1].record()
+        G.gdn_delta_prefill(self.cfg, self.y, self.alpha, self.beta, self.z, self.norm_w, self.out,
+                            self.S, self.slot, self.cu, self.his)
+        if ev:
+            ev[2].record()
+
+    # end-to-end: host inputs -> device, step, result -> host (pinned buffers)
+    def setup_e2e(self):
+        torch = self.torch
+        self.h_in = [a.cpu().pin_memory() for a in (self.x, self.alpha, self.beta, self.z)]
+        self.d_in = [self.x, self.alpha, self.beta, self.z]
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h2d = sum(a.numel() * a.element_size() for a in self.h_in)
+        self.d2h = self.h_out.numel() * self.h_out.element_size()
+
+    def step_e2e(self):
+        for h, d in zip(self.h_in, self.d_in):
+            d.copy_(h, non_blocking=True)
+        self.step()
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def config(self):
+        inp = self.inp
+        return {"workload": self.name, "n_seq": int(inp["n_seq"]), "tokens": self.tokens,
+                "lens": [int(v) for v in inp["lens"]], "qk_heads": int(inp["Hk"]),
+                "v_heads": int(inp["Hv"]), "head_dim": D, "conv_width": 4, "channels": int(inp["C"]),
+                "chunk": 64, "state_dtype": "f32", "act_dtype": inp["act"],
+                "l2": "flush 256 MiB between timed steps"}
+
+
+class StepWorkload:
+    """Verify windows (spec-verify-bf16: per window 36 verify launches, then one
+    batched commit of the accepted prefixes of all 36 layers) or decode
+    (decode-bf16: 36 verify launches with every token accepted). Each layer has
+    its own conv_state and state pools; inputs are seeded and generated on the
+    device (standard normals; alpha = exp(-softplus(N)), beta = sigmoid(N))."""
+
+    LAYERS = 36
+
+    def __init__(self, name, torch, G, device, T=None):
+        self.name, self.torch, self.G, self.dev = name, torch, G, device
+        decode = name == "decode-bf16"
+        self.decode = decode
+        self.B = 256 if decode else 32
+        self.T = 1 if decode else (T or 8)
+        self.Hk, self.Hv = 16, 32
+        self.C = (2 * self.Hk + self.Hv) * D
+        B, T, Hv, C, L = self.B, self.T, self.Hv, self.C, self.LAYERS
+        g = torch.Generator(device=device)
+        g.manual_seed(syn.seed_of(name) + T)
+        bf = torch.bfloat16
+        self.n_slots = B
+        rn = lambda *shape, dt=torch.float32: torch.randn(*shape, generator=g, device=device,
+                                                          dtype=torch.float32).to(dt)
+        self.layers = []
+        for _ in range(L):
+            lay = dict(x=rn(B, T, C, dt=bf), conv_w=(rn(C, 4) * 0.5).to(bf),
+                       conv_state=rn(B, 3, C, dt=bf), state=rn(B, Hv, D, D),
+                       alpha=torch.exp(-torch.nn.functional.softplus(rn(B, T, Hv))),
+                       beta=torch.sigmoid(rn(B, T, Hv)), z=rn(B, T, Hv * D, dt=bf))
+            self.layers.append(lay)
+        self.norm_w = (1 + 0.1 * rn(D)).contiguous()
+        self.slot = torch.randperm(B, generator=g, device=device).to(torch.int32)
+        self.n_keep = torch.randint(0, T + 1, (B,), generator=g, device=device, dtype=torch.int32)
+        self.out = torch.empty(B, T, Hv * D, dtype=bf, device=device)
+        self.cfg = G.make_config(self.Hk, self.Hv, bf, self.n_slots)
+        self.views = G.make_layer_views([{k: l[k] for k in ("x", "alpha", "beta", "conv_w",
+                                                             "conv_state", "state")}
+                                         for l in self.layers], device)
+        self.tokens = B * T                                 # per layer per step
+        self.launches_per_step = L + (0 if decode else 1)
+        nk = self.n_keep.cpu().numpy()
+        S_head = D * D * 4
+        per_seq_state = Hv * S_head
+        self.bytes = {
+            "verify": L * (B * per_seq_state * (2 if decode else 1)
+                           + B * 3 * C * 2 * (2 if decode else 1)
+                           + B * T * (C * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + C * 4 * 2),
+            "commit": 0 if decode else L * int(
+                sum(2 * per_seq_state + 2 * 3 * C * 2 + n * (C * 2 + 2 * Hv * 4) + C * 4 * 2
+                    for n in nk if n > 0)),
+        }
+
+    def reset(self):
+        pass                                                # state evolution does not change work
+
+    def step(self, ev=None):
+        G = self.G
+        if ev:
+            ev[0].record()
+        for lay in self.layers:
+            G.gdn_verify_step(self.cfg, lay["x"], lay["conv_w"], lay["conv_state"], lay["state"],
+                              lay["alpha"], lay["beta"], lay["z"], self.norm_w, self.out, self.slot,
+                              commit_all=self.decode)
+        if ev:
+            ev[1].record()
+        if not self.decode:
+            G.gdn_commit_layers(self.cfg, self.views, self.LAYERS, self.slot, self.n_keep, self.T)
+        if ev:
+            ev[2].record()
+
+    def setup_e2e(self):
+        torch = self.torch
+        self.h_x = [l["x"].cpu().pin_memory() for l in self.layers]
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h2d = sum(a.numel() * a.element_size() for a in self.h_x)
+        self.d2h = self.h_out.numel() * self.h_out.element_size()
+
+    def step_e2e(self):
+        for h, l in zip(self.h_x, self.layers):
+            l["x"].copy_(h, non_blocking=True)
+        self.step()
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def config(self):
+        return {"workload": self.name, "batch": self.B, "draft_tokens": self.T,
+                "layers": self.LAYERS, "qk_heads": self.Hk, "v_heads": self.Hv, "head_dim": D,
+                "channels": self.C, "state_dtype": "f32", "act_dtype": "bf16",
+                "n_keep": "uniform in [0, T]" if not self.decode else "all",
+                "l2": "state pools of all layers exceed L2; flush 256 MiB between timed steps"}
+
+
+# ----------------------------------------------------------------------------- CPU baseline
+def cpu_baseline(name, max_tokens=4096):
+    """The oracle as it stands (single thread) on a bounded sample of the
+    workload: the first max_tokens tokens of its sequences, conv + recurrence."""
+    import oracle as orc
+    inp = syn.workload_prefill(name)
+    lens, cu = inp["lens"], inp["cu_seqlens"]
+    keep, tot = [], 0
+    for s in range(inp["n_seq"]):
+        n = int(min(lens[s], max_tokens - tot))
+        if n <= 0:
+            break
+        keep.append((s, n))
+        tot += n
+    rows = np.concatenate([np.arange(cu[s], cu[s] + n) for s, n in keep])
+    cu2 = np.concatenate([[0], np.cumsum([n for _, n in keep])]).astype(np.int32)
+    ss = [s for s, _ in keep]
+    t0 = time.perf_counter()
+    y, _ = orc.conv_fwd(inp["x"][rows], inp["conv_w"], inp["conv_state"], inp["slot_idx"][ss], cu2,
+                        inp["has_init_conv"][ss], inp["Hk"], inp["Hv"])
+    if inp["act"] == "bf16":
+        y = orc.round_bf16(y)
+    orc.prefill(y, inp["alpha"][rows], inp["beta"][rows], inp["z"][rows], inp["norm_w"],
+                inp["state"], inp["slot_idx"][ss], cu2, inp["has_init_state"][ss], inp["Hk"],
+                inp["Hv"])
+    dt = time.perf_counter() - t0
+    return {"value": tot / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {tot} tokens of {len(keep)} sequence(s) of the {name} workload, "
+                      f"conv + token-by-token recurrence in f64, {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="varlen-prefill-bf16")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--T", type=int, default=8, help="draft tokens of spec-verify-bf16")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    from gated_deltanet_linear_12_gb300 import build as _build, gdn as G
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    if args.workload in ("spec-verify-bf16", "decode-bf16"):
+        W = StepWorkload(args.workload, torch, G, dev, T=args.T)
+    else:
+        W = PrefillWorkload(args.workload, torch, G, dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 3)):
+        W.reset()
+        W.step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        W.reset()
+        flush.fill_(float(k))
+        W.step(evs[k])
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    conv_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
+    pf_ms = [evs[k][1].elapsed_time(evs[k][2]) for k in range(args.steps)]
+    step_ms = [c + p for c, p in zip(conv_ms, pf_ms)]
+    ms = statistics.mean(step_ms)
+    ms_t = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+
+    # end-to-end through the public API with host buffers
+    W.setup_e2e()
+    for _ in range(3):
+        W.reset()
+        W.step_e2e()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for k in range(args.steps):
+        W.reset()
+        flush.fill_(float(k))
+        e0.record()
+        W.step_e2e()
+        e1.record()
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_t = torch.tensor([statistics.mean(e2e_ms)], device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+
+    if rank == 0:
+        peaks, peak_src = load_peaks()
+        a_avg, b_avg = statistics.mean(conv_ms), statistics.mean(pf_ms)
+        tokens_total = W.tokens * world
+        if isinstance(W, StepWorkload):
+            names = ("verify_step_kernel", "commit_kernel")
+            ka = {"ms": round(a_avg, 4), "bytes": W.bytes["verify"],
+                  "GB/s": round(W.bytes["verify"] / (a_avg * 1e-3) / 1e9, 1)}
+            ka["frac_hbm"] = round(ka["GB/s"] / peaks["hbm_gbs"], 4)
+            kernels = {names[0]: ka}
+            if not W.decode:
+                kb = {"ms": round(b_avg, 4), "bytes": W.bytes["commit"],
+                      "GB/s": round(W.bytes["commit"] / max(b_avg, 1e-9) / 1e6, 1)}
+                kb["frac_hbm"] = round(kb["GB/s"] / peaks["hbm_gbs"], 4)
+                kernels[names[1]] = kb
+            roof = {"kernel": names[0] + " (36 launches)", "bound": "hbm", "achieved": ka["GB/s"],
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ka["frac_hbm"],
+                    "traffic": None, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+            value = tokens_total * W.LAYERS / (ms_max * 1e-3)
+        else:
+            alu_peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
+            pf_tflops = W.flops["prefill"] / (b_avg * 1e-3) / 1e12
+            pf_gbs = W.bytes["prefill"] / (b_avg * 1e-3) / 1e9
+            conv_gbs = W.bytes["conv"] / (a_avg * 1e-3) / 1e9
+            if b_avg >= a_avg:
+                roof = {"kernel": "prefill_ffma_kernel", "bound": "alu",
+                        "achieved": round(pf_tflops, 3), "peak": round(alu_peak, 1),
+                        "unit": "TFLOP/s", "frac": round(pf_tflops / alu_peak, 4), "traffic": None,
+                        "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x "
+                                       f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz",
+                        "algorithmic_flops_per_launch": W.flops["prefill"],
+                        "hbm_gbs": round(pf_gbs, 1)}
+            else:
+                roof = {"kernel": "conv_fwd_kernel", "bound": "hbm", "achieved": round(conv_gbs, 1),
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(conv_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                        "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+            kernels = {
+                "conv_fwd_kernel": {"ms": round(a_avg, 4), "bytes": W.bytes["conv"],
+                                    "GB/s": round(conv_gbs, 1),
+                                    "frac_hbm": round(conv_gbs / peaks["hbm_gbs"], 4)},
+                "prefill_ffma_kernel": {"ms": round(b_avg, 4), "bytes": W.bytes["prefill"],
+                                        "GB/s": round(pf_gbs, 1), "TFLOP/s": round(pf_tflops, 3)},
+            }
+            value = tokens_total / (ms_max * 1e-3)
+        e2e_val = value * ms_max / float(e2e_t.item())
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": W.config(), "roofline": roof, "kernels": kernels,
+            "e2e": {"value": round(e2e_val, 1),
+                    "unit": "tokens/s", "h2d_bytes_per_step": W.h2d, "d2h_bytes_per_step": W.d2h},
+            "gpu_launches": W.launches_per_step * args.steps,
+            "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+            "wall_s_timed_region": round(t_wall, 3),
+        }
+        if world == 1 and not args.no_cpu_baseline and isinstance(W, PrefillWorkload):
+            line["cpu_baseline"] = cpu_baseline(args.workload)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def reference_arm(args, rank, world):
+    """The oracle as the reference arm: each step is one bounded sample of the
+    workload run by the single-threaded CPU oracle."""
+    if rank != 0:
+        return 0
+    import oracle as orc
+    orc.build()
+    for _ in range(args.warmup):
+        pass                                      # the oracle has no warm-up state
+    times, toks = [], 0
+    line0 = None
+    for _ in range(args.steps):
+        cb = cpu_baseline(args.workload, max_tokens=512)
+        times.append(1.0 / cb["value"])
+        line0 = cb
+    tps = 1.0 / statistics.mean(times)
+    line = {"impl": "reference", "metric": METRIC, "value": round(tps, 2), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(512 / tps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload,
+                       "sample": "first 512 tokens of the workload per step"},
+            "cpu_baseline": {"value": round(tps, 2), "unit": "tokens/s", "cores": 1,
+                             "kind": "oracle", "sample": line0["sample"] if line0 else ""},
+            "e2e": {"value": round(tps, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,58 @@
+// Internal launcher interface between the C ABI (gdn_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+struct StepArgs {
+  const void* x;            // [B][T][C]
+  const void* conv_w;       // [C][4]
+  void* conv_state;         // pool
+  float* state;             // pool
+  const float* alpha;       // [B][T][Hv]
+  const float* beta;
+  const void* z;            // [B][T][Hv*D]
+  const float* norm_w;      // [D]
+  void* out;                // [B][T][Hv*D]
+  void* postconv;           // nullable [B][T][C]
+  const int32_t* slot_idx;  // [B]
+  const int32_t* n_keep;    // [B] (commit)
+  const gdn_layer_view* layers;  // [L] (commit)
+  int B, T, Hk, Hv, n_slots;
+  float eps, q_scale;
+  uint32_t* dev_err;
+};
+
+struct PrefillArgs {
+  const void* qkv;
+  const float* alpha;
+  const float* beta;
+  const void* z;
+  const float* norm_w;
+  void* out;
+  float* state;
+  const int32_t* slot_idx;
+  const int32_t* cu;
+  const uint8_t* has_init;
+  int n_seq, Hk, Hv, n_slots;
+  int64_t n_tok;
+  float eps, q_scale;
+  uint32_t* dev_err;
+};
+
+cudaError_t launch_conv_fwd(const gdn_config& cfg, const void* x, int64_t ld_x, void* y,
+                            int64_t ld_y, const void* conv_w, void* conv_state,
+                            const int32_t* slot_idx, const int32_t* cu, const uint8_t* has_init,
+                            int n_seq, int64_t n_tok, int fuse_norm, cudaStream_t stream);
+cudaError_t launch_postconv_norm(const gdn_config& cfg, int in_t, const void* yin, int out_t,
+                                 void* yout, int64_t n_tok, int n_sm, cudaStream_t stream);
+cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, cudaStream_t stream);
+cudaError_t launch_commit(const StepArgs& a, int L, int act, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& a, int act, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,185 @@
+"""ctypes binding of libgdn.so: the C ABI of include/gdn.h with the same names.
+
+Argument marshalling only — every step of the path runs in the library's CUDA
+kernels. Tensors are PyTorch CUDA tensors (device memory); the current torch
+stream of the tensors' device is passed unless a stream is given. A non-OK
+status raises GdnError. If libgdn.so is missing the first call raises: there is
+no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+GDN_OK, GDN_ERR_INVALID, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
+GDN_F32, GDN_BF16 = 0, 1
+GDN_VERIFY_COMMIT_ALL = 1
+GDN_DEVERR_SLOT, GDN_DEVERR_NKEEP, GDN_DEVERR_SEQLENS = 1, 2, 4
+HEAD_DIM, CONV_WIDTH, CHUNK, MAX_DRAFT = 128, 4, 64, 8
+
+EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_step",
+           "gdn_commit_layers", "gdn_status_string"]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn} returned {status} ({msg})")
+        self.status = status
+
+
+class GdnConfig(ctypes.Structure):
+    _fields_ = [("n_qk_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("conv_width", ctypes.c_int32),
+                ("act", ctypes.c_int32), ("eps", ctypes.c_float), ("q_scale", ctypes.c_float),
+                ("n_slots", ctypes.c_int32), ("dev_err", ctypes.c_void_p)]
+
+
+class GdnLayerView(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+                ("conv_w", ctypes.c_void_p), ("conv_state", ctypes.c_void_p),
+                ("state", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libgdn.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"{_build.LIB} is missing: build it with "
+                                   "gated_deltanet_linear_12_gb300.build.build()")
+            L = ctypes.CDLL(_build.LIB)
+            vp, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+            cfgp = ctypes.POINTER(GdnConfig)
+            L.gdn_conv_fwd.argtypes = [cfgp, vp, i64, vp, i64, vp, vp, vp, vp, vp, i32, i64, i32, vp]
+            L.gdn_postconv_norm.argtypes = [cfgp, i32, vp, i32, vp, i64, vp]
+            L.gdn_delta_prefill.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64,
+                                            i32, vp]
+            L.gdn_verify_step.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                          u32, vp, vp]
+            L.gdn_commit_layers.argtypes = [cfgp, vp, i32, vp, vp, i32, i32, vp]
+            for f in EXPORTS[:-1]:
+                getattr(L, f).restype = ctypes.c_int
+            L.gdn_status_string.argtypes = [ctypes.c_int]
+            L.gdn_status_string.restype = ctypes.c_char_p
+            _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return load().gdn_status_string(status).decode()
+
+
+def _check(fn, status):
+    if status != GDN_OK:
+        raise GdnError(fn, status, status_string(status))
+
+
+def act_of(dtype: torch.dtype) -> int:
+    if dtype == torch.bfloat16:
+        return GDN_BF16
+    if dtype == torch.float32:
+        return GDN_F32
+    raise ValueError(f"unsupported activation dtype {dtype}")
+
+
+def make_config(n_qk_heads, n_v_heads, act, n_slots, *, eps=1e-6, q_scale=1.0, dev_err=None):
+    """gdn_config; act is GDN_F32/GDN_BF16 or a torch dtype; dev_err a CUDA int32 tensor."""
+    if isinstance(act, torch.dtype):
+        act = act_of(act)
+    return GdnConfig(n_qk_heads, n_v_heads, HEAD_DIM, CONV_WIDTH, act, eps, q_scale, n_slots,
+                     dev_err.data_ptr() if dev_err is not None else None)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    return t.data_ptr()
+
+
+def _stream(t, stream):
+    if stream is not None:
+        return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _dense(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+
+
+# ----------------------------------------------------------------------------- entry points
+def gdn_conv_fwd(cfg, x, y, conv_w, conv_state, slot_idx, cu_seqlens, has_init, *,
+                 fuse_norm=True, stream=None):
+    """x, y: [n_tok][>=C] (row stride = leading dimension); see include/gdn.h."""
+    if x.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("x and y rows must be contiguous")
+    _dense(conv_w, conv_state, slot_idx, cu_seqlens, has_init)
+    _check("gdn_conv_fwd", load().gdn_conv_fwd(
+        ctypes.byref(cfg), _ptr(x), x.stride(0), _ptr(y), y.stride(0), _ptr(conv_w),
+        _ptr(conv_state), _ptr(slot_idx), _ptr(cu_seqlens), _ptr(has_init), slot_idx.numel(),
+        x.shape[0], int(bool(fuse_norm)), _stream(x, stream)))
+
+
+def gdn_postconv_norm(cfg, y_in, y_out, *, stream=None):
+    _dense(y_in, y_out)
+    _check("gdn_postconv_norm", load().gdn_postconv_norm(
+        ctypes.byref(cfg), act_of(y_in.dtype), _ptr(y_in), act_of(y_out.dtype), _ptr(y_out),
+        y_in.shape[0], _stream(y_in, stream)))
+
+
+def gdn_delta_prefill(cfg, qkv, alpha, beta, z, norm_w, out, state, slot_idx, cu_seqlens,
+                      has_init, *, chunk=CHUNK, stream=None):
+    _dense(qkv, alpha, beta, z, norm_w, out, state, slot_idx, cu_seqlens, has_init)
+    _check("gdn_delta_prefill", load().gdn_delta_prefill(
+        ctypes.byref(cfg), _ptr(qkv), _ptr(alpha), _ptr(beta), _ptr(z), _ptr(norm_w), _ptr(out),
+        _ptr(state), _ptr(slot_idx), _ptr(cu_seqlens), _ptr(has_init), slot_idx.numel(),
+        qkv.shape[0], chunk, _stream(qkv, stream)))
+
+
+def gdn_verify_step(cfg, x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, *,
+                    commit_all=False, postconv_out=None, stream=None):
+    """x [B][T][C]; alpha, beta [B][T][Hv]; z, out [B][T][Hv*128]."""
+    _dense(x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, postconv_out)
+    B, T = x.shape[0], x.shape[1]
+    _check("gdn_verify_step", load().gdn_verify_step(
+        ctypes.byref(cfg), _ptr(x), _ptr(conv_w), _ptr(conv_state), _ptr(state), _ptr(alpha),
+        _ptr(beta), _ptr(z), _ptr(norm_w), _ptr(out), _ptr(slot_idx), B, T,
+        GDN_VERIFY_COMMIT_ALL if commit_all else 0, _ptr(postconv_out), _stream(x, stream)))
+
+
+def make_layer_views(layers, device):
+    """Device array [L] of gdn_layer_view from dicts with keys x, alpha, beta,
+    conv_w, conv_state, state (CUDA tensors). Returns a uint8 CUDA tensor; the
+    tensors it points to must outlive its use."""
+    arr = (GdnLayerView * len(layers))()
+    for i, l in enumerate(layers):
+        arr[i] = GdnLayerView(_ptr(l["x"]), _ptr(l["alpha"]), _ptr(l["beta"]), _ptr(l["conv_w"]),
+                              _ptr(l["conv_state"]), _ptr(l["state"]))
+    raw = bytes(arr)
+    host = torch.frombuffer(bytearray(raw), dtype=torch.uint8)
+    return host.to(device)
+
+
+def gdn_commit_layers(cfg, views, n_layers, slot_idx, n_keep, T, *, stream=None):
+    """views: uint8 CUDA tensor from make_layer_views (n_layers entries)."""
+    _dense(slot_idx, n_keep)
+    _check("gdn_commit_layers", load().gdn_commit_layers(
+        ctypes.byref(cfg), _ptr(views), n_layers, _ptr(slot_idx), _ptr(n_keep), slot_idx.numel(),
+        T, _stream(slot_idx, stream)))

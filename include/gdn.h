@@ -1,0 +1,198 @@
+/*
+ * gdn.h — C ABI of the Gated DeltaNet token-mixing library for GB300 (sm_103a).
+ *
+ * The path: width-4 depthwise causal conv1d over packed q|k|v channels with a
+ * per-sequence conv_state, SiLU, per-head L2 normalisation of q and k, the
+ * gated delta-rule recurrence
+ *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,   o_t = S_t q_t,
+ * and a z-gated RMSNorm of o_t. Three phases use it: varlen prefill, the
+ * speculative verify of T = 1..8 draft tokens, and the commit of the accepted
+ * prefix of conv_state and recurrent state across all layers.
+ *
+ * Sources (page title, section):
+ *   "perf(gdn): optimize post-conv and causal-conv kernels - #155" — the causal
+ *     conv ("Blocker"), the post-conv 128-lane sum of squares then 1/sqrt and the
+ *     initial/final conv_state rows of exact chunks ("Merged ...", "New issue #305");
+ *     exact causal-conv chunk descriptors ("Before starting").
+ *   "Strata PR #3226" — speculative verify over T draft tokens, the output norm,
+ *     and the one-call commit of conv_state and state for all layers ("Summary").
+ *
+ * Conventions shared by every entry point
+ *   - head_dim d = 128 and conv width 4 are the only supported values.
+ *   - C = (2*Hk + Hv) * 128 packed channels [q heads | k heads | v heads]; v head
+ *     h reads q/k head h / (Hv/Hk).
+ *   - Activations (x, post-conv rows, z, out, conv_w, conv_state) have the dtype
+ *     cfg->act: GDN_F32 or GDN_BF16. alpha, beta, norm_w and the state S are f32.
+ *   - Layouts are row-major: x/qkv [n_tok][C]; conv_w [C][4] (tap 3 multiplies
+ *     the current token); conv_state pool [n_slots][3][C] (oldest row first);
+ *     state pool [n_slots][Hv][128 value rows][128 key columns] f32;
+ *     alpha/beta [tokens][Hv]; z/out [tokens][Hv*128]; norm_w [128].
+ *   - All pointers are caller-owned DEVICE memory unless stated. The library
+ *     allocates nothing, keeps no state between calls, never synchronises, and
+ *     enqueues its kernels on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Every pointer must be 16-byte aligned; leading dimensions are in elements
+ *     and must keep rows 16-byte aligned.
+ *   - Errors: host-side validation failures return GDN_ERR_INVALID or
+ *     GDN_ERR_UNSUPPORTED and enqueue nothing; a failed launch returns
+ *     GDN_ERR_CUDA. Bad device-resident indices (a slot >= cfg->n_slots, n_keep
+ *     outside [0, T], inconsistent cu_seqlens) skip the affected sequence and OR
+ *     a GDN_DEVERR_* bit into *cfg->dev_err when that pointer is non-null. A
+ *     negative slot index marks padding: the entry is skipped without error.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID = 1,      /* null pointer, bad shape, aliasing, misalignment */
+  GDN_ERR_UNSUPPORTED = 2,  /* head_dim != 128, conv_width != 4, unknown dtype */
+  GDN_ERR_CUDA = 3          /* a kernel launch failed */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+#define GDN_HEAD_DIM 128
+#define GDN_CONV_WIDTH 4
+#define GDN_MAX_DRAFT 8
+#define GDN_CHUNK 64
+
+/* verify flags */
+#define GDN_VERIFY_COMMIT_ALL 1u  /* accept every draft token: advance conv_state
+                                     and state in place (decode) */
+
+/* device error bits */
+#define GDN_DEVERR_SLOT 1u        /* slot index >= n_slots */
+#define GDN_DEVERR_NKEEP 2u       /* n_keep outside [0, T] */
+#define GDN_DEVERR_SEQLENS 4u     /* cu_seqlens decreasing or beyond n_tok */
+
+typedef struct gdn_config {
+  int32_t n_qk_heads;   /* Hk >= 1 */
+  int32_t n_v_heads;    /* Hv >= 1, a multiple of Hk */
+  int32_t head_dim;     /* must be 128 */
+  int32_t conv_width;   /* must be 4 */
+  int32_t act;          /* gdn_dtype of the activations */
+  float eps;            /* epsilon of the q/k L2 norm and of the RMSNorm (inside the root) */
+  float q_scale;        /* multiplies o_t; 1.0 gives o_t = S_t q_t */
+  int32_t n_slots;      /* slots in the conv_state and state pools */
+  uint32_t* dev_err;    /* nullable device word receiving GDN_DEVERR_* bits */
+} gdn_config;
+
+/* One layer's device views for gdn_commit_layers (the array itself lives in
+ * device memory). x, alpha, beta are that layer's verify inputs. */
+typedef struct gdn_layer_view {
+  const void* x;         /* [B][T][C] act */
+  const float* alpha;    /* [B][T][Hv] */
+  const float* beta;     /* [B][T][Hv] */
+  const void* conv_w;    /* [C][4] act */
+  void* conv_state;      /* [n_slots][3][C] act, updated in place */
+  float* state;          /* [n_slots][Hv][128][128], updated in place */
+} gdn_layer_view;
+
+/*
+ * gdn_conv_fwd — varlen causal conv1d (width 4) + SiLU (+ q/k L2 norm).
+ * Source: "perf(gdn) ... #155" — the causal conv and its exact 64-token chunks
+ * aligned to each sequence start; the initial conv_state is read and the final
+ * one written by the same thread block (the chunk-0 block), so the read/write
+ * race of "New issue #305" cannot occur.
+ *
+ *   x          [n_tok][ld_x] act; sequence s owns rows cu_seqlens[s]..cu_seqlens[s+1]-1
+ *   y          [n_tok][ld_y] act; must not overlap x (other blocks read x halos)
+ *   conv_w     [C][4] act
+ *   conv_state pool; slot slot_idx[s] is read when has_init[s] (else zeros) and
+ *              always receives the last 3 rows of (initial rows ++ x rows of s)
+ *   slot_idx   [n_seq] int32, cu_seqlens [n_seq+1] int32, has_init [n_seq] uint8
+ *   fuse_norm  1: L2-normalise q and k heads of the SiLU output (f32 math before
+ *              the store); 0: store SiLU output only (see gdn_postconv_norm)
+ * Every sequence, empty ones included, commits its conv_state.
+ */
+gdn_status gdn_conv_fwd(const gdn_config* cfg, const void* x, int64_t ld_x, void* y,
+                        int64_t ld_y, const void* conv_w, void* conv_state,
+                        const int32_t* slot_idx, const int32_t* cu_seqlens,
+                        const uint8_t* has_init, int32_t n_seq, int64_t n_tok,
+                        int32_t fuse_norm, void* stream);
+
+/*
+ * gdn_postconv_norm — per-head L2 norm of the q and k heads of post-conv rows;
+ * v channels are copied (converted to out_t).
+ * Source: "perf(gdn) ... #155", "Merged ...": 128-lane sum of squares, then
+ * 1/sqrt, then scale. The f32 order is fixed: squares of 16 groups of 8
+ * contiguous channels folded with strides 4, 2, 1, then the 16 group sums with
+ * strides 8, 4, 2, 1; r = 1/sqrt(sum + eps) with correctly rounded sqrt and
+ * divide. An f32 -> f32 call is therefore bitwise reproducible.
+ *   y_in [n_tok][C] in_t, y_out [n_tok][C] out_t; y_out may equal y_in when
+ *   in_t == out_t (in place); partial overlap is invalid.
+ */
+gdn_status gdn_postconv_norm(const gdn_config* cfg, int32_t in_t, const void* y_in,
+                             int32_t out_t, void* y_out, int64_t n_tok, void* stream);
+
+/*
+ * gdn_delta_prefill — chunked (WY-form) gated delta rule over varlen sequences,
+ * with the z-gated RMSNorm fused into the output.
+ * Source: the recurrence S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T,
+ * o_t = S_t q_t, and "Strata PR #3226" (output norm after the recurrence).
+ *   qkv     [n_tok][C] act: post-conv rows (q, k L2-normalised), e.g. from
+ *           gdn_conv_fwd(fuse_norm=1)
+ *   alpha, beta [n_tok][Hv] f32 (already activated gates)
+ *   z, out  [n_tok][Hv*128] act; out = RMSNorm(o) * norm_w * silu(z)
+ *   norm_w  [128] f32
+ *   state   pool: read at slot_idx[s] when has_init[s] (else zero), always
+ *           written with the state after the last token of s
+ *   chunk   must be GDN_CHUNK (64)
+ */
+gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const float* alpha,
+                             const float* beta, const void* z, const float* norm_w, void* out,
+                             float* state, const int32_t* slot_idx, const int32_t* cu_seqlens,
+                             const uint8_t* has_init, int32_t n_seq, int64_t n_tok,
+                             int32_t chunk, void* stream);
+
+/*
+ * gdn_verify_step — speculative verify of T draft tokens for B sequences of one
+ * layer: conv from conv_state (+SiLU, +L2 norm), the recurrence from the current
+ * state, and the gated RMSNorm, for every draft token.
+ * Source: "Strata PR #3226" ("Summary": verify forward launched once per layer).
+ *   x       [B][T][C] act (raw, pre-conv rows of the draft tokens)
+ *   alpha, beta [B][T][Hv] f32; z, out [B][T][Hv*128] act; norm_w [128] f32
+ *   slot_idx [B] int32 into both pools
+ *   flags   0: conv_state and state are only read;
+ *           GDN_VERIFY_COMMIT_ALL: both advance in place by all T tokens,
+ *           bitwise equal to this call without the flag followed by
+ *           gdn_commit_layers with n_keep = T.
+ *   postconv_out  nullable [B][T][C] act: the post-conv activations used
+ *   T in 1..GDN_MAX_DRAFT.
+ */
+gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* conv_w,
+                           void* conv_state, float* state, const float* alpha,
+                           const float* beta, const void* z, const float* norm_w, void* out,
+                           const int32_t* slot_idx, int32_t B, int32_t T, uint32_t flags,
+                           void* postconv_out, void* stream);
+
+/*
+ * gdn_commit_layers — commit the accepted prefix of a verify window in every
+ * layer in one call: for each layer l and batch entry b with 0 < n = n_keep[b]
+ * <= T, conv_state <- last 3 rows of (conv_state ++ x[b, 0:n]) and state <- the
+ * state after the first n draft tokens, recomputed exactly as gdn_verify_step
+ * computes them. n_keep[b] == 0 leaves slot b untouched in every layer.
+ * Source: "Strata PR #3226", "Summary" item 1 (batched commit across layers).
+ *   layers  DEVICE array [L] of gdn_layer_view
+ *   slot_idx, n_keep [B] int32 (device), shared by all layers
+ * The result for a (layer, slot, n_keep) is bitwise independent of L, B and of
+ * how layers are grouped into calls.
+ */
+gdn_status gdn_commit_layers(const gdn_config* cfg, const gdn_layer_view* layers, int32_t L,
+                             const int32_t* slot_idx, const int32_t* n_keep, int32_t B,
+                             int32_t T, void* stream);
+
+/* Static description of a status code. */
+const char* gdn_status_string(gdn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -138,6 +138,15 @@ def gated_rmsnorm(o, z, w, *, eps=1e-6, prec="f64"):
     return out
 
 
+def silu(v, prec="f64"):
+    """SiLU y / (1 + exp(-y)) elementwise (f32: the documented exp scheme)."""
+    vw = widen(v, prec).copy()
+    f = _fn("oracle_silu", prec)
+    f.restype = None
+    f(_p(vw), ctypes.c_int64(vw.size))
+    return vw
+
+
 def round_bf16(v, prec="f64"):
     """Round to bfloat16 values (nearest even), returned in the oracle type."""
     vw = widen(v, prec).copy()
@@ -172,8 +181,11 @@ def prefill(qkv, alpha, beta, z, norm_w, state, slot_idx, cu_seqlens, has_init, 
 
 def verify(x, conv_w, conv_state, state, alpha, beta, z, norm_w, slot_idx, Hk, Hv, *,
            q_scale=1.0, eps=1e-6, round_act=True, commit_all=False, prec="f64",
-           want_raw=False):
+           want_raw=False, act32=False):
     """Speculative verify of T draft tokens (x [B][T][C]).
+
+    act32: compute the post-conv activations with the float instantiation
+    (the float order the GPU follows) whatever prec is.
 
     Returns (out [B][T][Hv*D], postconv [B][T][C], conv_state', state'[, o_raw]);
     the states are unchanged copies unless commit_all.
@@ -191,13 +203,13 @@ def verify(x, conv_w, conv_state, state, alpha, beta, z, norm_w, slot_idx, Hk, H
     f(_p(xw), _p(widen(conv_w, prec)), _p(cs), _p(st), _p(widen(alpha, prec)),
       _p(widen(beta, prec)), _p(widen(z, prec)), _p(widen(norm_w, prec)), _p(_i32(slot_idx)),
       ctypes.c_int(B), ctypes.c_int(Tn), ctypes.c_int(Hk), ctypes.c_int(Hv),
-      _c_t(prec)(q_scale), _c_t(prec)(eps), ctypes.c_int(int(round_act)),
+      _c_t(prec)(q_scale), _c_t(prec)(eps), ctypes.c_int(int(round_act)), ctypes.c_int(int(act32)),
       ctypes.c_int(int(commit_all)), _p(out), _p(pc), _p(raw))
     return (out, pc, cs, st, raw) if want_raw else (out, pc, cs, st)
 
 
 def commit(x, alpha, beta, conv_w, conv_state, state, slot_idx, n_keep, Hk, Hv, *,
-           eps=1e-6, round_act=True, prec="f64"):
+           eps=1e-6, round_act=True, prec="f64", act32=False):
     """Commit the accepted prefix n_keep[b] of one layer. Returns (conv_state', state')."""
     xw = widen(x, prec)
     B, Tn, C = xw.shape
@@ -207,5 +219,6 @@ def commit(x, alpha, beta, conv_w, conv_state, state, slot_idx, n_keep, Hk, Hv, 
     f.restype = None
     f(_p(xw), _p(widen(alpha, prec)), _p(widen(beta, prec)), _p(widen(conv_w, prec)), _p(cs),
       _p(st), _p(_i32(slot_idx)), _p(_i32(n_keep)), ctypes.c_int(B), ctypes.c_int(Tn),
-      ctypes.c_int(Hk), ctypes.c_int(Hv), _c_t(prec)(eps), ctypes.c_int(int(round_act)))
+      ctypes.c_int(Hk), ctypes.c_int(Hv), _c_t(prec)(eps), ctypes.c_int(int(round_act)),
+      ctypes.c_int(int(act32)))
     return cs, st

@@ -42,6 +42,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 #include <vector>
 
 namespace {
@@ -64,7 +65,35 @@ template <class T> T round_bf16(T v) {
   return std::ldexp(r, e - 8);
 }
 
-template <class T> T silu(T y) { return y / (T(1) + std::exp(-y)); }
+// exp of the float instantiation, by a published scheme whose every step is a
+// correctly rounded IEEE operation, so that it is reproducible bit for bit on
+// any IEEE machine: Cody & Waite's reduction x = n ln2 + r with ln 2 split in
+// a 16-bit high part (n * hi exact) and a low part, then the degree-7 Taylor
+// polynomial of e^r in Horner form (|r| <= ln2/2: truncation < 0.1 ulp), then
+// scaling by 2^n. The argument is first clamped to [-87, 88], which keeps
+// 2^n a normal number (SiLU saturates long before: for |y| > 87 it is y or
+// about -0). The double instantiation uses the library exp. Both are pinned
+// against the library exp.
+inline float exp_cw(float x) {
+  x = std::fmin(std::fmax(x, -87.0f), 88.0f);
+  const float n = std::nearbyint(x * 1.44269504088896341f);      // log2(e)
+  float r = std::fma(-n, 0.693145751953125f, x);                   // ln2 high part
+  r = std::fma(-n, 1.42860682030941723212e-6f, r);                 // ln2 low part
+  float p = 1.0f / 5040.0f;
+  p = std::fma(p, r, 1.0f / 720.0f);
+  p = std::fma(p, r, 1.0f / 120.0f);
+  p = std::fma(p, r, 1.0f / 24.0f);
+  p = std::fma(p, r, 1.0f / 6.0f);
+  p = std::fma(p, r, 0.5f);
+  p = std::fma(p, r, 1.0f);
+  p = std::fma(p, r, 1.0f);
+  return p * std::ldexp(1.0f, (int)n);
+}
+
+template <class T> T exp_t(T x) { return std::exp(x); }
+template <> inline float exp_t<float>(float x) { return exp_cw(x); }
+
+template <class T> T silu(T y) { return y / (T(1) + exp_t(-y)); }
 
 // The canonical sum-of-squares tree over 128 values: 16 groups of 8
 // contiguous channels; inside a group the strides 4, 2, 1 are folded, then the
@@ -107,12 +136,13 @@ struct Geo {
 };
 
 // Causal depthwise conv of one channel's padded column xp (3 state rows then
-// the tokens): y[t] = sum_j w[j] * xp[t + j], accumulated in tap order.
+// the tokens): y[t] = sum_j w[j] * xp[t + j], accumulated in tap order with
+// fused multiply-adds (one rounding per tap).
 template <class T> T conv_tap(const T* w, const T* xp_t) {
   T acc = w[0] * xp_t[0];
-  acc = acc + w[1] * xp_t[1];
-  acc = acc + w[2] * xp_t[2];
-  acc = acc + w[3] * xp_t[3];
+  acc = std::fma(w[1], xp_t[1], acc);
+  acc = std::fma(w[2], xp_t[2], acc);
+  acc = std::fma(w[3], xp_t[3], acc);
   return acc;
 }
 
@@ -325,12 +355,22 @@ void prefill(const T* qkv, const T* alpha, const T* beta, const T* z, const T* n
 // Post-conv activations of T draft tokens of batch entry b from its
 // conv_state, rounded to the activation type when round_act (they are stored
 // activations in every phase).
+// act32: compute the activations with the float instantiation (the order the
+// GPU follows bit for bit) and widen them, whatever T is.
 template <class T>
 void draft_activations(const Geo& g, const T* xb, int Tn, const T* w, const T* st, T eps,
-                       int round_act, T* qkv) {
+                       int round_act, int act32, T* qkv) {
+  const int64_t n = (int64_t)Tn * g.C;
+  if (act32 && !std::is_same<T, float>::value) {
+    std::vector<float> xf(xb, xb + n), wf(w, w + (int64_t)g.C * KW), sf(st, st + (int64_t)KS * g.C);
+    std::vector<float> yf(n);
+    conv_block<float>(g, xf.data(), Tn, wf.data(), sf.data(), 1, 1, (float)eps, yf.data());
+    for (int64_t i = 0; i < n; ++i) qkv[i] = (T)(round_act ? round_bf16(yf[i]) : yf[i]);
+    return;
+  }
   conv_block(g, xb, Tn, w, st, 1, 1, eps, qkv);
   if (round_act)
-    for (int64_t i = 0; i < (int64_t)Tn * g.C; ++i) qkv[i] = round_bf16(qkv[i]);
+    for (int64_t i = 0; i < n; ++i) qkv[i] = round_bf16(qkv[i]);
 }
 
 // [P3 "Summary"; DEF] speculative verify of T draft tokens per batch entry:
@@ -339,7 +379,8 @@ void draft_activations(const Geo& g, const T* xb, int Tn, const T* w, const T* s
 template <class T>
 void verify(const T* x, const T* w, T* conv_state, T* state, const T* alpha, const T* beta,
             const T* z, const T* norm_w, const int32_t* slot_idx, int B, int Tn, int Hk, int Hv,
-            T q_scale, T eps, int round_act, int commit_all, T* out, T* postconv, T* o_raw) {
+            T q_scale, T eps, int round_act, int act32, int commit_all, T* out, T* postconv,
+            T* o_raw) {
   Geo g(Hk, Hv);
   const int64_t HvD = (int64_t)Hv * D, SS = (int64_t)Hv * D * D;
   std::vector<T> qkv((size_t)Tn * g.C), S(SS), tail((size_t)KS * g.C);
@@ -348,7 +389,7 @@ void verify(const T* x, const T* w, T* conv_state, T* state, const T* alpha, con
     if (slot < 0) continue;
     const T* xb = x + (int64_t)b * Tn * g.C;
     T* st = conv_state + (int64_t)slot * KS * g.C;
-    draft_activations(g, xb, Tn, w, st, eps, round_act, qkv.data());
+    draft_activations(g, xb, Tn, w, st, eps, round_act, act32, qkv.data());
     if (postconv) std::memcpy(postconv + (int64_t)b * Tn * g.C, qkv.data(), sizeof(T) * qkv.size());
     std::memcpy(S.data(), state + slot * SS, sizeof(T) * SS);
     recurrence_seq(g, qkv.data(), alpha + (int64_t)b * Tn * Hv, beta + (int64_t)b * Tn * Hv,
@@ -370,7 +411,7 @@ void verify(const T* x, const T* w, T* conv_state, T* state, const T* alpha, con
 template <class T>
 void commit(const T* x, const T* alpha, const T* beta, const T* w, T* conv_state, T* state,
             const int32_t* slot_idx, const int32_t* n_keep, int B, int Tn, int Hk, int Hv,
-            T eps, int round_act) {
+            T eps, int round_act, int act32) {
   Geo g(Hk, Hv);
   const int64_t SS = (int64_t)Hv * D * D;
   std::vector<T> qkv((size_t)Tn * g.C), S(SS), tail((size_t)KS * g.C);
@@ -380,7 +421,7 @@ void commit(const T* x, const T* alpha, const T* beta, const T* w, T* conv_state
     if (slot < 0 || n <= 0 || n > Tn) continue;
     const T* xb = x + (int64_t)b * Tn * g.C;
     T* st = conv_state + (int64_t)slot * KS * g.C;
-    draft_activations(g, xb, n, w, st, eps, round_act, qkv.data());
+    draft_activations(g, xb, n, w, st, eps, round_act, act32, qkv.data());
     std::memcpy(S.data(), state + slot * SS, sizeof(T) * SS);
     recurrence_seq<T>(g, qkv.data(), alpha + (int64_t)b * Tn * Hv, beta + (int64_t)b * Tn * Hv,
                       nullptr, nullptr, S.data(), n, T(1), eps, nullptr, nullptr);
@@ -409,6 +450,9 @@ void commit(const T* x, const T* alpha, const T* beta, const T* w, T* conv_state
                                                 T* out) {                                       \
     gated_rmsnorm(o, z, w, eps, out);                                                           \
   }                                                                                             \
+  ORACLE_EXPORT void oracle_silu_##SUF(T* v, int64_t n) {                                       \
+    for (int64_t i = 0; i < n; ++i) v[i] = silu(v[i]);                                          \
+  }                                                                                             \
   ORACLE_EXPORT void oracle_round_bf16_##SUF(T* v, int64_t n) {                                 \
     for (int64_t i = 0; i < n; ++i) v[i] = round_bf16(v[i]);                                    \
   }                                                                                             \
@@ -421,16 +465,16 @@ void commit(const T* x, const T* alpha, const T* beta, const T* w, T* conv_state
   }                                                                                             \
   ORACLE_EXPORT void oracle_verify_##SUF(const T* x, const T* w, T* conv_state, T* state,      \
       const T* alpha, const T* beta, const T* z, const T* norm_w, const int32_t* slot_idx,      \
-      int B, int Tn, int Hk, int Hv, T q_scale, T eps, int round_act, int commit_all, T* out,   \
-      T* postconv, T* o_raw) {                                                                  \
+      int B, int Tn, int Hk, int Hv, T q_scale, T eps, int round_act, int act32, int commit_all, \
+      T* out, T* postconv, T* o_raw) {                                                          \
     verify<T>(x, w, conv_state, state, alpha, beta, z, norm_w, slot_idx, B, Tn, Hk, Hv,         \
-              q_scale, eps, round_act, commit_all, out, postconv, o_raw);                       \
+              q_scale, eps, round_act, act32, commit_all, out, postconv, o_raw);                \
   }                                                                                             \
   ORACLE_EXPORT void oracle_commit_##SUF(const T* x, const T* alpha, const T* beta,            \
       const T* w, T* conv_state, T* state, const int32_t* slot_idx, const int32_t* n_keep,      \
-      int B, int Tn, int Hk, int Hv, T eps, int round_act) {                                    \
+      int B, int Tn, int Hk, int Hv, T eps, int round_act, int act32) {                         \
     commit<T>(x, alpha, beta, w, conv_state, state, slot_idx, n_keep, B, Tn, Hk, Hv, eps,       \
-              round_act);                                                                       \
+              round_act, act32);                                                                \
   }
 
 ORACLE_INSTANTIATE(float, f32)

@@ -1,0 +1,113 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, exports every entry
+point include/gdn.h declares, and rejects bad arguments on the host before any
+CUDA call (so these run without a GPU: no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_deltanet_linear_12_gb300 import build, gdn
+    build.build()
+    return gdn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char\*)\s+(gdn_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 6
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in gdn.h but not exported"
+
+
+def test_status_strings(lib):
+    from gated_deltanet_linear_12_gb300 import gdn
+    assert gdn.status_string(0) == "ok"
+    assert "invalid" in gdn.status_string(1)
+    assert "unsupported" in gdn.status_string(2)
+
+
+def _cfg(**kw):
+    from gated_deltanet_linear_12_gb300 import gdn
+    c = gdn.GdnConfig(2, 4, 128, 4, gdn.GDN_BF16, 1e-6, 1.0, 8, None)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+# Fake, 16-byte aligned device addresses: validation rejects before any use.
+P = [0x7f0000000000 + i * 0x10000000 for i in range(16)]
+
+
+def _conv(lib, cfg, x=P[0], ldx=1024, y=P[1], ldy=1024, n_seq=2, n_tok=100):
+    return lib.gdn_conv_fwd(ctypes.byref(cfg) if cfg is not None else None, x, ldx, y, ldy, P[2],
+                            P[3], P[4], P[5], P[6], n_seq, n_tok, 1, None)
+
+
+def test_conv_host_validation(lib):
+    assert _conv(lib, None) == 1
+    assert _conv(lib, _cfg(head_dim=64)) == 2
+    assert _conv(lib, _cfg(conv_width=3)) == 2
+    assert _conv(lib, _cfg(act=7)) == 2
+    assert _conv(lib, _cfg(n_v_heads=3)) == 1            # Hv % Hk != 0
+    assert _conv(lib, _cfg(n_qk_heads=1, n_v_heads=17)) == 2   # group too large
+    assert _conv(lib, _cfg(n_slots=0)) == 1
+    assert _conv(lib, _cfg(), x=0) == 1
+    assert _conv(lib, _cfg(), y=P[0]) == 1               # y overlaps x
+    assert _conv(lib, _cfg(), x=P[0] + 8) == 1           # misaligned
+    assert _conv(lib, _cfg(), ldx=1000) == 1             # ld < C
+    assert _conv(lib, _cfg(), ldx=1028) == 1             # row not 16-byte aligned
+    assert _conv(lib, _cfg(), n_seq=-1) == 1
+    assert _conv(lib, _cfg(), n_seq=0) == 0              # empty batch: no-op
+
+
+def test_postconv_norm_host_validation(lib):
+    c = _cfg()
+    assert lib.gdn_postconv_norm(ctypes.byref(c), 3, P[0], 1, P[1], 10, None) == 2
+    assert lib.gdn_postconv_norm(ctypes.byref(c), 1, P[0], 1, P[0] + 64, 10, None) == 1
+    assert lib.gdn_postconv_norm(ctypes.byref(c), 1, P[0], 1, P[1], 0, None) == 0
+    assert lib.gdn_postconv_norm(ctypes.byref(c), 1, 0, 1, P[1], 5, None) == 1
+
+
+def test_prefill_host_validation(lib):
+    c = _cfg()
+    args = [P[i] for i in range(10)]
+    assert lib.gdn_delta_prefill(ctypes.byref(c), *args, 2, 100, 32, None) == 2   # chunk
+    assert lib.gdn_delta_prefill(ctypes.byref(c), *args, 0, 100, 64, None) == 0
+    bad = list(args)
+    bad[5] = P[0]                                          # out aliases qkv
+    assert lib.gdn_delta_prefill(ctypes.byref(c), *bad, 2, 100, 64, None) == 1
+    bad = list(args)
+    bad[6] = 0                                             # state null
+    assert lib.gdn_delta_prefill(ctypes.byref(c), *bad, 2, 100, 64, None) == 1
+
+
+def test_verify_and_commit_host_validation(lib):
+    c = _cfg()
+    v = [P[i] for i in range(10)]
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 9, 0, None, None) == 1   # T > 8
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 0, 0, None, None) == 1   # T < 1
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 2, 4, None, None) == 1   # bad flag
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 0, 2, 0, None, None) == 0   # B = 0
+    assert lib.gdn_commit_layers(ctypes.byref(c), P[0], 36, P[1], P[2], 4, 0, None) == 1
+    assert lib.gdn_commit_layers(ctypes.byref(c), 0, 36, P[1], P[2], 4, 2, None) == 1
+    assert lib.gdn_commit_layers(ctypes.byref(c), P[0], 0, P[1], P[2], 4, 2, None) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    from gated_deltanet_linear_12_gb300 import gdn
+    cfg = gdn.make_config(1, 1, torch.float32, 1)
+    t = torch.zeros(4, 384)
+    with pytest.raises(ValueError):
+        gdn.gdn_postconv_norm(cfg, t, t)

@@ -1,0 +1,202 @@
+"""GPU parity of speculative verify, decode (verify with every token accepted)
+and the batched accepted-prefix commit, against the CPU oracle and against
+each other (bitwise), through the C ABI."""
+import numpy as np
+import pytest
+
+from gated_deltanet_linear_12_gb300 import synthetic as syn
+from tests.helpers import bits, check_bf16, check_f32_out, check_states, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def G():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_deltanet_linear_12_gb300 import gdn
+    gdn.load()
+    return gdn
+
+
+class Layer:
+    """Device copies of one layer's verify inputs and pools."""
+
+    def __init__(self, inp):
+        self.inp = inp
+        self.act = torch.bfloat16 if inp["act"] == "bf16" else torch.float32
+        self.x = to_dev(inp["x"])
+        self.conv_w = to_dev(inp["conv_w"])
+        self.cs = to_dev(inp["conv_state"])
+        self.S = to_dev(inp["state"])
+        self.alpha = to_dev(inp["alpha"])
+        self.beta = to_dev(inp["beta"])
+        self.z = to_dev(inp["z"])
+        self.norm_w = to_dev(inp["norm_w"])
+        self.slot = to_dev(inp["slot_idx"])
+        B, T, Hv = inp["B"], inp["T"], inp["Hv"]
+        self.out = torch.zeros(B, T, Hv * 128, dtype=self.act, device="cuda")
+        self.pc = torch.zeros(B, T, inp["C"], dtype=self.act, device="cuda")
+
+    def cfg(self, G, dev_err=None):
+        return G.make_config(self.inp["Hk"], self.inp["Hv"], self.act, self.S.shape[0],
+                             dev_err=dev_err)
+
+    def verify(self, G, commit_all=False, dev_err=None):
+        G.gdn_verify_step(self.cfg(G, dev_err), self.x, self.conv_w, self.cs, self.S, self.alpha,
+                          self.beta, self.z, self.norm_w, self.out, self.slot,
+                          commit_all=commit_all, postconv_out=self.pc)
+
+    def view(self):
+        return dict(x=self.x, alpha=self.alpha, beta=self.beta, conv_w=self.conv_w,
+                    conv_state=self.cs, state=self.S)
+
+
+def _oracle_verify(orc, inp, commit_all=False):
+    """Oracle verify: activations in the float order (bitwise the GPU's), the
+    recurrence and norm in double."""
+    return orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"], inp["alpha"],
+                      inp["beta"], inp["z"], inp["norm_w"], inp["slot_idx"], inp["Hk"], inp["Hv"],
+                      round_act=inp["act"] == "bf16", commit_all=commit_all, act32=True)
+
+
+def _act_bits(pc, act):
+    pc = np.asarray(pc, np.float32)
+    return syn.f32_to_bf16_bits(pc).view(np.int16) if act == "bf16" else pc.view(np.int32)
+
+
+def _used_slots(inp):
+    return [int(s) for s in inp["slot_idx"] if s >= 0]
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
+def test_verify_bf16(G, orc, T):
+    inp = syn.verify_inputs(6, T, 2, 4, "bf16", seed=200 + T, pad_slots=1)
+    L = Layer(inp)
+    L.verify(G)
+    torch.cuda.synchronize()
+    out, pc, cs, st = _oracle_verify(orc, inp)
+    check_bf16(to_np(L.out), out, what=f"verify out T={T}")
+    assert np.array_equal(bits(L.pc)[:5], _act_bits(pc[:5], "bf16")), "post-conv bitwise"
+    # verify is read-only
+    assert np.array_equal(bits(L.cs), inp["conv_state"].view(np.int16))
+    assert np.array_equal(bits(L.S), inp["state"].view(np.int32))
+    assert np.all(to_np(L.out)[5] == 0), "padding entry must not be written"
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_verify_f32_arm(G, orc, T):
+    inp = syn.verify_inputs(3, T, 1, 2, "f32", seed=210 + T)
+    L = Layer(inp)
+    L.verify(G)
+    torch.cuda.synchronize()
+    out, pc, _, _ = _oracle_verify(orc, inp)
+    check_f32_out(to_np(L.out), out, 1e-4, "verify f32 out")
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_commit_all_equals_verify_then_commit_bitwise(G, orc, T):
+    inp = syn.verify_inputs(5, T, 2, 4, "bf16", seed=220 + T)
+    A = Layer(inp)
+    A.verify(G, commit_all=True)
+    Bl = Layer(inp)
+    Bl.verify(G)
+    views = G.make_layer_views([Bl.view()], "cuda")
+    n_keep = torch.full((5,), T, dtype=torch.int32, device="cuda")
+    G.gdn_commit_layers(Bl.cfg(G), views, 1, Bl.slot, n_keep, T)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(A.out), bits(Bl.out))
+    assert np.array_equal(bits(A.S), bits(Bl.S))
+    assert np.array_equal(bits(A.cs), bits(Bl.cs))
+    # and against the oracle
+    out, _, cs, st = _oracle_verify(orc, inp, commit_all=True)
+    check_bf16(to_np(A.out), out, what="decode out")
+    assert np.array_equal(to_np(A.cs), cs), "conv_state commit must be bit-exact"
+    check_states(to_np(A.S), st, range(st.shape[0]), 1e-4, "decode state")
+
+
+@pytest.mark.parametrize("T", [2, 5, 8])
+def test_commit_layers_against_oracle_and_per_layer(G, orc, T):
+    nl = 3
+    inps = [syn.verify_inputs(7, T, 2, 4, "bf16", seed=300 + 10 * T + l) for l in range(nl)]
+    n_keep = syn.verify_inputs(7, T, 2, 4, "bf16", seed=399)["n_keep"]
+    n_keep[0], n_keep[1] = 0, T                     # both ends always present
+    for inp in inps:
+        inp["n_keep"] = n_keep
+        inp["slot_idx"] = inps[0]["slot_idx"]
+    batched = [Layer(i) for i in inps]
+    single = [Layer(i) for i in inps]
+    nk = to_dev(n_keep)
+    views = G.make_layer_views([l.view() for l in batched], "cuda")
+    G.gdn_commit_layers(batched[0].cfg(G), views, nl, batched[0].slot, nk, T)
+    for l in single:
+        v1 = G.make_layer_views([l.view()], "cuda")
+        G.gdn_commit_layers(l.cfg(G), v1, 1, l.slot, nk, T)
+        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    for lb, ls, inp in zip(batched, single, inps):
+        assert np.array_equal(bits(lb.S), bits(ls.S)), "batched == per-layer commit (bitwise)"
+        assert np.array_equal(bits(lb.cs), bits(ls.cs))
+        cs, st = orc.commit(inp["x"], inp["alpha"], inp["beta"], inp["conv_w"], inp["conv_state"],
+                            inp["state"], inp["slot_idx"], n_keep, 2, 4, act32=True)
+        assert np.array_equal(to_np(lb.cs), cs), "conv_state commit must be bit-exact"
+        check_states(to_np(lb.S), st, range(st.shape[0]), 1e-4, "committed state")
+        # slots with n_keep == 0 and slots nobody references stay bitwise untouched
+        keep0 = [int(inp["slot_idx"][b]) for b in range(7) if n_keep[b] == 0]
+        unused = sorted(set(range(inp["state"].shape[0])) - set(int(s) for s in inp["slot_idx"]))
+        for sl in keep0 + unused:
+            assert np.array_equal(bits(lb.S)[sl], inp["state"][sl].view(np.int32))
+            assert np.array_equal(bits(lb.cs)[sl], inp["conv_state"][sl].view(np.int16))
+
+
+def test_commit_bad_n_keep_and_slot_flag_errors(G):
+    T = 4
+    inp = syn.verify_inputs(4, T, 1, 2, "bf16", seed=410)
+    L = Layer(inp)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n_keep = torch.tensor([T + 1, 2, -1, 1], dtype=torch.int32, device="cuda")
+    slots = inp["slot_idx"].copy()
+    slots[3] = inp["state"].shape[0] + 7
+    L.slot = to_dev(slots)
+    views = G.make_layer_views([L.view()], "cuda")
+    G.gdn_commit_layers(L.cfg(G, err), views, 1, L.slot, n_keep, T)
+    torch.cuda.synchronize()
+    e = int(err.item())
+    assert e & G.GDN_DEVERR_NKEEP and e & G.GDN_DEVERR_SLOT
+    S = bits(L.S)
+    for b in (0, 2):                                  # skipped entries untouched
+        sl = slots[b]
+        assert np.array_equal(S[sl], inp["state"][sl].view(np.int32))
+    assert not np.array_equal(S[slots[1]], inp["state"][slots[1]].view(np.int32))
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_verify_group_of_three_v_heads(G, orc, T):
+    """Hv/Hk = 3 (the 48-over-16 grouping of a larger model)."""
+    inp = syn.verify_inputs(3, T, 2, 6, "bf16", seed=420 + T)
+    L = Layer(inp)
+    L.verify(G, commit_all=True)
+    torch.cuda.synchronize()
+    out, _, cs, st = _oracle_verify(orc, inp, commit_all=True)
+    check_bf16(to_np(L.out), out, what="verify G=3")
+    assert np.array_equal(to_np(L.cs), cs)
+    check_states(to_np(L.S), st, _used_slots(inp), 1e-4, "state G=3")
+
+
+def test_verify_postconv_matches_conv_fwd_bitwise(G):
+    """The activations verify uses equal gdn_conv_fwd's on the same rows."""
+    T = 6
+    inp = syn.verify_inputs(2, T, 2, 4, "bf16", seed=430)
+    L = Layer(inp)
+    L.verify(G)
+    C = inp["C"]
+    x = L.x.reshape(2 * T, C)
+    y = torch.empty_like(x)
+    cs = to_dev(inp["conv_state"])
+    cu = torch.tensor([0, T, 2 * T], dtype=torch.int32, device="cuda")
+    hi = torch.ones(2, dtype=torch.uint8, device="cuda")
+    G.gdn_conv_fwd(L.cfg(G), x, y, L.conv_w, cs, L.slot, cu, hi)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(y), bits(L.pc.reshape(2 * T, C)))

@@ -4,7 +4,9 @@ Each test fixes one part of the oracle to something other than itself, so
 that a plausible slip (a dropped term, a wrong sign or index, a transposed
 operand, a changed reduction order) fails at least one of them:
 
-  P1  conv = explicit 4-term sums; has_init=0 = zero-padded np.convolve
+  P1  conv = exact 4-term sums (rational arithmetic) within 4 roundings;
+      has_init=0 = zero-padded np.convolve; SiLU = y / (1 + e^-y), the f32 exp
+      scheme within 2 ulp of the library exp
   P2  delta conv weights: pass-through of the current token and a 3-row shift
       that reads the conv_state (pins tap orientation and state row order)
   P3  L2 norm: unit norm, tree sum within the pairwise bound of the exact sum,
@@ -20,6 +22,7 @@ operand, a changed reduction order) fails at least one of them:
   BF  bfloat16 rounding against torch's conversion
 """
 import math
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -48,11 +51,11 @@ def test_p1_conv_explicit_sums(orc):
         for c in range(0, inp["C"], 37):
             col = [prev[0, c], prev[1, c], prev[2, c]] + [x[t0 + t, c] for t in range(n)]
             for t in range(n):
-                want = w[c, 0] * col[t]
-                want = want + w[c, 1] * col[t + 1]
-                want = want + w[c, 2] * col[t + 2]
-                want = want + w[c, 3] * col[t + 3]
-                assert y[t0 + t, c] == want
+                terms = [Fraction(float(w[c, j])) * Fraction(float(col[t + j])) for j in range(4)]
+                exact = sum(terms)
+                # one rounded product and three fused multiply-adds: 4 roundings
+                bound = 4 * 2.0 ** -53 * float(sum(abs(v) for v in terms))
+                assert abs(Fraction(float(y[t0 + t, c])) - exact) <= Fraction(bound)
             # committed state = last three rows of the padded column
             assert [st[slot, r, c] for r in range(3)] == col[n:n + 3]
 
@@ -78,6 +81,20 @@ def test_p1_silu_applied_after_conv(orc):
     post, _ = orc.conv_fwd(*args, silu=True, l2norm=False)
     want = np.vectorize(lambda a: a / (1.0 + math.exp(-a)))(pre)
     np.testing.assert_allclose(post, want, rtol=1e-15, atol=0)
+
+
+def test_p1_f32_exp_scheme_within_two_ulp(orc):
+    """The float instantiation's exp (Cody-Waite + Taylor) against math.exp."""
+    xs = np.concatenate([np.linspace(-87.0, 88.0, 200001, dtype=np.float32),
+                         np.float32([0.0, -0.0, 1e-8, -1e-8, 0.34657359, -0.34657359])])
+    ys = np.float32(-xs)                       # silu(y) uses exp(-y)
+    got = orc.silu(ys, prec="f32").astype(np.float64)
+    for y, g in zip(ys[::97].astype(np.float64), got[::97]):
+        e = math.exp(-y)
+        want = y / (1.0 + e)
+        ulp = np.spacing(np.float32(abs(want))) if want != 0 else 2.0 ** -149
+        # exp within 2 ulp, then a rounded add and divide: 4 ulp of the result
+        assert abs(g - want) <= 4 * float(ulp), (y, g, want)
 
 
 # ------------------------------------------------------------------ P2
