@@ -88,24 +88,32 @@ __device__ __forceinline__ float2 conv4x2(float2 w0, float2 w1, float2 w2, float
   return acc;
 }
 
-// e^x with x clamped to [-87, 88], by Cody & Waite's reduction x = n ln2 + r
-// (ln 2 split in a 16-bit high part, so n * high is exact, and a low part)
-// and the degree-7 Taylor polynomial of e^r in Horner form, then scaling by
-// 2^n. Every step is one correctly rounded IEEE operation, so any IEEE
-// machine that follows the same steps gets the same bits: the post-conv
-// activations, and hence their rounding to bf16, are reproducible. n is
-// nearbyint(x * log2 e), obtained by adding and subtracting 1.5 * 2^23 (the
-// add rounds to an integer); 2^n is built from the integer in t's low bits.
-// Two values per call, with Blackwell's paired f32 instructions.
-__device__ __forceinline__ float2 exp_cw2(float2 x) {
+// SiLU, two values at a time with Blackwell's paired f32 instructions, by
+// published schemes made only of correctly rounded IEEE operations, so the
+// result is reproducible bit for bit by any IEEE implementation of the same
+// steps (the post-conv activations then round to the same bf16 values
+// everywhere):
+//   t = e^-|y|: Cody & Waite's reduction -|y| = n ln2 + r (ln 2 split in a
+//     16-bit high part, so n * high is exact, and a low part; the argument
+//     clamped at -87 keeps 2^n normal), degree-7 Taylor polynomial of e^r in
+//     Horner form, scaled by 2^n. n, the nearest integer to the exact
+//     a log2 e, comes from one fused multiply-add with 1.5 * 2^23 (which
+//     rounds to an integer) and an exact subtraction; 2^n is built from the
+//     integer left in the low bits of the sum;
+//   (Each multiply whose result feeds a single add is written as an explicit
+//   fused multiply-add, on both sides: the compiler is otherwise free to fuse
+//   paired f32 multiplies into the next add, which changes the rounding.)
+//   s = 1/(1 + t), d in [1, 2]: Newton-Raphson from 24/17 - 8/17 d (relative
+//     error <= 1/17), three steps x <- x + x (1 - d x);
+//   sigmoid = s (y >= 0) or t s (y < 0);  silu = y sigmoid.
+__device__ __forceinline__ float2 silu2(float2 y) {
   constexpr float kMagic = 12582912.0f;                 // 1.5 * 2^23
-  x.x = fminf(fmaxf(x.x, -87.0f), 88.0f);
-  x.y = fminf(fmaxf(x.y, -87.0f), 88.0f);
-  const float2 t = __fadd2_rn(__fmul2_rn(x, make_float2(1.44269504088896341f, 1.44269504088896341f)),
-                              make_float2(kMagic, kMagic));
-  const float2 n = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
+  constexpr float kLog2e = 1.44269504088896341f;
+  const float2 a = make_float2(fmaxf(-fabsf(y.x), -87.0f), fmaxf(-fabsf(y.y), -87.0f));
+  const float2 tt = __ffma2_rn(a, make_float2(kLog2e, kLog2e), make_float2(kMagic, kMagic));
+  const float2 n = __fadd2_rn(tt, make_float2(-kMagic, -kMagic));
   const float2 mn = make_float2(-n.x, -n.y);
-  float2 r = __ffma2_rn(mn, make_float2(0.693145751953125f, 0.693145751953125f), x);
+  float2 r = __ffma2_rn(mn, make_float2(0.693145751953125f, 0.693145751953125f), a);
   r = __ffma2_rn(mn, make_float2(1.42860682030941723212e-6f, 1.42860682030941723212e-6f), r);
   float2 p = make_float2(1.0f / 5040.0f, 1.0f / 5040.0f);
   p = __ffma2_rn(p, r, make_float2(1.0f / 720.0f, 1.0f / 720.0f));
@@ -115,16 +123,21 @@ __device__ __forceinline__ float2 exp_cw2(float2 x) {
   p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
   p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
   p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
-  // 2^n: n sits in the low mantissa bits of t; (bits << 23) + bias is 2^n's pattern
-  const float2 sc = make_float2(__int_as_float((__float_as_int(t.x) << 23) + 0x3f800000),
-                                __int_as_float((__float_as_int(t.y) << 23) + 0x3f800000));
-  return __fmul2_rn(p, sc);
-}
-
-// SiLU y / (1 + e^-y) with the exp above and an IEEE divide, two at a time.
-__device__ __forceinline__ float2 silu2(float2 y) {
-  const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), exp_cw2(make_float2(-y.x, -y.y)));
-  return make_float2(__fdiv_rn(y.x, d.x), __fdiv_rn(y.y, d.y));
+  const float2 sc = make_float2(__int_as_float((__float_as_int(tt.x) << 23) + 0x3f800000),
+                                __int_as_float((__float_as_int(tt.y) << 23) + 0x3f800000));
+  const float2 t = __fmul2_rn(p, sc);                   // e^-|y|
+  const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), t);
+  const float2 md = make_float2(-d.x, -d.y);
+  float2 x = __ffma2_rn(make_float2(-8.0f / 17.0f, -8.0f / 17.0f), d,
+                        make_float2(24.0f / 17.0f, 24.0f / 17.0f));
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const float2 e = __ffma2_rn(md, x, make_float2(1.0f, 1.0f));
+    x = __ffma2_rn(x, e, x);
+  }
+  const float2 ts = __fmul2_rn(t, x);
+  const float2 sig = make_float2(y.x >= 0.0f ? x.x : ts.x, y.y >= 0.0f ? x.y : ts.y);
+  return __fmul2_rn(y, sig);
 }
 
 __device__ __forceinline__ float silu(float y) { return silu2(make_float2(y, 0.f)).x; }
@@ -133,15 +146,16 @@ __device__ __forceinline__ float silu(float y) { return silu2(make_float2(y, 0.f
 // of 16 consecutive lanes (lane & 15 = channel group). In-lane: strides 4, 2, 1;
 // across lanes: xor 8, 4, 2, 1, which gives every lane the same bits because
 // float addition is commutative. Must be called by all 32 lanes of the warp.
+// Scalar __fmul_rn / __fadd_rn: these are never merged into multiply-adds,
+// so each square is rounded before it is summed (paired f32 multiplies have
+// been seen fused into the following paired add).
 __device__ __forceinline__ float head_sum_sq16(const float v[8]) {
-  const float2 e01 = __fmul2_rn(make_float2(v[0], v[1]), make_float2(v[0], v[1]));
-  const float2 e23 = __fmul2_rn(make_float2(v[2], v[3]), make_float2(v[2], v[3]));
-  const float2 e45 = __fmul2_rn(make_float2(v[4], v[5]), make_float2(v[4], v[5]));
-  const float2 e67 = __fmul2_rn(make_float2(v[6], v[7]), make_float2(v[6], v[7]));
-  const float2 p01 = __fadd2_rn(e01, e45);          // e0+e4, e1+e5
-  const float2 p23 = __fadd2_rn(e23, e67);          // e2+e6, e3+e7
-  const float2 q = __fadd2_rn(p01, p23);            // (p0+p2), (p1+p3)
-  float g = __fadd_rn(q.x, q.y);
+  float e[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) e[j] = __fmul_rn(v[j], v[j]);
+  const float p0 = __fadd_rn(e[0], e[4]), p1 = __fadd_rn(e[1], e[5]);
+  const float p2 = __fadd_rn(e[2], e[6]), p3 = __fadd_rn(e[3], e[7]);
+  float g = __fadd_rn(__fadd_rn(p0, p2), __fadd_rn(p1, p3));
 #pragma unroll
   for (int m = 8; m >= 1; m >>= 1) g = __fadd_rn(g, __shfl_xor_sync(FULL, g, m));
   return g;

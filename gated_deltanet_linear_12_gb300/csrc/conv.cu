@@ -23,7 +23,7 @@ constexpr int CONV_THREADS = 256;
 constexpr int CONV_QUARTERS = 4;                      // token quarters of a chunk
 constexpr int CONV_TOK = CHUNK / CONV_QUARTERS;       // 16 tokens per thread
 constexpr int CONV_HEADS_PER_BLOCK = 4;               // 4 heads x 16 lanes x 4 quarters
-constexpr int CONV_BATCH = 2;                         // tokens loaded ahead per step
+constexpr int CONV_BATCH = 4;                         // tokens loaded ahead per step
 
 // Thread layout: warp w covers quarter w / 2 of the chunk and heads
 // 2 (w % 2), 2 (w % 2) + 1 of the block's 4 heads (16 lanes each, 8 contiguous
@@ -104,11 +104,16 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
       }
     }
 
-    for (int64_t t = t_begin; t < t_stop; t += CONV_BATCH) {
+    // 16 tokens, fully unrolled so the three-row window rotates through
+    // registers; loads run CONV_BATCH tokens ahead of the arithmetic.
+    const int n_here = (int)(t_stop - t_begin);           // 1..16, uniform per warp
+#pragma unroll
+    for (int b0 = 0; b0 < CONV_TOK; b0 += CONV_BATCH) {
+      if (b0 >= n_here) break;
       float xv[CONV_BATCH][8];
 #pragma unroll
       for (int u = 0; u < CONV_BATCH; ++u) {
-        if (active && t + u < t_stop) load8<A>(x, (t + u) * ld_x + c0, xv[u]);
+        if (active && b0 + u < n_here) load8<A>(x, (t_begin + b0 + u) * ld_x + c0, xv[u]);
         else {
 #pragma unroll
           for (int j = 0; j < 8; ++j) xv[u][j] = 0.f;
@@ -116,7 +121,7 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
       }
 #pragma unroll
       for (int u = 0; u < CONV_BATCH; ++u) {
-        if (t + u >= t_stop) break;                       // uniform per warp
+        if (b0 + u >= n_here) break;
         float v[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -138,7 +143,7 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
             }
           }
         }
-        if (active) store8<A>(y, (t + u) * ld_y + c0, v);
+        if (active) store8<A>(y, (t_begin + b0 + u) * ld_y + c0, v);
       }
     }
   }

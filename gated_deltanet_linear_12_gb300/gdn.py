@@ -23,7 +23,7 @@ GDN_DEVERR_SLOT, GDN_DEVERR_NKEEP, GDN_DEVERR_SEQLENS = 1, 2, 4
 HEAD_DIM, CONV_WIDTH, CHUNK, MAX_DRAFT = 128, 4, 64, 8
 
 EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_step",
-           "gdn_commit_layers", "gdn_status_string"]
+           "gdn_commit_layers", "gdn_selftest_tc_gemm", "gdn_status_string"]
 
 
 class GdnError(RuntimeError):
@@ -71,6 +71,7 @@ def load() -> ctypes.CDLL:
             L.gdn_verify_step.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                           u32, vp, vp]
             L.gdn_commit_layers.argtypes = [cfgp, vp, i32, vp, vp, i32, i32, vp]
+            L.gdn_selftest_tc_gemm.argtypes = [vp, vp, vp, i32, i32, vp, vp]
             for f in EXPORTS[:-1]:
                 getattr(L, f).restype = ctypes.c_int
             L.gdn_status_string.argtypes = [ctypes.c_int]
@@ -183,3 +184,10 @@ def gdn_commit_layers(cfg, views, n_layers, slot_idx, n_keep, T, *, stream=None)
     _check("gdn_commit_layers", load().gdn_commit_layers(
         ctypes.byref(cfg), _ptr(views), n_layers, _ptr(slot_idx), _ptr(n_keep), slot_idx.numel(),
         T, _stream(slot_idx, stream)))
+
+
+def gdn_selftest_tc_gemm(A, B, D, *, dev_err=None, stream=None):
+    """Diagnostic: D[128][N] = A[128][K] @ B[N][K]^T on the tensor cores (bf16 -> f32)."""
+    _dense(A, B, D)
+    _check("gdn_selftest_tc_gemm", load().gdn_selftest_tc_gemm(
+        _ptr(A), _ptr(B), _ptr(D), B.shape[0], A.shape[1], _ptr(dev_err), _stream(A, stream)))

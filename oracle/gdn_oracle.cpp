@@ -65,19 +65,28 @@ template <class T> T round_bf16(T v) {
   return std::ldexp(r, e - 8);
 }
 
-// exp of the float instantiation, by a published scheme whose every step is a
-// correctly rounded IEEE operation, so that it is reproducible bit for bit on
-// any IEEE machine: Cody & Waite's reduction x = n ln2 + r with ln 2 split in
-// a 16-bit high part (n * hi exact) and a low part, then the degree-7 Taylor
-// polynomial of e^r in Horner form (|r| <= ln2/2: truncation < 0.1 ulp), then
-// scaling by 2^n. The argument is first clamped to [-87, 88], which keeps
-// 2^n a normal number (SiLU saturates long before: for |y| > 87 it is y or
-// about -0). The double instantiation uses the library exp. Both are pinned
+// SiLU of the float instantiation, by published schemes whose every step is a
+// correctly rounded IEEE operation, so that any IEEE machine following the
+// same steps gets the same bits (this fixes how post-conv activations round to
+// bf16 on every implementation):
+//   t = e^-|y| : Cody & Waite's reduction -|y| = n ln2 + r (n the nearest
+//                integer to -|y| log2 e; ln 2 split in a 16-bit high part, so
+//                n * high is exact, and a low part; the argument clamped at
+//                -87 so 2^n stays normal), then the
+//                degree-7 Taylor polynomial of e^r in Horner form
+//                (|r| <= ln2/2: truncation < 0.1 ulp), scaled by 2^n;
+//   s = 1/(1 + t) on [1, 2] : Newton-Raphson from the linear start
+//                24/17 - 8/17 d (relative error <= 1/17), three iterations
+//                x <- x + x (1 - d x);
+//   sigmoid(y) = s for y >= 0, t s for y < 0;   silu(y) = y sigmoid(y).
+// The double instantiation is the plain y / (1 + exp(-y)). Both are pinned
 // against the library exp.
-inline float exp_cw(float x) {
-  x = std::fmin(std::fmax(x, -87.0f), 88.0f);
-  const float n = std::nearbyint(x * 1.44269504088896341f);      // log2(e)
-  float r = std::fma(-n, 0.693145751953125f, x);                   // ln2 high part
+inline float exp_neg_cw(float a) {          // e^a for a <= 0
+  a = std::fmax(a, -87.0f);
+  // n = nearbyint(a log2 e) of the exact product: one fused multiply-add with
+  // 1.5 * 2^23 rounds it to an integer, the subtraction is exact
+  const float n = std::fma(a, 1.44269504088896341f, 12582912.0f) - 12582912.0f;
+  float r = std::fma(-n, 0.693145751953125f, a);                   // ln2 high part
   r = std::fma(-n, 1.42860682030941723212e-6f, r);                 // ln2 low part
   float p = 1.0f / 5040.0f;
   p = std::fma(p, r, 1.0f / 720.0f);
@@ -90,10 +99,24 @@ inline float exp_cw(float x) {
   return p * std::ldexp(1.0f, (int)n);
 }
 
-template <class T> T exp_t(T x) { return std::exp(x); }
-template <> inline float exp_t<float>(float x) { return exp_cw(x); }
+inline float recip_12(float d) {            // 1/d for d in [1, 2]
+  float x = std::fma(-8.0f / 17.0f, d, 24.0f / 17.0f);
+  for (int i = 0; i < 3; ++i) {
+    const float e = std::fma(-d, x, 1.0f);
+    x = std::fma(x, e, x);
+  }
+  return x;
+}
 
-template <class T> T silu(T y) { return y / (T(1) + exp_t(-y)); }
+inline float silu_f32(float y) {
+  const float t = exp_neg_cw(-std::fabs(y));
+  const float s = recip_12(1.0f + t);
+  const float sig = y >= 0.0f ? s : t * s;
+  return y * sig;
+}
+
+template <class T> T silu(T y) { return y / (T(1) + std::exp(-y)); }
+template <> inline float silu<float>(float y) { return silu_f32(y); }
 
 // The canonical sum-of-squares tree over 128 values: 16 groups of 8
 // contiguous channels; inside a group the strides 4, 2, 1 are folded, then the

@@ -1,0 +1,40 @@
+"""The tensor-core building block (tcgen05.mma from shared memory into TMEM)
+against a host GEMM of the same bf16 operands."""
+import numpy as np
+import pytest
+
+from gated_deltanet_linear_12_gb300 import synthetic as syn
+from tests.helpers import to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def G():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_deltanet_linear_12_gb300 import gdn
+    gdn.load()
+    return gdn
+
+
+def _gemm(G, A, B):
+    D = torch.full((128, B.shape[0]), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G.gdn_selftest_tc_gemm(to_dev(A), to_dev(B), D, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "tensor-core completion wait timed out"
+    return D.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("N,K", [(16, 16), (64, 128), (128, 64), (256, 128)])
+def test_tc_gemm_matches_host(G, N, K):
+    rng = np.random.default_rng(N * 1000 + K)
+    A = syn.f32_to_bf16_bits(rng.standard_normal((128, K)).astype(np.float32))
+    B = syn.f32_to_bf16_bits(rng.standard_normal((N, K)).astype(np.float32))
+    ref = syn.bf16_bits_to_f32(A).astype(np.float64) @ syn.bf16_bits_to_f32(B).astype(np.float64).T
+    got = _gemm(G, A, B)
+    scale = np.abs(syn.bf16_bits_to_f32(A)).astype(np.float64) @ np.abs(syn.bf16_bits_to_f32(B)).astype(np.float64).T
+    assert np.all(np.abs(got - ref) <= 1e-5 * scale + 1e-30)

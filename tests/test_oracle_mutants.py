@@ -28,13 +28,15 @@ MUTANTS = {
                       "  acc = std::fma(w[1], xp_t[2], acc);\n  acc = std::fma(w[0], xp_t[3], acc);"),
     "exp_poly_term_dropped": ("  p = std::fma(p, r, 1.0f / 24.0f);\n", "  p = std::fma(p, r, 0.0f);\n"),
     "exp_ln2_low_dropped": ("  r = std::fma(-n, 1.42860682030941723212e-6f, r);", "  r = r;"),
+    "recip_two_iterations": ("  for (int i = 0; i < 3; ++i) {", "  for (int i = 0; i < 2; ++i) {"),
+    "sigmoid_branch_swapped": ("const float sig = y >= 0.0f ? s : t * s;", "const float sig = y >= 0.0f ? t * s : s;"),
     "tail_off_by_one": ("int64_t idx = n + r;", "int64_t idx = n + r - 1;"),
     "tree_adjacent_pairs": ("T p0 = e[0] + e[4], p1 = e[1] + e[5], p2 = e[2] + e[6], p3 = e[3] + e[7];",
                             "T p0 = e[0] + e[1], p1 = e[4] + e[5], p2 = e[2] + e[3], p3 = e[6] + e[7];"),
     "eps_outside_root": ("T r = T(1) / std::sqrt(ss + eps);", "T r = T(1) / (std::sqrt(ss) + eps);"),
     "rms_not_mean": ("T ms = tree_sum_sq(o) / T(D);", "T ms = tree_sum_sq(o);"),
-    "silu_sign": ("template <class T> T silu(T y) { return y / (T(1) + exp_t(-y)); }",
-                  "template <class T> T silu(T y) { return y / (T(1) + exp_t(y)); }"),
+    "silu_sign": ("template <class T> T silu(T y) { return y / (T(1) + std::exp(-y)); }",
+                  "template <class T> T silu(T y) { return y / (T(1) + std::exp(y)); }"),
     "grouping_interleaved": ("int qk_head(int h) const { return h / (Hv / Hk); }",
                              "int qk_head(int h) const { return h % Hk; }"),
     "chunk_decay_flipped": ("A[(size_t)t * chunk + s] = beta[(c0 + t) * g.Hv + h] * std::exp(G[t] - G[s])",
