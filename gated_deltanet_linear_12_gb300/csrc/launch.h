@@ -54,5 +54,6 @@ cudaError_t launch_postconv_norm(const gdn_config& cfg, int in_t, const void* yi
 cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, cudaStream_t stream);
 cudaError_t launch_commit(const StepArgs& a, int L, int act, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, int act, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
 
 }  // namespace gdn

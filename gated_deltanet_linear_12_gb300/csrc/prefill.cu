@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_ffma_kernel(PrefillArgs
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, int act, cudaStream_t stream) {
+  if (act == GDN_BF16) return launch_prefill_tc(a, stream);   // tensor-core path
   const size_t smem = prefill_smem_bytes();
   dim3 grid(a.Hv, a.n_seq);
   cudaError_t e;

@@ -1,0 +1,461 @@
+// Chunked (WY-form) gated delta rule over varlen sequences on the 5th-gen
+// tensor cores (bf16 activations), 64-token chunks, z-gated RMSNorm fused.
+//
+// Source: the rule S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T,
+// o_t = S_t q_t, and the output norm after the recurrence ("Strata PR #3226").
+// Per chunk (chunk-local g_t = sum_{u<=t} log a_u, G_t = e^{g_t},
+// c_t = e^{g_last - g_t}):
+//   A_ts = b_t e^{g_t - g_s} k_t.k_s (s < t),     Tinv = (I + A)^-1
+//   R_t  = b_t v_t - b_t G_t S0 k_t,              d = Tinv R
+//   o_t  = G_t S0 q_t + sum_{s<=t} e^{g_t - g_s} (q_t.k_s) d_s
+//   S    = G_last S0 + sum_s c_s d_s k_s^T
+// Written transposed, value row i of S is TMEM lane i and the products are
+//   MMA1  P^T  = S0 [K;Q]^T     M=128 N=128 K=128   S0 as bf16 hi + lo (2 passes)
+//   MMA2  G    = [K;Q] K^T      M=128 N=64  K=128   exact bf16 products
+//   MMA4  D^T  = R^T Tinv^T     M=128 N=64  K=64    3 passes (hi hi, lo hi, hi lo)
+//   MMA5  O^T  = D^T X^T        M=128 N=64  K=64    3 passes
+//   MMA3  dS   = (c D)^T K      M=128 N=128 K=64    (c D) as hi + lo (2 passes)
+// where X_ts = e^{g_t - g_s} q_t.k_s (s <= t). An f32 operand x enters as
+// hi = bf16(x), lo = bf16(x - hi): the dropped lo*lo term and the rounding of
+// lo leave a relative error near 2^-16 per product, far below the 1e-4 bound
+// on states. S stays in f32 in TMEM for the whole sequence; only its bf16
+// hi/lo copies (MMA operands) are rewritten per chunk. CUDA cores build the
+// decay tables, invert I + A (64 x 64, blocked) and do the RMSNorm epilogue.
+// One block of 256 threads per (sequence, v head); warps w and w + 4 share
+// TMEM lane quarter w % 4 (rows i = 32 (w % 4) + lane). Every wait is bounded.
+#include "common.cuh"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int PT = 256;
+constexpr int C64 = CHUNK;           // 64
+constexpr int AP = C64 + 1;          // row stride of the f32 64x64 tables
+
+// shared memory map (bytes); K-major tiles use tc::kmajor_offset
+constexpr int SM_SHI = 0;                          // S hi   128x128 bf16 (MMA1 A)
+constexpr int SM_SLO = SM_SHI + 32768;             // S lo
+constexpr int SM_KQ = SM_SLO + 32768;              // [K;Q]  128x128 bf16 (MMA1 B, MMA2 A and B);
+                                                   // then (cD)^T hi | lo, 128x64 each (MMA3 A)
+constexpr int SM_KT = SM_KQ + 32768;               // K^T    128x64 bf16 (MMA3 B)
+constexpr int SM_RD = SM_KT + 16384;               // R^T hi | lo, then D^T hi | lo, 128x64 each
+                                                   // (MMA4 / MMA5 A); then outputs [64][128] f32
+constexpr int SM_TI = SM_RD + 32768;               // Tinv hi | lo, 64x64 each (MMA4 B)
+constexpr int SM_XB = SM_TI + 16384;               // X hi | lo, 64x64 each (MMA5 B)
+constexpr int SM_AB = SM_XB + 16384;               // A f32 [64][AP]
+constexpr int SM_TB = SM_AB + 64 * AP * 4;         // Tinv f32 [64][AP]
+constexpr int SM_TMP = SM_TB + 64 * AP * 4;        // inverse scratch [1024] f32
+constexpr int SM_VEC = SM_TMP + 1024 * 4;          // g2, G, b, c, la [64] f32
+constexpr int SM_BAR = SM_VEC + 5 * 64 * 4;        // mbarrier (8 B) + TMEM slot
+constexpr int SM_TOTAL = SM_BAR + 16;
+
+constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t TM_S = 0;         // S f32                    cols   0..127
+constexpr uint32_t TM_P = 128;       // P^T = [S0 k | S0 q]      cols 128..255
+constexpr uint32_t TM_G = 256;       // G = [K;Q] K^T            cols 256..319
+constexpr uint32_t TM_D = 320;       // D^T                      cols 320..383
+constexpr uint32_t TM_DS = 256;      // dS (after G and D^T are read)  256..383
+constexpr uint32_t TM_O = 384;       // O^T                      cols 384..447
+constexpr uint32_t WAIT_POLLS = 1u << 24;
+
+__device__ __forceinline__ void st16(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// 2^x by the hardware approximation (relative error about 2^-22).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One row (K = 64 values) of a K-major tile with `rows` rows, as bf16 hi | lo.
+__device__ __forceinline__ void put_row64(uint8_t* hi_tile, uint8_t* lo_tile, int row, int rows,
+                                          const float* x) {
+#pragma unroll
+  for (int q8 = 0; q8 < 8; ++q8) {
+    uint4 hi, lo;
+    tc::split8(x + 8 * q8, hi, lo);
+    st16(hi_tile + tc::kmajor_offset(row, 8 * q8, rows), hi);
+    st16(lo_tile + tc::kmajor_offset(row, 8 * q8, rows), lo);
+  }
+}
+
+// n_slices K=16 slices of one MMA pass over K-major tiles of a_rows / b_rows
+// rows (the K-slice stride is two core-matrix columns: 2 * rows/8 * 128 bytes).
+__device__ __forceinline__ void mma_pass(uint32_t d_tmem, uint32_t a, int a_rows, uint32_t b,
+                                         int b_rows, int n_slices, uint32_t idesc, bool acc_first) {
+  const uint32_t a_lbo = (uint32_t)(a_rows / 8) * 128, b_lbo = (uint32_t)(b_rows / 8) * 128;
+#pragma unroll 1
+  for (int ks = 0; ks < n_slices; ++ks)
+    tc::mma_bf16(d_tmem, tc::smem_desc(a + ks * 2 * a_lbo, a_lbo, 128),
+                 tc::smem_desc(b + ks * 2 * b_lbo, b_lbo, 128), idesc,
+                 (acc_first || ks > 0) ? 1u : 0u);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint8_t* SHI = sm + SM_SHI;
+  uint8_t* SLO = sm + SM_SLO;
+  uint8_t* KQ = sm + SM_KQ;
+  uint8_t* KT = sm + SM_KT;
+  uint8_t* RD = sm + SM_RD;
+  uint8_t* TI = sm + SM_TI;
+  uint8_t* XB = sm + SM_XB;
+  float* OB = reinterpret_cast<float*>(sm + SM_RD);
+  float* AB = reinterpret_cast<float*>(sm + SM_AB);
+  float* TB = reinterpret_cast<float*>(sm + SM_TB);
+  float* tmp = reinterpret_cast<float*>(sm + SM_TMP);
+  float* g2_s = reinterpret_cast<float*>(sm + SM_VEC);   // chunk-local log2 decay
+  float* G_s = g2_s + 64;
+  float* b_s = G_s + 64;
+  float* c_s = b_s + 64;
+  float* la_s = c_s + 64;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + SM_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SM_BAR + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int h = blockIdx.x, s = blockIdx.y;
+  const int Hk = p.Hk, Hv = p.Hv, hq = h / (Hv / Hk);
+  const int C = (2 * Hk + Hv) * D;
+  const int slot = p.slot_idx[s];
+  if (slot < 0) return;
+  if (slot >= p.n_slots) {
+    if (tid == 0 && h == 0) report(p.dev_err, GDN_DEVERR_SLOT);
+    return;
+  }
+  const int64_t seq0 = p.cu[s], seq1 = p.cu[s + 1];
+  if (seq1 < seq0 || seq0 < 0 || seq1 > p.n_tok) {
+    if (tid == 0 && h == 0) report(p.dev_err, GDN_DEVERR_SEQLENS);
+    return;
+  }
+  const uint16_t* qkv = static_cast<const uint16_t*>(p.qkv);
+
+  if (tid == 0) tc::mbar_init(mbar, 1);
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, TM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t lane_addr = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
+  const int i = tid & 127;                 // value row (TMEM lane) of this thread
+  const bool owner = tid < 128;            // warps 0..3 own the rows; warps 4..7 help
+
+  // ---- initial state: row i into TMEM (f32) and the bf16 hi/lo tiles
+  float* Sg = p.state + (((int64_t)slot * Hv + h) * D) * D;
+  const bool has_init = p.has_init[s] != 0;
+  {
+    const int cb0 = owner ? 0 : 4;                   // owners columns 0..63, helpers 64..127
+#pragma unroll 1
+    for (int cb = cb0; cb < cb0 + 4; ++cb) {
+      float v[16];
+      if (has_init) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 f = reinterpret_cast<const float4*>(Sg + (int64_t)i * D + 16 * cb)[q];
+          v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] = 0.f;
+      }
+      tc::tmem_st16(lane_addr + TM_S + 16 * cb, v);
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        uint4 hi, lo;
+        tc::split8(v + 8 * hlf, hi, lo);
+        st16(SHI + tc::kmajor_offset(i, 16 * cb + 8 * hlf, 128), hi);
+        st16(SLO + tc::kmajor_offset(i, 16 * cb + 8 * hlf, 128), lo);
+      }
+    }
+    tc::tmem_st_wait();
+  }
+
+  uint32_t phase = 0;
+  bool timed_out = false;
+  const uint32_t id128 = tc::idesc_bf16_f32(128, 128);
+  const uint32_t id64 = tc::idesc_bf16_f32(128, 64);
+  const uint32_t a_SHI = tc::smem_u32(SHI), a_SLO = tc::smem_u32(SLO), a_KQ = tc::smem_u32(KQ);
+  const uint32_t a_KT = tc::smem_u32(KT), a_RD = tc::smem_u32(RD), a_TI = tc::smem_u32(TI);
+  const uint32_t a_XB = tc::smem_u32(XB);
+
+  // Thread 0 commits the MMAs it issued; everyone waits (bounded). Returns
+  // false, for the whole block, if the wait gave up.
+  auto commit_and_wait = [&]() -> bool {
+    if (tid == 0) tc::mma_commit(mbar);
+    const bool ok = tc::mbar_wait(mbar, phase, WAIT_POLLS);
+    if (ok) phase ^= 1;
+    tc::fence_after_sync();
+    return __syncthreads_or(!ok) == 0;
+  };
+
+  for (int64_t c0 = seq0; c0 < seq1; c0 += C64) {
+    const int m = (int)(seq1 - c0 < C64 ? seq1 - c0 : C64);
+
+    // ---- (a) stage keys and queries ([K;Q] K-major, K^T K-major) and gates
+    for (int it = tid; it < C64 * 32; it += PT) {
+      const int t = it >> 5, part = it & 31, isq = part >> 4, w8 = part & 15;
+      uint4 piece = make_uint4(0u, 0u, 0u, 0u);
+      if (t < m)
+        piece = *reinterpret_cast<const uint4*>(qkv + (c0 + t) * C + (isq ? hq : Hk + hq) * D + 8 * w8);
+      st16(KQ + tc::kmajor_offset(isq * 64 + t, 8 * w8, 128), piece);
+      if (!isq) {
+        const uint32_t wv[4] = {piece.x, piece.y, piece.z, piece.w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint16_t*>(KT + tc::kmajor_offset(8 * w8 + u, t, 128)) =
+              (uint16_t)(wv[u >> 1] >> (16 * (u & 1)));
+      }
+    }
+    if (tid < C64) {
+      const int t = tid;
+      la_s[t] = t < m ? log2f(p.alpha[(c0 + t) * Hv + h]) : 0.f;
+      b_s[t] = t < m ? p.beta[(c0 + t) * Hv + h] : 0.f;
+    }
+    tc::fence_async_smem();
+    __syncthreads();
+
+    // ---- (b) MMA1 (S0 hi, lo) and MMA2, while the decay tables are built
+    if (tid == 0) {
+      tc::fence_after_sync();
+      mma_pass(tbase + TM_P, a_SHI, 128, a_KQ, 128, 8, id128, false);
+      mma_pass(tbase + TM_P, a_SLO, 128, a_KQ, 128, 8, id128, true);
+      mma_pass(tbase + TM_G, a_KQ, 128, a_KQ, 128, 8, id64, false);
+    }
+    if (tid < C64) {                                     // prefix sums in a fixed order
+      float acc = 0.f;
+      for (int u = 0; u <= tid; ++u) acc += la_s[u];
+      g2_s[tid] = acc;
+      G_s[tid] = ex2(acc);
+    }
+    __syncthreads();
+    if (tid < C64) c_s[tid] = ex2(g2_s[C64 - 1] - g2_s[tid]);
+    if (!commit_and_wait()) { timed_out = true; break; }
+
+    // ---- (c) tables from G (owners); R^T rows from P^T (helpers)
+    if (owner) {
+      float gr[64];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::tmem_ld16(lane_addr + TM_G + 16 * cb, gr + 16 * cb);
+      if (i < C64) {                                     // A row i (f32, strictly lower)
+        const float gi = g2_s[i], bi = b_s[i];
+#pragma unroll
+        for (int u = 0; u < C64; ++u)
+          AB[i * AP + u] = u < i ? __fmul_rn(__fmul_rn(bi, ex2(gi - g2_s[u])), gr[u]) : 0.f;
+      } else {                                           // X row t: the MMA5 B tile
+        const int t = i - C64;
+        const float gt = g2_s[t];
+        float x[64];
+#pragma unroll
+        for (int u = 0; u < C64; ++u) x[u] = u <= t ? __fmul_rn(ex2(gt - g2_s[u]), gr[u]) : 0.f;
+        put_row64(XB, XB + 8192, t, 64, x);
+      }
+    } else {                                             // R^T row i: the MMA4 A tile
+      const uint16_t* vcol = qkv + c0 * C + (2 * Hk + h) * D + i;
+      float r[64];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        float pk[16];
+        tc::tmem_ld16(lane_addr + TM_P + 16 * cb, pk);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int t = 16 * cb + u;
+          const float vt = t < m ? bf2f(vcol[(int64_t)t * C]) : 0.f;
+          const float bt = b_s[t];
+          r[t] = __fmaf_rn(-__fmul_rn(bt, G_s[t]), pk[u], __fmul_rn(bt, vt));
+        }
+      }
+      put_row64(RD, RD + 16384, i, 128, r);
+    }
+    for (int e = tid; e < C64 * AP; e += PT) TB[e] = 0.f;
+    __syncthreads();
+
+    // ---- (d) Tinv = (I + A)^-1 by recursive doubling over 16/32/64 blocks
+    if (tid < C64) {
+      const int j = tid, blk = j & ~15;
+      TB[j * AP + j] = 1.f;
+      for (int t = j + 1; t < blk + 16; ++t) {
+        float acc = 0.f;
+        for (int u = j; u < t; ++u) acc = __fmaf_rn(AB[t * AP + u], TB[u * AP + j], acc);
+        TB[t * AP + j] = -acc;
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < 512; e += PT) {                // level 2: A21 Y11 per 32-block
+      const int P = e >> 8, ent = e & 255, r = ent >> 4, j = ent & 15, base = 32 * P;
+      float acc = 0.f;
+#pragma unroll 4
+      for (int u = 0; u < 16; ++u)
+        acc = __fmaf_rn(AB[(base + 16 + r) * AP + base + u], TB[(base + u) * AP + base + j], acc);
+      tmp[e] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < 512; e += PT) {
+      const int P = e >> 8, ent = e & 255, r = ent >> 4, j = ent & 15, base = 32 * P;
+      float acc = 0.f;
+#pragma unroll 4
+      for (int u = 0; u < 16; ++u)
+        acc = __fmaf_rn(TB[(base + 16 + r) * AP + base + 16 + u], tmp[P * 256 + u * 16 + j], acc);
+      TB[(base + 16 + r) * AP + base + j] = -acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < 1024; e += PT) {               // level 3: A[32:,:32] Y[:32,:32]
+      const int r = e >> 5, j = e & 31;
+      float acc = 0.f;
+      for (int u = j & ~15; u < 32; ++u) acc = __fmaf_rn(AB[(32 + r) * AP + u], TB[u * AP + j], acc);
+      tmp[e] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < 1024; e += PT) {
+      const int r = e >> 5, j = e & 31;
+      float acc = 0.f;
+      for (int u = 0; u <= r; ++u) acc = __fmaf_rn(TB[(32 + r) * AP + 32 + u], tmp[u * 32 + j], acc);
+      TB[(32 + r) * AP + j] = -acc;
+    }
+    __syncthreads();
+    if (tid < C64) {                                     // Tinv row t: the MMA4 B tile
+      float x[64];
+#pragma unroll
+      for (int u = 0; u < C64; ++u) x[u] = TB[tid * AP + u];
+      put_row64(TI, TI + 8192, tid, 64, x);
+    }
+    tc::fence_async_smem();
+    __syncthreads();
+
+    // ---- (e) MMA4: D^T = R^T Tinv^T
+    if (tid == 0) {
+      tc::fence_after_sync();
+      mma_pass(tbase + TM_D, a_RD, 128, a_TI, 64, 4, id64, false);               // hi hi
+      mma_pass(tbase + TM_D, a_RD + 16384, 128, a_TI, 64, 4, id64, true);        // lo hi
+      mma_pass(tbase + TM_D, a_RD, 128, a_TI + 8192, 64, 4, id64, true);         // hi lo
+    }
+    if (!commit_and_wait()) { timed_out = true; break; }
+
+    // ---- (f) D^T row i -> MMA5 A tile (owners); (c D)^T row i -> MMA3 A tile (helpers)
+    {
+      float d[64];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::tmem_ld16(lane_addr + TM_D + 16 * cb, d + 16 * cb);
+      if (owner) {
+        put_row64(RD, RD + 16384, i, 128, d);
+      } else {
+#pragma unroll
+        for (int u = 0; u < C64; ++u) d[u] = __fmul_rn(c_s[u], d[u]);
+        put_row64(KQ, KQ + 16384, i, 128, d);
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+
+    // ---- (g) MMA5: O^T = D^T X^T;  MMA3: dS = (c D)^T K
+    if (tid == 0) {
+      tc::fence_after_sync();
+      mma_pass(tbase + TM_O, a_RD, 128, a_XB, 64, 4, id64, false);
+      mma_pass(tbase + TM_O, a_RD + 16384, 128, a_XB, 64, 4, id64, true);
+      mma_pass(tbase + TM_O, a_RD, 128, a_XB + 8192, 64, 4, id64, true);
+      mma_pass(tbase + TM_DS, a_KQ, 128, a_KT, 128, 4, id128, false);
+      mma_pass(tbase + TM_DS, a_KQ + 16384, 128, a_KT, 128, 4, id128, true);
+    }
+    if (!commit_and_wait()) { timed_out = true; break; }
+
+    // ---- (h) owners: o = G (S0 q) + O^T into the output buffer (the RD region
+    //          is free now); helpers: S = G_last S + dS, TMEM and hi/lo tiles
+    if (owner) {
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        float pq[16], ov[16];
+        tc::tmem_ld16(lane_addr + TM_P + 64 + 16 * cb, pq);
+        tc::tmem_ld16(lane_addr + TM_O + 16 * cb, ov);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int t = 16 * cb + u;
+          OB[t * D + i] = __fmul_rn(__fmaf_rn(G_s[t], pq[u], ov[u]), p.q_scale);
+        }
+      }
+    } else {
+      const float gl = G_s[C64 - 1];
+#pragma unroll 1
+      for (int cb = 0; cb < 8; ++cb) {
+        float sv[16], dv[16];
+        tc::tmem_ld16(lane_addr + TM_S + 16 * cb, sv);
+        tc::tmem_ld16(lane_addr + TM_DS + 16 * cb, dv);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) sv[u] = __fmaf_rn(gl, sv[u], dv[u]);
+        tc::tmem_st16(lane_addr + TM_S + 16 * cb, sv);
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          uint4 hi, lo;
+          tc::split8(sv + 8 * hlf, hi, lo);
+          st16(SHI + tc::kmajor_offset(i, 16 * cb + 8 * hlf, 128), hi);
+          st16(SLO + tc::kmajor_offset(i, 16 * cb + 8 * hlf, 128), lo);
+        }
+      }
+      tc::tmem_st_wait();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+
+    // ---- (i) z-gated RMSNorm of the outputs: 16 lanes per token
+    for (int it = 0; it < C64 / (PT / 16); ++it) {
+      const int t = it * (PT / 16) + (tid >> 4), l16 = tid & 15;
+      const bool live = t < m;
+      float o[8];
+      const float4 u0 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16];
+      const float4 u1 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16 + 1];
+      o[0] = u0.x; o[1] = u0.y; o[2] = u0.z; o[3] = u0.w;
+      o[4] = u1.x; o[5] = u1.y; o[6] = u1.z; o[7] = u1.w;
+      const float ss = head_sum_sq16(o);
+      if (live) {
+        const float r = inv_norm(__fmul_rn(ss, 1.0f / D), p.eps);
+        const int64_t zo = (c0 + t) * Hv * D + (int64_t)h * D + l16 * 8;
+        float zv[8], res[8];
+        load8<BF16>(p.z, zo, zv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu(zv[j]));
+        store8<BF16>(p.out, zo, res);
+      }
+    }
+    __syncthreads();
+  }
+
+  if (timed_out) {
+    if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
+    tc::mbar_wait(mbar, phase, WAIT_POLLS);              // the pending phase: work in flight
+  } else {
+    const int cb0 = owner ? 0 : 4;                       // final state: row i from TMEM
+#pragma unroll 1
+    for (int cb = cb0; cb < cb0 + 4; ++cb) {
+      float v[16];
+      tc::tmem_ld16(lane_addr + TM_S + 16 * cb, v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        reinterpret_cast<float4*>(Sg + (int64_t)i * D + 16 * cb)[q] =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, TM_COLS);
+}
+
+size_t prefill_tc_smem_bytes() { return SM_TOTAL; }
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
+  const int smem = (int)SM_TOTAL;
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.Hv, a.n_seq);
+  prefill_tc_kernel<<<grid, PT, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

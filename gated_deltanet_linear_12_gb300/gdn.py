@@ -19,7 +19,7 @@ from . import build as _build
 GDN_OK, GDN_ERR_INVALID, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
 GDN_F32, GDN_BF16 = 0, 1
 GDN_VERIFY_COMMIT_ALL = 1
-GDN_DEVERR_SLOT, GDN_DEVERR_NKEEP, GDN_DEVERR_SEQLENS = 1, 2, 4
+GDN_DEVERR_SLOT, GDN_DEVERR_NKEEP, GDN_DEVERR_SEQLENS, GDN_DEVERR_TIMEOUT = 1, 2, 4, 8
 HEAD_DIM, CONV_WIDTH, CHUNK, MAX_DRAFT = 128, 4, 64, 8
 
 EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_step",

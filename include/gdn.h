@@ -70,6 +70,8 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_DEVERR_SLOT 1u        /* slot index >= n_slots */
 #define GDN_DEVERR_NKEEP 2u       /* n_keep outside [0, T] */
 #define GDN_DEVERR_SEQLENS 4u     /* cu_seqlens decreasing or beyond n_tok */
+#define GDN_DEVERR_TIMEOUT 8u     /* a tensor-core completion wait gave up; the
+                                     sequence's outputs and state are incomplete */
 
 typedef struct gdn_config {
   int32_t n_qk_heads;   /* Hk >= 1 */
