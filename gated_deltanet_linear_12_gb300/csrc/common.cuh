@@ -64,6 +64,37 @@ template <int A> __device__ __forceinline__ void store8(void* base, int64_t i, c
   }
 }
 
+// Eight activations kept packed between load and use (4 registers for bf16).
+template <int A> struct Raw8;
+template <> struct Raw8<BF16> { uint4 u; };
+template <> struct Raw8<F32> { float4 a, b; };
+
+template <int A> __device__ __forceinline__ void raw_load(const void* base, int64_t i, Raw8<A>& r) {
+  if constexpr (A == BF16) r.u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + i);
+  else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+    r.a = p[0];
+    r.b = p[1];
+  }
+}
+template <int A> __device__ __forceinline__ void raw_zero(Raw8<A>& r) {
+  if constexpr (A == BF16) r.u = make_uint4(0u, 0u, 0u, 0u);
+  else { r.a = make_float4(0.f, 0.f, 0.f, 0.f); r.b = r.a; }
+}
+template <int A> __device__ __forceinline__ void raw_unpack(const Raw8<A>& r, float v[8]) {
+  if constexpr (A == BF16) {
+    const uint32_t w[4] = {r.u.x, r.u.y, r.u.z, r.u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __uint_as_float(w[j] << 16);
+      v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  } else {
+    v[0] = r.a.x; v[1] = r.a.y; v[2] = r.a.z; v[3] = r.a.w;
+    v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
+  }
+}
+
 __device__ __forceinline__ void report(uint32_t* dev_err, uint32_t bit) {
   if (dev_err) atomicOr(dev_err, bit);
 }
@@ -141,6 +172,12 @@ __device__ __forceinline__ float2 silu2(float2 y) {
 }
 
 __device__ __forceinline__ float silu(float y) { return silu2(make_float2(y, 0.f)).x; }
+
+// SiLU for the output gate z, where no bitwise agreement is asked for: the
+// fast exponential and divide intrinsics (relative error about 1e-6).
+__device__ __forceinline__ float silu_gate(float z) {
+  return __fdividef(z, 1.0f + __expf(-z));
+}
 
 // Sum of squares of a 128-channel head held as 8 contiguous channels by each
 // of 16 consecutive lanes (lane & 15 = channel group). In-lane: strides 4, 2, 1;

@@ -23,7 +23,7 @@ constexpr int CONV_THREADS = 256;
 constexpr int CONV_QUARTERS = 4;                      // token quarters of a chunk
 constexpr int CONV_TOK = CHUNK / CONV_QUARTERS;       // 16 tokens per thread
 constexpr int CONV_HEADS_PER_BLOCK = 4;               // 4 heads x 16 lanes x 4 quarters
-constexpr int CONV_BATCH = 4;                         // tokens loaded ahead per step
+constexpr int CONV_BATCH = 2;                         // tokens loaded ahead per step
 
 // Thread layout: warp w covers quarter w / 2 of the chunk and heads
 // 2 (w % 2), 2 (w % 2) + 1 of the block's 4 heads (16 lanes each, 8 contiguous
@@ -105,31 +105,38 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
     }
 
     // 16 tokens, fully unrolled so the three-row window rotates through
-    // registers; loads run CONV_BATCH tokens ahead of the arithmetic.
+    // registers. Rows stay packed until used, and the loads of the next batch
+    // of CONV_BATCH tokens are issued before the current batch is computed.
     const int n_here = (int)(t_stop - t_begin);           // 1..16, uniform per warp
+    Raw8<A> cur[CONV_BATCH], nxt[CONV_BATCH];
+#pragma unroll
+    for (int u = 0; u < CONV_BATCH; ++u) {
+      if (active && u < n_here) raw_load<A>(x, (t_begin + u) * ld_x + c0, cur[u]);
+      else raw_zero<A>(cur[u]);
+    }
 #pragma unroll
     for (int b0 = 0; b0 < CONV_TOK; b0 += CONV_BATCH) {
       if (b0 >= n_here) break;
-      float xv[CONV_BATCH][8];
+      if (b0 + CONV_BATCH < CONV_TOK) {
 #pragma unroll
-      for (int u = 0; u < CONV_BATCH; ++u) {
-        if (active && b0 + u < n_here) load8<A>(x, (t_begin + b0 + u) * ld_x + c0, xv[u]);
-        else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) xv[u][j] = 0.f;
+        for (int u = 0; u < CONV_BATCH; ++u) {
+          const int tt = b0 + CONV_BATCH + u;
+          if (active && tt < n_here) raw_load<A>(x, (t_begin + tt) * ld_x + c0, nxt[u]);
+          else raw_zero<A>(nxt[u]);
         }
       }
 #pragma unroll
       for (int u = 0; u < CONV_BATCH; ++u) {
         if (b0 + u >= n_here) break;
-        float v[8];
+        float xv[8], v[8];
+        raw_unpack<A>(cur[u], xv);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float2 cur = make_float2(xv[u][2 * q], xv[u][2 * q + 1]);
-          const float2 a = silu2(conv4x2(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cur));
+          const float2 cv = make_float2(xv[2 * q], xv[2 * q + 1]);
+          const float2 a = silu2(conv4x2(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cv));
           v[2 * q] = a.x;
           v[2 * q + 1] = a.y;
-          p0[q] = p1[q]; p1[q] = p2[q]; p2[q] = cur;
+          p0[q] = p1[q]; p1[q] = p2[q]; p2[q] = cv;
         }
         if constexpr (NORM) {
           const float ss = head_sum_sq16(v);           // all lanes take part
@@ -145,6 +152,8 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
         }
         if (active) store8<A>(y, (t_begin + b0 + u) * ld_y + c0, v);
       }
+#pragma unroll
+      for (int u = 0; u < CONV_BATCH; ++u) cur[u] = nxt[u];
     }
   }
 

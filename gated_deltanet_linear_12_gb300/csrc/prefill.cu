@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_ffma_kernel(PrefillArgs
         load8<A>(p.z, zo, zv);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu(zv[j]));
+          res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu_gate(zv[j]));
         store8<A>(p.out, zo, res);
       }
     }

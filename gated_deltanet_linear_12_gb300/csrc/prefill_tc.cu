@@ -118,7 +118,27 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SM_BAR + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int h = blockIdx.x, s = blockIdx.y;
+  const int h = blockIdx.x;
+  // Longest sequences first: block row y takes the sequence of rank y by
+  // length (ties by index), so the long chains start in the first wave.
+  int s = blockIdx.y;
+  if (p.n_seq <= 256) {
+    int* pick = reinterpret_cast<int*>(sm + SM_BAR + 12);
+    if (tid == 0) *pick = blockIdx.y;
+    __syncthreads();
+    for (int q = tid; q < p.n_seq; q += PT) {
+      const int lq = p.cu[q + 1] - p.cu[q];
+      int rank = 0;
+      for (int r = 0; r < p.n_seq; ++r) {
+        const int lr = p.cu[r + 1] - p.cu[r];
+        rank += (lr > lq) || (lr == lq && r < q);
+      }
+      if (rank == (int)blockIdx.y) *pick = q;
+    }
+    __syncthreads();
+    s = *pick;
+    __syncthreads();
+  }
   const int Hk = p.Hk, Hv = p.Hv, hq = h / (Hv / Hk);
   const int C = (2 * Hk + Hv) * D;
   const int slot = p.slot_idx[s];
@@ -198,19 +218,41 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
   for (int64_t c0 = seq0; c0 < seq1; c0 += C64) {
     const int m = (int)(seq1 - c0 < C64 ? seq1 - c0 : C64);
 
-    // ---- (a) stage keys and queries ([K;Q] K-major, K^T K-major) and gates
-    for (int it = tid; it < C64 * 32; it += PT) {
-      const int t = it >> 5, part = it & 31, isq = part >> 4, w8 = part & 15;
-      uint4 piece = make_uint4(0u, 0u, 0u, 0u);
-      if (t < m)
-        piece = *reinterpret_cast<const uint4*>(qkv + (c0 + t) * C + (isq ? hq : Hk + hq) * D + 8 * w8);
-      st16(KQ + tc::kmajor_offset(isq * 64 + t, 8 * w8, 128), piece);
-      if (!isq) {
-        const uint32_t wv[4] = {piece.x, piece.y, piece.z, piece.w};
+    // ---- (a) stage keys and queries ([K;Q] K-major, K^T K-major), values
+    //          (row-major, in the Tinv tiles' space until (d)) and gates.
+    //          All 12 loads of a thread are issued before any store.
+    {
+      uint4 pc[12];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint16_t*>(KT + tc::kmajor_offset(8 * w8 + u, t, 128)) =
-              (uint16_t)(wv[u >> 1] >> (16 * (u & 1)));
+      for (int k = 0; k < 12; ++k) {
+        const int it = tid + k * PT;                     // 0..2047 keys/queries, then values
+        pc[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (k < 8) {
+          const int t = it >> 5, part = it & 31, isq = part >> 4, w8 = part & 15;
+          if (t < m)
+            pc[k] = *reinterpret_cast<const uint4*>(qkv + (c0 + t) * C + (isq ? hq : Hk + hq) * D + 8 * w8);
+        } else {
+          const int iv = it - 2048, t = iv >> 4, w8 = iv & 15;
+          if (t < m) pc[k] = *reinterpret_cast<const uint4*>(qkv + (c0 + t) * C + (2 * Hk + h) * D + 8 * w8);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 12; ++k) {
+        const int it = tid + k * PT;
+        if (k < 8) {
+          const int t = it >> 5, part = it & 31, isq = part >> 4, w8 = part & 15;
+          st16(KQ + tc::kmajor_offset(isq * 64 + t, 8 * w8, 128), pc[k]);
+          if (!isq) {
+            const uint32_t wv[4] = {pc[k].x, pc[k].y, pc[k].z, pc[k].w};
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint16_t*>(KT + tc::kmajor_offset(8 * w8 + u, t, 128)) =
+                  (uint16_t)(wv[u >> 1] >> (16 * (u & 1)));
+          }
+        } else {
+          const int iv = it - 2048, t = iv >> 4, w8 = iv & 15;
+          st16(TI + (t * D + 8 * w8) * 2, pc[k]);
+        }
       }
     }
     if (tid < C64) {
@@ -257,7 +299,7 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
         put_row64(XB, XB + 8192, t, 64, x);
       }
     } else {                                             // R^T row i: the MMA4 A tile
-      const uint16_t* vcol = qkv + c0 * C + (2 * Hk + h) * D + i;
+      const uint16_t* vcol = reinterpret_cast<const uint16_t*>(TI) + i;   // staged values
       float r[64];
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
@@ -266,7 +308,7 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int t = 16 * cb + u;
-          const float vt = t < m ? bf2f(vcol[(int64_t)t * C]) : 0.f;
+          const float vt = bf2f(vcol[t * D]);            // zero past m
           const float bt = b_s[t];
           r[t] = __fmaf_rn(-__fmul_rn(bt, G_s[t]), pk[u], __fmul_rn(bt, vt));
         }
@@ -402,25 +444,34 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     tc::fence_before_sync();
     __syncthreads();
 
-    // ---- (i) z-gated RMSNorm of the outputs: 16 lanes per token
-    for (int it = 0; it < C64 / (PT / 16); ++it) {
-      const int t = it * (PT / 16) + (tid >> 4), l16 = tid & 15;
-      const bool live = t < m;
-      float o[8];
-      const float4 u0 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16];
-      const float4 u1 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16 + 1];
-      o[0] = u0.x; o[1] = u0.y; o[2] = u0.z; o[3] = u0.w;
-      o[4] = u1.x; o[5] = u1.y; o[6] = u1.z; o[7] = u1.w;
-      const float ss = head_sum_sq16(o);
-      if (live) {
-        const float r = inv_norm(__fmul_rn(ss, 1.0f / D), p.eps);
-        const int64_t zo = (c0 + t) * Hv * D + (int64_t)h * D + l16 * 8;
-        float zv[8], res[8];
-        load8<BF16>(p.z, zo, zv);
+    // ---- (i) z-gated RMSNorm of the outputs: 16 lanes per token (z prefetched)
+    {
+      constexpr int NIT = C64 / (PT / 16);
+      float zv[NIT][8];
+      const int l16 = tid & 15;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu(zv[j]));
-        store8<BF16>(p.out, zo, res);
+      for (int it = 0; it < NIT; ++it) {
+        const int t = it * (PT / 16) + (tid >> 4);
+        if (t < m) load8<BF16>(p.z, (c0 + t) * Hv * D + (int64_t)h * D + l16 * 8, zv[it]);
+      }
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        const int t = it * (PT / 16) + (tid >> 4);
+        const bool live = t < m;
+        float o[8];
+        const float4 u0 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16];
+        const float4 u1 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16 + 1];
+        o[0] = u0.x; o[1] = u0.y; o[2] = u0.z; o[3] = u0.w;
+        o[4] = u1.x; o[5] = u1.y; o[6] = u1.z; o[7] = u1.w;
+        const float ss = head_sum_sq16(o);
+        if (live) {
+          const float r = inv_norm(__fmul_rn(ss, 1.0f / D), p.eps);
+          float res[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu_gate(zv[it][j]));
+          store8<BF16>(p.out, (c0 + t) * Hv * D + (int64_t)h * D + l16 * 8, res);
+        }
       }
     }
     __syncthreads();

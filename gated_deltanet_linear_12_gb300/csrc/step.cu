@@ -30,12 +30,14 @@
 // after a block barrier. The read-only verify mode uses one block per v head.
 #include "common.cuh"
 #include "launch.h"
+#include "tc.cuh"
 
 namespace gdn {
 
 enum StepMode { VERIFY = 0, VERIFY_COMMIT_ALL = 1, COMMIT = 2 };
 
 constexpr int STEP_THREADS = 256;
+constexpr int MAX_HEADS = 16;                    // v heads per block (Hv / Hk limit)
 
 
 // Post-conv activation of 8 channels of draft token t: rows t..t+3 of
@@ -114,9 +116,18 @@ __device__ __forceinline__ void rows_dot(const float4 (&S)[2][8], const float* v
   r1 = a1;
 }
 
-template <int A, int MODE>
+// Tensor-core variant (TC): the 2T state dot products of every value row come
+// from one tcgen05 product S0 [k_0..k_7 ; q_0..q_7]^T (M = 128 rows, N = 16,
+// K = 128) with S0 entering as bf16 hi + lo parts (two passes, relative error
+// near 2^-16) and the keys/queries exact in bf16; thread i < 128 then owns
+// value row i (TMEM lane i) for the deltas and outputs. The f32 copy of S0
+// stays in registers (coalesced layout) for the state commit.
+constexpr int TC_REGION = 32768 * 2 + 4096 + MAXT * D * 4;   // S hi, S lo, B tile, deltas
+
+template <int A, int MODE, bool TC>
 __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
-  extern __shared__ __align__(16) float smem[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  float* smem = reinterpret_cast<float*>(smem_raw + (TC ? TC_REGION : 0));
   constexpr bool COMMITS = MODE != VERIFY;
   constexpr bool OUTPUTS = MODE != COMMIT;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -158,6 +169,41 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
   const int h0 = (MODE == VERIFY) ? blockIdx.x : blockIdx.x * G;   // first v head
   const int nh = (MODE == VERIFY) ? 1 : G;                         // v heads here
 
+  // The first head's state rows go in flight before anything else, so the
+  // 64 KiB read overlaps the conv and table phases (coalesced: 4 lanes cover
+  // 64 contiguous bytes of a row; this thread owns rows 2rp, 2rp+1).
+  const int rp = tid >> 2, cg = tid & 3;
+  const int row0 = 2 * rp;
+  float4 S[2][8];
+  {
+    const float* Sg0 = state + (((int64_t)slot * Hv + h0) * D) * D;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        S[rr][m] = reinterpret_cast<const float4*>(Sg0 + (int64_t)(row0 + rr) * D)[4 * m + cg];
+  }
+
+  // tensor-core resources: TMEM accumulator (32 columns), completion barrier
+  uint8_t* SHI = smem_raw;
+  uint8_t* SLO = smem_raw + 32768;
+  uint8_t* BT = smem_raw + 65536;                          // [k ; q] 16 x 128 bf16
+  float* dtab = reinterpret_cast<float*>(smem_raw + 65536 + 4096);   // [8][128] deltas
+  __shared__ uint64_t tc_bar;
+  __shared__ uint32_t tc_slot;
+  uint32_t tbase = 0, tc_phase = 0;
+  if constexpr (TC) {
+    if (tid == 0) tc::mbar_init(&tc_bar, 1);
+    if (warp == 0) {
+      tc::tmem_alloc(&tc_slot, 32);
+      tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    tbase = tc_slot;
+  }
+
   // shared memory: q[T][D], k[T][D], v[nh][T][D], o[T][D], small tables
   float* q_s = smem;
   float* k_s = q_s + MAXT * D;
@@ -171,11 +217,21 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
   float* g_s = E_s + MAXT;                       // [8] g_t
   float* bg_s = g_s + MAXT;                      // [8] b_t g_t
   float* b_s = bg_s + MAXT;                      // [8] b_t
+  float* al_s = b_s + MAXT;                      // [nh][8] alpha of the block's heads
+  float* be_s = al_s + MAXT * MAX_HEADS;         // [nh][8] beta
 
   const int64_t xb_off = (int64_t)b * T * C;
   const void* x_b = static_cast<const char*>(x) + xb_off * (A == BF16 ? 2 : 4);
   const int64_t cs_off = (int64_t)slot * KS * C;
   const void* cs = static_cast<const char*>(conv_state) + cs_off * (A == BF16 ? 2 : 4);
+
+  // gates of the block's heads for the n tokens, staged once
+  for (int e = tid; e < nh * n; e += STEP_THREADS) {
+    const int g = e / n, t = e % n;
+    const int64_t gi = ((int64_t)b * T + t) * Hv + h0 + g;
+    al_s[g * MAXT + t] = alpha[gi];
+    be_s[g * MAXT + t] = beta[gi];
+  }
 
   // ---- phase 1: post-conv activations of the block's channels, tokens < n
   {
@@ -248,48 +304,140 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
     else if (OUTPUTS) { const float d = warp_dot128(q_s + t * D, k_s + s * D); if (lane == 0) qk_s[t * MAXT + s] = d; }
   }
 
-  const int rp = tid >> 2, cg = tid & 3;                   // rows 2rp, 2rp+1
-  const int row0 = 2 * rp;
+
+  if constexpr (TC) {                                      // [k_0..k_7 ; q_0..q_7] as bf16
+    const int row = tid >> 4, w8 = tid & 15;               // 16 rows x 16 pieces
+    const int t = row & 7;
+    const bool live = t < n && (row < 8 || OUTPUTS);
+    const float* src = (row < 8 ? k_s : q_s) + t * D + 8 * w8;
+    float v8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v8[j] = live ? src[j] : 0.f;
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v8[2 * j], v8[2 * j + 1]);
+      w[j] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(BT + tc::kmajor_offset(row, 8 * w8, 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  bool tc_failed = false;
 
   for (int g = 0; g < nh; ++g) {
     const int h = h0 + g;
     __syncthreads();                                      // kk/qk ready; tables free
-    // gate tables for head h (one warp, fixed order)
-    if (warp == 0 && lane < MAXT) {
-      const int t = lane;
-      if (t < n) {
-        const float* ab = alpha + ((int64_t)b * T) * Hv + h;
-        const float* bb = beta + ((int64_t)b * T) * Hv + h;
-        const float bt = bb[(int64_t)t * Hv];
-        float gt = ab[0];
-        for (int u = 1; u <= t; ++u) gt = __fmul_rn(gt, ab[(int64_t)u * Hv]);
-        g_s[t] = gt;
-        b_s[t] = bt;
-        bg_s[t] = __fmul_rn(bt, gt);
-        for (int s = 0; s <= t; ++s) {
-          float r = 1.f;                                   // r(t,s) = a_{s+1} ... a_t
-          for (int u = s + 1; u <= t; ++u) r = __fmul_rn(r, ab[(int64_t)u * Hv]);
-          if (s < t) A_s[t * MAXT + s] = __fmul_rn(__fmul_rn(bt, r), kk_s[t * MAXT + s]);
-          if (OUTPUTS) Oc_s[t * MAXT + s] = __fmul_rn(r, qk_s[t * MAXT + s]);
-          if (t == n - 1) E_s[s] = r;
+    // gate tables for head h: one thread per (t, s), products in ascending
+    // order (r(t,s) = a_{s+1} ... a_t, g_t = a_0 ... a_t)
+    if (tid < MAXT * MAXT) {
+      const int t = tid >> 3, sidx = tid & 7;
+      if (t < n && sidx <= t) {
+        const float* al = al_s + g * MAXT;
+        float r = 1.f;
+        for (int u = sidx + 1; u <= t; ++u) r = __fmul_rn(r, al[u]);
+        const float bt = be_s[g * MAXT + t];
+        if (sidx < t) A_s[t * MAXT + sidx] = __fmul_rn(__fmul_rn(bt, r), kk_s[t * MAXT + sidx]);
+        if (OUTPUTS) Oc_s[t * MAXT + sidx] = __fmul_rn(r, qk_s[t * MAXT + sidx]);
+        if (t == n - 1) E_s[sidx] = r;
+        if (sidx == 0) {
+          float gt = al[0];
+          for (int u = 1; u <= t; ++u) gt = __fmul_rn(gt, al[u]);
+          g_s[t] = gt;
+          b_s[t] = bt;
+          bg_s[t] = __fmul_rn(bt, gt);
         }
       }
     }
-    // state rows into registers (coalesced: 4 lanes cover 64 contiguous bytes)
+    // z of this head for the epilogue, in flight during the dot products
+    Raw8<A> zraw;
+    const int ep_t = tid >> 4, ep_l16 = tid & 15;
+    const int64_t ep_zo = ((int64_t)b * T + ep_t) * Hv * D + (int64_t)h * D + ep_l16 * 8;
+    if (OUTPUTS && tid < 128 && ep_t < n) raw_load<A>(p.z, ep_zo, zraw);
+    // state rows of head h (the first head's are already in flight)
     float* Sg = state + (((int64_t)slot * Hv + h) * D) * D;
-    float4 S[2][8];
+    if (g > 0) {
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
+      for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
-      for (int m = 0; m < 8; ++m)
-        S[rr][m] = reinterpret_cast<const float4*>(Sg + (int64_t)(row0 + rr) * D)[4 * m + cg];
+        for (int m = 0; m < 8; ++m)
+          S[rr][m] = reinterpret_cast<const float4*>(Sg + (int64_t)(row0 + rr) * D)[4 * m + cg];
+    }
+    if constexpr (TC) {                                    // S0 as bf16 hi / lo K-major tiles
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float4 f = S[rr][m];
+          const __nv_bfloat162 h01 = __floats2bfloat162_rn(f.x, f.y);
+          const __nv_bfloat162 h23 = __floats2bfloat162_rn(f.z, f.w);
+          const float2 g01 = __bfloat1622float2(h01), g23 = __bfloat1622float2(h23);
+          const __nv_bfloat162 l01 = __floats2bfloat162_rn(f.x - g01.x, f.y - g01.y);
+          const __nv_bfloat162 l23 = __floats2bfloat162_rn(f.z - g23.x, f.w - g23.y);
+          const uint32_t off = tc::kmajor_offset(row0 + rr, 16 * m + 4 * cg, 128);
+          *reinterpret_cast<uint2*>(SHI + off) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+          *reinterpret_cast<uint2*>(SLO + off) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
+        }
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+    }
     __syncthreads();                                      // tables ready
 
-    // deltas (and outputs) token by token
     float d0[MAXT], d1[MAXT];
     const float* vh = v_s + (size_t)g * MAXT * D;
+    if constexpr (TC) {
+      // S0 [k ; q]^T on the tensor core, then row i = tid (< 128) from TMEM lane i
+      if (tid == 0) {
+        tc::fence_after_sync();
+        const uint32_t sh = tc::smem_u32(SHI), sl = tc::smem_u32(SLO), bt = tc::smem_u32(BT);
+        const uint32_t id = tc::idesc_bf16_f32(128, 16);
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tbase, tc::smem_desc(sh + ks * 4096, 2048, 128),
+                       tc::smem_desc(bt + ks * 512, 256, 128), id, ks > 0);
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tbase, tc::smem_desc(sl + ks * 4096, 2048, 128),
+                       tc::smem_desc(bt + ks * 512, 256, 128), id, 1);
+        tc::mma_commit(&tc_bar);
+      }
+      const bool ok = tc::mbar_wait(&tc_bar, tc_phase, 1u << 24);
+      if (ok) tc_phase ^= 1;
+      tc::fence_after_sync();
+      if (__syncthreads_or(!ok)) { tc_failed = true; break; }
+      if (tid < 128) {
+        float acc[16];
+        tc::tmem_ld16(tbase + ((uint32_t)(32 * warp) << 16), acc);
+        const int i = tid;
+        float dr[MAXT];
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t) {
+          if (t < n) {
+            const float bt = b_s[t], bgt = bg_s[t];
+            float r = __fmaf_rn(-bgt, acc[t], __fmul_rn(bt, vh[t * D + i]));
+#pragma unroll
+            for (int u = 0; u < t; ++u) r = __fmaf_rn(-A_s[t * MAXT + u], dr[u], r);
+            dr[t] = r;
+            dtab[t * D + i] = r;
+            if constexpr (OUTPUTS) {
+              float o = __fmul_rn(g_s[t], acc[8 + t]);
+#pragma unroll
+              for (int u = 0; u <= t; ++u) o = __fmaf_rn(Oc_s[t * MAXT + u], dr[u], o);
+              o_s[t * D + i] = __fmul_rn(o, p.q_scale);
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncthreads();                                    // deltas and outputs in smem
+#pragma unroll
+      for (int t = 0; t < MAXT; ++t) {
+        if (t < n) { d0[t] = dtab[t * D + row0]; d1[t] = dtab[t * D + row0 + 1]; }
+      }
+    }
 #pragma unroll
     for (int t = 0; t < MAXT; ++t) {
+      if (TC) break;
       if (t < n) {
         float sk0, sk1;
         rows_dot(S, k_s + t * D, cg, sk0, sk1);
@@ -370,33 +518,56 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
         const float ss = head_sum_sq16(o);
         if (live) {
           const float r = inv_norm(__fmul_rn(ss, 1.0f / D), p.eps);
-          const int64_t zo = ((int64_t)b * T + t) * Hv * D + (int64_t)h * D + l16 * 8;
+          const int64_t zo = ep_zo;
           float zv[8], res[8];
-          load8<A>(p.z, zo, zv);
+          raw_unpack<A>(zraw, zv);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu(zv[j]));
+            res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu_gate(zv[j]));
           store8<A>(p.out, zo, res);
         }
       }
     }
   }
+  if constexpr (TC) {
+    if (tc_failed) {
+      if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
+      tc::mbar_wait(&tc_bar, tc_phase, 1u << 24);          // the pending phase: work in flight
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tbase, 32);
+  }
 }
 
-size_t step_smem_bytes(int nh) {
-  return sizeof(float) * ((size_t)(3 + nh) * MAXT * D + 4 * MAXT * MAXT + 4 * MAXT);
+size_t step_smem_bytes(int nh, bool tc) {
+  return (tc ? TC_REGION : 0) +
+         sizeof(float) * ((size_t)(3 + nh) * MAXT * D + 4 * MAXT * MAXT + 4 * MAXT +
+                          2 * MAXT * MAX_HEADS);
 }
 
-template <int A, int MODE>
-static cudaError_t launch_mode(const StepArgs& a, dim3 grid, int nh, cudaStream_t stream) {
-  const size_t smem = step_smem_bytes(nh);
+template <int A, int MODE, bool TC>
+static cudaError_t launch_variant(const StepArgs& a, dim3 grid, int nh, cudaStream_t stream) {
+  const size_t smem = step_smem_bytes(nh, TC);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(step_kernel<A, MODE>,
+    cudaError_t e = cudaFuncSetAttribute(step_kernel<A, MODE, TC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  step_kernel<A, MODE><<<grid, STEP_THREADS, smem, stream>>>(a);
+  step_kernel<A, MODE, TC><<<grid, STEP_THREADS, smem, stream>>>(a);
   return cudaGetLastError();
+}
+
+// The read-only verify of two or more bf16 draft tokens uses the tensor-core
+// variant (its 2T dot products per state row dominate); the committing modes
+// (n accepted key dots per row, no query dots) and T = 1 use CUDA cores. The
+// two committing modes always share a variant, so decode and verify + commit
+// leave bitwise equal states; verify outputs at T >= 2 differ from decode's
+// by rounding only.
+template <int A, int MODE>
+static cudaError_t launch_mode(const StepArgs& a, dim3 grid, int nh, cudaStream_t stream) {
+  if (A == BF16 && MODE == VERIFY && a.T >= 2) return launch_variant<A, MODE, true>(a, grid, nh, stream);
+  return launch_variant<A, MODE, false>(a, grid, nh, stream);
 }
 
 cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, cudaStream_t stream) {

@@ -12,7 +12,7 @@ inline int tc_st_smem(int N, int K) { return (128 + N) * K * 2; }
 
 __global__ void __launch_bounds__(128, 1)
 tc_selftest_kernel(const uint16_t* __restrict__ A, const uint16_t* __restrict__ B,
-                   float* __restrict__ Dout, int N, int K, uint32_t* err) {
+                   float* __restrict__ Dout, int N, int K, int starve, uint32_t* err) {
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ uint64_t mbar;
   __shared__ uint32_t tslot;
@@ -52,12 +52,20 @@ tc_selftest_kernel(const uint16_t* __restrict__ A, const uint16_t* __restrict__ 
       const uint64_t bd = tc::smem_desc(tc::smem_u32(Bs) + ks * 2 * ((N / 8) * 128), lboB, sboB);
       tc::mma_bf16(tbase, ad, bd, idesc, ks > 0);
     }
-    tc::mma_commit(&mbar);
+    if (!starve) tc::mma_commit(&mbar);
   }
-  bool ok = tc::mbar_wait(&mbar, 0, 1u << 22);
+  // starve: nothing ever arrives on the barrier (the completion of the MMAs is
+  // not attached to it), so the bounded wait must give up and report.
+  const uint32_t polls = starve ? 4096u : (1u << 22);
+  bool ok = tc::mbar_wait(&mbar, 0, polls);
   if (!ok) {
     if (err) atomicOr(err, 1u);
-    tc::mbar_wait(&mbar, 0, 1u << 22);            // give the MMAs in flight a second chance
+    if (starve) {                                   // attach the MMAs now, then drain them
+      if (tid == 0) tc::mma_commit(&mbar);
+      tc::mbar_wait(&mbar, 0, 1u << 22);
+    } else {
+      tc::mbar_wait(&mbar, 0, 1u << 22);            // give the MMAs in flight a second chance
+    }
   }
   tc::fence_after_sync();
   if (ok) {
@@ -76,7 +84,8 @@ tc_selftest_kernel(const uint16_t* __restrict__ A, const uint16_t* __restrict__ 
 }  // namespace gdn
 
 extern "C" gdn_status gdn_selftest_tc_gemm(const uint16_t* A, const uint16_t* B, float* D, int32_t N,
-                                           int32_t K, uint32_t* dev_err, void* stream) {
+                                           int32_t K, int32_t starve_wait, uint32_t* dev_err,
+                                           void* stream) {
   if (!A || !B || !D) return GDN_ERR_INVALID;
   if (N < 16 || N > 256 || N % 16 || K < 16 || K > 128 || K % 16) return GDN_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u) return GDN_ERR_INVALID;
@@ -84,7 +93,7 @@ extern "C" gdn_status gdn_selftest_tc_gemm(const uint16_t* A, const uint16_t* B,
   cudaError_t e = cudaFuncSetAttribute(gdn::tc_selftest_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return GDN_ERR_CUDA;
-  gdn::tc_selftest_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(A, B, D, N, K,
-                                                                              dev_err);
+  gdn::tc_selftest_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
+      A, B, D, N, K, starve_wait ? 1 : 0, dev_err);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

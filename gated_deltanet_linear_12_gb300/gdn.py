@@ -71,7 +71,7 @@ def load() -> ctypes.CDLL:
             L.gdn_verify_step.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                           u32, vp, vp]
             L.gdn_commit_layers.argtypes = [cfgp, vp, i32, vp, vp, i32, i32, vp]
-            L.gdn_selftest_tc_gemm.argtypes = [vp, vp, vp, i32, i32, vp, vp]
+            L.gdn_selftest_tc_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
             for f in EXPORTS[:-1]:
                 getattr(L, f).restype = ctypes.c_int
             L.gdn_status_string.argtypes = [ctypes.c_int]
@@ -186,8 +186,10 @@ def gdn_commit_layers(cfg, views, n_layers, slot_idx, n_keep, T, *, stream=None)
         T, _stream(slot_idx, stream)))
 
 
-def gdn_selftest_tc_gemm(A, B, D, *, dev_err=None, stream=None):
-    """Diagnostic: D[128][N] = A[128][K] @ B[N][K]^T on the tensor cores (bf16 -> f32)."""
+def gdn_selftest_tc_gemm(A, B, D, *, starve_wait=False, dev_err=None, stream=None):
+    """Diagnostic: D[128][N] = A[128][K] @ B[N][K]^T on the tensor cores (bf16 -> f32).
+    starve_wait exercises the bounded-wait failure path (see gdn_selftest.h)."""
     _dense(A, B, D)
     _check("gdn_selftest_tc_gemm", load().gdn_selftest_tc_gemm(
-        _ptr(A), _ptr(B), _ptr(D), B.shape[0], A.shape[1], _ptr(dev_err), _stream(A, stream)))
+        _ptr(A), _ptr(B), _ptr(D), B.shape[0], A.shape[1], int(bool(starve_wait)),
+        _ptr(dev_err), _stream(A, stream)))

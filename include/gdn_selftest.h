@@ -20,10 +20,14 @@ extern "C" {
  * D (row-major, device), computed by one thread block with tcgen05.mma from
  * shared memory into TMEM. N in {16, 32, ..., 256}, K in {16, 32, ..., 128}.
  * dev_err (device, nullable) receives bit 1 if the completion wait timed out.
+ * starve_wait = 1 exercises that failure path without any fault: the MMAs'
+ * completion is not attached to the barrier the block waits on, so the
+ * bounded wait gives up, sets bit 1, then attaches and drains the MMAs,
+ * frees its TMEM and returns (D is left unwritten).
  * Returns GDN_ERR_INVALID for other shapes, GDN_ERR_CUDA on launch failure.
  */
 gdn_status gdn_selftest_tc_gemm(const uint16_t* A, const uint16_t* B, float* D, int32_t N,
-                                int32_t K, uint32_t* dev_err, void* stream);
+                                int32_t K, int32_t starve_wait, uint32_t* dev_err, void* stream);
 
 #ifdef __cplusplus
 }

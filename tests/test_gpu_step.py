@@ -107,9 +107,12 @@ def test_commit_all_equals_verify_then_commit_bitwise(G, orc, T):
     n_keep = torch.full((5,), T, dtype=torch.int32, device="cuda")
     G.gdn_commit_layers(Bl.cfg(G), views, 1, Bl.slot, n_keep, T)
     torch.cuda.synchronize()
-    assert np.array_equal(bits(A.out), bits(Bl.out))
-    assert np.array_equal(bits(A.S), bits(Bl.S))
+    assert np.array_equal(bits(A.S), bits(Bl.S)), "decode == verify + commit(T), bitwise"
     assert np.array_equal(bits(A.cs), bits(Bl.cs))
+    if T == 1:                       # same variant: outputs bitwise too
+        assert np.array_equal(bits(A.out), bits(Bl.out))
+    else:                            # verify uses the tensor cores: rounding only
+        check_bf16(to_np(A.out), to_np(Bl.out), what="decode vs verify outputs")
     # and against the oracle
     out, _, cs, st = _oracle_verify(orc, inp, commit_all=True)
     check_bf16(to_np(A.out), out, what="decode out")

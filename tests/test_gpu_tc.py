@@ -38,3 +38,21 @@ def test_tc_gemm_matches_host(G, N, K):
     got = _gemm(G, A, B)
     scale = np.abs(syn.bf16_bits_to_f32(A)).astype(np.float64) @ np.abs(syn.bf16_bits_to_f32(B)).astype(np.float64).T
     assert np.all(np.abs(got - ref) <= 1e-5 * scale + 1e-30)
+
+
+def test_bounded_wait_gives_up_and_reports(G):
+    """Failure detection without a fault: the block waits on a barrier nothing
+    arrives on; the wait must give up, report, release TMEM and return, and the
+    context must stay usable (the next GEMM is exact)."""
+    rng = np.random.default_rng(7)
+    A = syn.f32_to_bf16_bits(rng.standard_normal((128, 32)).astype(np.float32))
+    B = syn.f32_to_bf16_bits(rng.standard_normal((16, 32)).astype(np.float32))
+    D = torch.full((128, 16), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G.gdn_selftest_tc_gemm(to_dev(A), to_dev(B), D, starve_wait=True, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+    assert torch.isnan(D).all(), "a block that gave up must not write results"
+    ref = syn.bf16_bits_to_f32(A).astype(np.float64) @ syn.bf16_bits_to_f32(B).astype(np.float64).T
+    got = _gemm(G, A, B)
+    assert np.allclose(got, ref, rtol=1e-5, atol=1e-5)
