@@ -33,7 +33,7 @@ namespace {
 
 constexpr int PT = 256;
 constexpr int C64 = CHUNK;           // 64
-constexpr int AP = C64 + 1;          // row stride of the f32 64x64 tables
+constexpr int AP = C64 + 4;          // row stride of the f32 64x64 tables (16-byte rows)
 
 // shared memory map (bytes); K-major tiles use tc::kmajor_offset
 constexpr int SM_SHI = 0;                          // S hi   128x128 bf16 (MMA1 A)
@@ -69,6 +69,21 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+// 16-byte global -> shared copy that bypasses registers; src_bytes = 0 fills
+// the destination with zeros (padding past the sequence end).
+__device__ __forceinline__ void cp_async16(uint8_t* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // One row (K = 64 values) of a K-major tile with `rows` rows, as bf16 hi | lo.
 __device__ __forceinline__ void put_row64(uint8_t* hi_tile, uint8_t* lo_tile, int row, int rows,
@@ -215,51 +230,88 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     return __syncthreads_or(!ok) == 0;
   };
 
+  // Copies of a chunk's keys and queries (into the K-major [K;Q] tile), values
+  // (row-major, into the Tinv tiles' space) and raw gates, in flight while the
+  // previous chunk finishes. Rows past the sequence end are zero-filled.
+  float* al_raw = la_s;                                  // raw alpha until log2 is taken
+  auto prefetch = [&](int64_t pc0, int pm) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {                        // keys / queries: a warp = 32 tokens
+      const int it = tid + k * PT, t = it & 63, part = it >> 6, isq = part >> 4, w8 = part & 15;
+      const int tt = t < pm ? t : 0;
+      cp_async16(KQ + tc::kmajor_offset(isq * 64 + t, 8 * w8, 128),
+                 qkv + (pc0 + tt) * C + (isq ? hq : Hk + hq) * D + 8 * w8, t < pm ? 16u : 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {                        // values: a warp = 2 tokens
+      const int iv = tid + k * PT, t = iv >> 4, w8 = iv & 15;
+      const int tt = t < pm ? t : 0;
+      cp_async16(TI + (t * D + 8 * w8) * 2, qkv + (pc0 + tt) * C + (2 * Hk + h) * D + 8 * w8,
+                 t < pm ? 16u : 0u);
+    }
+    if (tid < C64) {
+      const int t = tid, tt = t < pm ? t : 0;
+      cp_async4(al_raw + t, p.alpha + (pc0 + tt) * Hv + h, t < pm ? 4u : 0u);
+      cp_async4(b_s + t, p.beta + (pc0 + tt) * Hv + h, t < pm ? 4u : 0u);
+    }
+    cp_async_commit();
+  };
+
+  // z-gated RMSNorm of a chunk's outputs (16 lanes per token). It runs while
+  // the next chunk's first products are on the tensor core: it reads only the
+  // output buffer, which the next chunk overwrites after that wait.
+  auto epilogue = [&](int64_t ec0, int em) {
+      constexpr int NIT = C64 / (PT / 16);
+      float zv[NIT][8];
+      const int l16 = tid & 15;
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        const int t = it * (PT / 16) + (tid >> 4);
+        if (t < em) load8<BF16>(p.z, (ec0 + t) * Hv * D + (int64_t)h * D + l16 * 8, zv[it]);
+      }
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        const int t = it * (PT / 16) + (tid >> 4);
+        const bool live = t < em;
+        float o[8];
+        const float4 u0 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16];
+        const float4 u1 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16 + 1];
+        o[0] = u0.x; o[1] = u0.y; o[2] = u0.z; o[3] = u0.w;
+        o[4] = u1.x; o[5] = u1.y; o[6] = u1.z; o[7] = u1.w;
+        const float ss = head_sum_sq16(o);
+        if (live) {
+          const float r = inv_norm(__fmul_rn(ss, 1.0f / D), p.eps);
+          float res[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu_gate(zv[it][j]));
+          store8<BF16>(p.out, (ec0 + t) * Hv * D + (int64_t)h * D + l16 * 8, res);
+        }
+      }
+  };
+
+  int64_t prev_c0 = -1;
+  int prev_m = 0;
+  if (seq0 < seq1) prefetch(seq0, (int)(seq1 - seq0 < C64 ? seq1 - seq0 : C64));
   for (int64_t c0 = seq0; c0 < seq1; c0 += C64) {
     const int m = (int)(seq1 - c0 < C64 ? seq1 - c0 : C64);
 
-    // ---- (a) stage keys and queries ([K;Q] K-major, K^T K-major), values
-    //          (row-major, in the Tinv tiles' space until (d)) and gates.
-    //          All 12 loads of a thread are issued before any store.
-    {
-      uint4 pc[12];
+    // ---- (a) the prefetched chunk: wait for it, transpose the keys into K^T,
+    //          take log2 of the gates (alpha = 1 past the end: zero-filled raw
+    //          alpha is mapped to log2 = 0)
+    cp_async_wait_all();
+    __syncthreads();
 #pragma unroll
-      for (int k = 0; k < 12; ++k) {
-        const int it = tid + k * PT;                     // 0..2047 keys/queries, then values
-        pc[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (k < 8) {
-          const int t = it >> 5, part = it & 31, isq = part >> 4, w8 = part & 15;
-          if (t < m)
-            pc[k] = *reinterpret_cast<const uint4*>(qkv + (c0 + t) * C + (isq ? hq : Hk + hq) * D + 8 * w8);
-        } else {
-          const int iv = it - 2048, t = iv >> 4, w8 = iv & 15;
-          if (t < m) pc[k] = *reinterpret_cast<const uint4*>(qkv + (c0 + t) * C + (2 * Hk + h) * D + 8 * w8);
-        }
-      }
+    for (int k = 0; k < 4; ++k) {                        // key pieces: a warp = 32 tokens
+      const int it = tid + k * PT, t = it & 63, w8 = it >> 6;
+      const uint4 pc = *reinterpret_cast<const uint4*>(KQ + tc::kmajor_offset(t, 8 * w8, 128));
+      const uint32_t wv[4] = {pc.x, pc.y, pc.z, pc.w};
 #pragma unroll
-      for (int k = 0; k < 12; ++k) {
-        const int it = tid + k * PT;
-        if (k < 8) {
-          const int t = it >> 5, part = it & 31, isq = part >> 4, w8 = part & 15;
-          st16(KQ + tc::kmajor_offset(isq * 64 + t, 8 * w8, 128), pc[k]);
-          if (!isq) {
-            const uint32_t wv[4] = {pc[k].x, pc[k].y, pc[k].z, pc[k].w};
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint16_t*>(KT + tc::kmajor_offset(8 * w8 + u, t, 128)) =
-                  (uint16_t)(wv[u >> 1] >> (16 * (u & 1)));
-          }
-        } else {
-          const int iv = it - 2048, t = iv >> 4, w8 = iv & 15;
-          st16(TI + (t * D + 8 * w8) * 2, pc[k]);
-        }
-      }
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint16_t*>(KT + tc::kmajor_offset(8 * w8 + u, t, 128)) =
+            (uint16_t)(wv[u >> 1] >> (16 * (u & 1)));
     }
-    if (tid < C64) {
-      const int t = tid;
-      la_s[t] = t < m ? log2f(p.alpha[(c0 + t) * Hv + h]) : 0.f;
-      b_s[t] = t < m ? p.beta[(c0 + t) * Hv + h] : 0.f;
-    }
+    if (tid < C64) la_s[tid] = tid < m ? log2f(al_raw[tid]) : 0.f;
     tc::fence_async_smem();
     __syncthreads();
 
@@ -278,6 +330,7 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     }
     __syncthreads();
     if (tid < C64) c_s[tid] = ex2(g2_s[C64 - 1] - g2_s[tid]);
+    if (prev_c0 >= 0) epilogue(prev_c0, prev_m);         // previous chunk, overlapped
     if (!commit_and_wait()) { timed_out = true; break; }
 
     // ---- (c) tables from G (owners); R^T rows from P^T (helpers)
@@ -319,45 +372,79 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     __syncthreads();
 
     // ---- (d) Tinv = (I + A)^-1 by recursive doubling over 16/32/64 blocks
-    if (tid < C64) {
-      const int j = tid, blk = j & ~15;
-      TB[j * AP + j] = 1.f;
-      for (int t = j + 1; t < blk + 16; ++t) {
+    if (tid < C64) {                                     // column j of its 16x16 diagonal block,
+      const int j = tid, blk = j & ~15, jl = j & 15;     // kept in registers (zeros above jl)
+      float y[16];
+#pragma unroll
+      for (int tl = 0; tl < 16; ++tl) {
         float acc = 0.f;
-        for (int u = j; u < t; ++u) acc = __fmaf_rn(AB[t * AP + u], TB[u * AP + j], acc);
-        TB[t * AP + j] = -acc;
+#pragma unroll
+        for (int ul = 0; ul < tl; ++ul) acc = __fmaf_rn(AB[(blk + tl) * AP + blk + ul], y[ul], acc);
+        y[tl] = tl < jl ? 0.f : (tl == jl ? 1.f : -acc);
       }
+#pragma unroll
+      for (int tl = 0; tl < 16; ++tl) TB[(blk + tl) * AP + j] = y[tl];
     }
     __syncthreads();
+    // levels 2 and 3: products with the left factor's rows read as float4
+    // (the zero parts of the block-triangular factors add exact zeros)
     for (int e = tid; e < 512; e += PT) {                // level 2: A21 Y11 per 32-block
       const int P = e >> 8, ent = e & 255, r = ent >> 4, j = ent & 15, base = 32 * P;
+      const float4* arow = reinterpret_cast<const float4*>(AB + (base + 16 + r) * AP + base);
       float acc = 0.f;
-#pragma unroll 4
-      for (int u = 0; u < 16; ++u)
-        acc = __fmaf_rn(AB[(base + 16 + r) * AP + base + u], TB[(base + u) * AP + base + j], acc);
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const float4 a = arow[u4];
+        acc = __fmaf_rn(a.x, TB[(base + 4 * u4) * AP + base + j], acc);
+        acc = __fmaf_rn(a.y, TB[(base + 4 * u4 + 1) * AP + base + j], acc);
+        acc = __fmaf_rn(a.z, TB[(base + 4 * u4 + 2) * AP + base + j], acc);
+        acc = __fmaf_rn(a.w, TB[(base + 4 * u4 + 3) * AP + base + j], acc);
+      }
       tmp[e] = acc;
     }
     __syncthreads();
     for (int e = tid; e < 512; e += PT) {
       const int P = e >> 8, ent = e & 255, r = ent >> 4, j = ent & 15, base = 32 * P;
+      const float4* yrow = reinterpret_cast<const float4*>(TB + (base + 16 + r) * AP + base + 16);
       float acc = 0.f;
-#pragma unroll 4
-      for (int u = 0; u < 16; ++u)
-        acc = __fmaf_rn(TB[(base + 16 + r) * AP + base + 16 + u], tmp[P * 256 + u * 16 + j], acc);
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const float4 a = yrow[u4];
+        acc = __fmaf_rn(a.x, tmp[P * 256 + (4 * u4) * 16 + j], acc);
+        acc = __fmaf_rn(a.y, tmp[P * 256 + (4 * u4 + 1) * 16 + j], acc);
+        acc = __fmaf_rn(a.z, tmp[P * 256 + (4 * u4 + 2) * 16 + j], acc);
+        acc = __fmaf_rn(a.w, tmp[P * 256 + (4 * u4 + 3) * 16 + j], acc);
+      }
       TB[(base + 16 + r) * AP + base + j] = -acc;
     }
     __syncthreads();
     for (int e = tid; e < 1024; e += PT) {               // level 3: A[32:,:32] Y[:32,:32]
       const int r = e >> 5, j = e & 31;
+      const float4* arow = reinterpret_cast<const float4*>(AB + (32 + r) * AP);
       float acc = 0.f;
-      for (int u = j & ~15; u < 32; ++u) acc = __fmaf_rn(AB[(32 + r) * AP + u], TB[u * AP + j], acc);
+#pragma unroll
+      for (int u4 = 0; u4 < 8; ++u4) {
+        const float4 a = arow[u4];
+        acc = __fmaf_rn(a.x, TB[(4 * u4) * AP + j], acc);
+        acc = __fmaf_rn(a.y, TB[(4 * u4 + 1) * AP + j], acc);
+        acc = __fmaf_rn(a.z, TB[(4 * u4 + 2) * AP + j], acc);
+        acc = __fmaf_rn(a.w, TB[(4 * u4 + 3) * AP + j], acc);
+      }
       tmp[e] = acc;
     }
     __syncthreads();
     for (int e = tid; e < 1024; e += PT) {
       const int r = e >> 5, j = e & 31;
+      const float4* yrow = reinterpret_cast<const float4*>(TB + (32 + r) * AP + 32);
       float acc = 0.f;
-      for (int u = 0; u <= r; ++u) acc = __fmaf_rn(TB[(32 + r) * AP + 32 + u], tmp[u * 32 + j], acc);
+#pragma unroll
+      for (int u4 = 0; u4 < 8; ++u4) {
+        const float4 a = yrow[u4];
+        acc = __fmaf_rn(a.x, tmp[(4 * u4) * 32 + j], acc);
+        acc = __fmaf_rn(a.y, tmp[(4 * u4 + 1) * 32 + j], acc);
+        acc = __fmaf_rn(a.z, tmp[(4 * u4 + 2) * 32 + j], acc);
+        acc = __fmaf_rn(a.w, tmp[(4 * u4 + 3) * 32 + j], acc);
+      }
       TB[(32 + r) * AP + j] = -acc;
     }
     __syncthreads();
@@ -407,6 +494,11 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     }
     if (!commit_and_wait()) { timed_out = true; break; }
 
+    if (c0 + C64 < seq1) {                               // next chunk's inputs: KQ and TI are free
+      const int64_t n0 = c0 + C64;
+      prefetch(n0, (int)(seq1 - n0 < C64 ? seq1 - n0 : C64));
+    }
+
     // ---- (h) owners: o = G (S0 q) + O^T into the output buffer (the RD region
     //          is free now); helpers: S = G_last S + dS, TMEM and hi/lo tiles
     if (owner) {
@@ -443,39 +535,10 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     }
     tc::fence_before_sync();
     __syncthreads();
-
-    // ---- (i) z-gated RMSNorm of the outputs: 16 lanes per token (z prefetched)
-    {
-      constexpr int NIT = C64 / (PT / 16);
-      float zv[NIT][8];
-      const int l16 = tid & 15;
-#pragma unroll
-      for (int it = 0; it < NIT; ++it) {
-        const int t = it * (PT / 16) + (tid >> 4);
-        if (t < m) load8<BF16>(p.z, (c0 + t) * Hv * D + (int64_t)h * D + l16 * 8, zv[it]);
-      }
-#pragma unroll
-      for (int it = 0; it < NIT; ++it) {
-        const int t = it * (PT / 16) + (tid >> 4);
-        const bool live = t < m;
-        float o[8];
-        const float4 u0 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16];
-        const float4 u1 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16 + 1];
-        o[0] = u0.x; o[1] = u0.y; o[2] = u0.z; o[3] = u0.w;
-        o[4] = u1.x; o[5] = u1.y; o[6] = u1.z; o[7] = u1.w;
-        const float ss = head_sum_sq16(o);
-        if (live) {
-          const float r = inv_norm(__fmul_rn(ss, 1.0f / D), p.eps);
-          float res[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu_gate(zv[it][j]));
-          store8<BF16>(p.out, (c0 + t) * Hv * D + (int64_t)h * D + l16 * 8, res);
-        }
-      }
-    }
-    __syncthreads();
+    prev_c0 = c0;
+    prev_m = m;
   }
+  if (!timed_out && prev_c0 >= 0) epilogue(prev_c0, prev_m);   // the last chunk
 
   if (timed_out) {
     if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
