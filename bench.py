@@ -71,6 +71,40 @@ def fp32_alu_peak_tflops(sm_mhz, n_sm=152, lanes=128):
 
 
 # ----------------------------------------------------------------------------- helpers
+KERNEL_SOURCES = {
+    "prefill_tc_kernel": ["gated_deltanet_linear_12_gb300/csrc/prefill_tc.cu",
+                          "gated_deltanet_linear_12_gb300/csrc/tc.cuh",
+                          "gated_deltanet_linear_12_gb300/csrc/common.cuh"],
+    "conv_fwd_kernel": ["gated_deltanet_linear_12_gb300/csrc/conv.cu",
+                        "gated_deltanet_linear_12_gb300/csrc/common.cuh"],
+    "step_kernel": ["gated_deltanet_linear_12_gb300/csrc/step.cu",
+                    "gated_deltanet_linear_12_gb300/csrc/tc.cuh",
+                    "gated_deltanet_linear_12_gb300/csrc/common.cuh"],
+}
+
+
+def source_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu record of this kernel and
+    workload, or None when the kernel's source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(f"{kernel}/{workload}")
+    if not rec or rec.get("source_hash") != source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -435,17 +469,30 @@ def main():
                       "GB/s": round(W.bytes["commit"] / max(b_avg, 1e-9) / 1e6, 1)}
                 kb["frac_hbm"] = round(kb["GB/s"] / peaks["hbm_gbs"], 4)
                 kernels[names[1]] = kb
-            roof = {"kernel": names[0] + " (36 launches)", "bound": "hbm", "achieved": ka["GB/s"],
+            roof = {"kernel": "step_kernel (verify" + (", every token accepted" if W.decode else "")
+                              + "; 36 launches)", "bound": "hbm", "achieved": ka["GB/s"],
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ka["frac_hbm"],
-                    "traffic": None, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+                    "traffic": ncu_traffic("step_kernel", W.name + f"/T{W.T}"),
+                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
             value = tokens_total * W.LAYERS / (ms_max * 1e-3)
         else:
             alu_peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
             pf_tflops = W.flops["prefill"] / (b_avg * 1e-3) / 1e12
             pf_gbs = W.bytes["prefill"] / (b_avg * 1e-3) / 1e9
             conv_gbs = W.bytes["conv"] / (a_avg * 1e-3) / 1e9
-            if b_avg >= a_avg:
-                roof = {"kernel": "prefill_ffma_kernel", "bound": "alu",
+            pf_name = "prefill_tc_kernel" if W.inp["act"] == "bf16" else "prefill_ffma_kernel"
+            if b_avg >= a_avg and pf_name == "prefill_tc_kernel":
+                peak = peaks.get("bf16_tflops", 1920.0)
+                roof = {"kernel": pf_name, "bound": "tensor", "achieved": round(pf_tflops, 3),
+                        "peak": peak, "unit": "TFLOP/s", "frac": round(pf_tflops / peak, 4),
+                        "traffic": ncu_traffic(pf_name, W.name),
+                        "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)",
+                        "algorithmic_flops_per_launch": W.flops["prefill"],
+                        "algorithmic_bytes_per_launch": W.bytes["prefill"],
+                        "hbm_gbs": round(pf_gbs, 1),
+                        "hbm_frac": round(pf_gbs / peaks["hbm_gbs"], 4)}
+            elif b_avg >= a_avg:
+                roof = {"kernel": pf_name, "bound": "alu",
                         "achieved": round(pf_tflops, 3), "peak": round(alu_peak, 1),
                         "unit": "TFLOP/s", "frac": round(pf_tflops / alu_peak, 4), "traffic": None,
                         "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x "
@@ -455,14 +502,15 @@ def main():
             else:
                 roof = {"kernel": "conv_fwd_kernel", "bound": "hbm", "achieved": round(conv_gbs, 1),
                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(conv_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                        "frac": round(conv_gbs / peaks["hbm_gbs"], 4),
+                        "traffic": ncu_traffic("conv_fwd_kernel", W.name),
                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
             kernels = {
                 "conv_fwd_kernel": {"ms": round(a_avg, 4), "bytes": W.bytes["conv"],
                                     "GB/s": round(conv_gbs, 1),
                                     "frac_hbm": round(conv_gbs / peaks["hbm_gbs"], 4)},
-                "prefill_ffma_kernel": {"ms": round(b_avg, 4), "bytes": W.bytes["prefill"],
-                                        "GB/s": round(pf_gbs, 1), "TFLOP/s": round(pf_tflops, 3)},
+                pf_name: {"ms": round(b_avg, 4), "bytes": W.bytes["prefill"],
+                          "GB/s": round(pf_gbs, 1), "TFLOP/s": round(pf_tflops, 3)},
             }
             value = tokens_total / (ms_max * 1e-3)
         e2e_val = value * ms_max / float(e2e_t.item())
