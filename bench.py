@@ -95,14 +95,15 @@ def source_hash(kernel):
 def ncu_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu record of this kernel and
     workload, or None when the kernel's source changed since the capture."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        rec = json.load(f).get(f"{kernel}/{workload}")
-    if not rec or rec.get("source_hash") != source_hash(kernel):
-        return None
-    return rec.get("dram_bytes_per_launch")
+        for line in f:
+            parts = line.split()
+            if len(parts) == 3 and not line.startswith("#") and parts[0] == f"{kernel}/{workload}":
+                return int(parts[2]) if parts[1] == source_hash(kernel) else None
+    return None
 
 
 def load_peaks():
