@@ -123,11 +123,17 @@ gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const float
   return from_cuda(gdn::launch_prefill(a, cfg->act, static_cast<cudaStream_t>(stream)));
 }
 
+int64_t gdn_verify_workspace_bytes(const gdn_config* cfg, int32_t B, int32_t T) {
+  if (check_cfg(cfg) != GDN_OK || B < 0 || T < 1 || T > GDN_MAX_DRAFT) return -1;
+  return gdn::verify_ws_layout(B, T, cfg->n_qk_heads, cfg->n_v_heads, cfg->act).total;
+}
+
 gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* conv_w,
                            void* conv_state, float* state, const float* alpha,
                            const float* beta, const void* z, const float* norm_w, void* out,
                            const int32_t* slot_idx, int32_t B, int32_t T, uint32_t flags,
-                           void* postconv_out, void* stream) {
+                           void* postconv_out, void* workspace, int64_t workspace_bytes,
+                           void* stream) {
   gdn_status st = check_cfg(cfg);
   if (st != GDN_OK) return st;
   if (B < 0 || T < 1 || T > GDN_MAX_DRAFT) return GDN_ERR_INVALID;
@@ -138,17 +144,28 @@ gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* con
       !slot_idx)
     return GDN_ERR_INVALID;
   if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_state) || !aligned16(state) ||
-      !aligned16(z) || !aligned16(out) || (postconv_out && !aligned16(postconv_out)))
+      !aligned16(z) || !aligned16(out) || !aligned16(norm_w) ||
+      (postconv_out && !aligned16(postconv_out)))
     return GDN_ERR_INVALID;
   const size_t es = esize(cfg->act);
   const size_t HvD = (size_t)cfg->n_v_heads * GDN_HEAD_DIM, nt = (size_t)B * T;
   if (overlap(out, nt * HvD * es, x, nt * channels(cfg) * es) ||
       overlap(out, nt * HvD * es, z, nt * HvD * es))
     return GDN_ERR_INVALID;
+  if (!(flags & GDN_VERIFY_COMMIT_ALL)) {
+    const int64_t need = gdn::verify_ws_layout(B, T, cfg->n_qk_heads, cfg->n_v_heads, cfg->act).total;
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return GDN_ERR_INVALID;
+    const size_t wb = (size_t)workspace_bytes;
+    if (overlap(workspace, wb, out, nt * HvD * es) || overlap(workspace, wb, x, nt * channels(cfg) * es) ||
+        overlap(workspace, wb, z, nt * HvD * es) ||
+        (postconv_out && overlap(workspace, wb, postconv_out, nt * channels(cfg) * es)))
+      return GDN_ERR_INVALID;
+  }
   gdn::StepArgs a{x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, postconv_out,
                   slot_idx, nullptr, nullptr, B, T, cfg->n_qk_heads, cfg->n_v_heads,
                   cfg->n_slots, cfg->eps, cfg->q_scale, cfg->dev_err};
-  return from_cuda(gdn::launch_verify(a, (flags & GDN_VERIFY_COMMIT_ALL) != 0, cfg->act,
+  return from_cuda(gdn::launch_verify(a, (flags & GDN_VERIFY_COMMIT_ALL) != 0, cfg->act, workspace,
                                       static_cast<cudaStream_t>(stream)));
 }
 

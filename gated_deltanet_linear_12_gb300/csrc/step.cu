@@ -1,6 +1,7 @@
-// Speculative verify (T = 1..8 draft tokens), decode (verify with every draft
-// token accepted, state advanced in place) and the batched accepted-prefix
-// commit across layers.
+// Decode (the verify of T draft tokens with every token accepted, state and
+// conv_state advanced in place) and the batched accepted-prefix commit across
+// layers. The read-only verify is in verify.cu and follows the same order of
+// arithmetic.
 //
 // Source: "Strata PR #3226" ("Summary": verify forward launched once per GDN
 // layer; the 2-launch batched commit of conv_state and recurrent state across 36
@@ -20,21 +21,19 @@
 // rank-n update. Value rows of S are independent, so each thread owns two rows
 // x 32 columns of S0 in registers and the rows' deltas.
 //
-// One template body serves the three modes, so the deltas and the committed
-// state are computed by the same instructions in verify+commit and in decode:
-// the bitwise agreement is by construction. No atomics, no inter-block waits.
+// One template body serves both modes, so the deltas and the committed state
+// are computed by the same instructions in verify+commit and in decode: the
+// bitwise agreement is by construction. No atomics, no inter-block waits.
 //
-// conv_state ownership: in the committing modes a block owns a whole q/k head
-// group (the q and k heads and the Hv/Hk v heads that read them), so the block
-// that reads a channel's conv_state rows is the only one that rewrites them,
-// after a block barrier. The read-only verify mode uses one block per v head.
+// conv_state ownership: a block owns a whole q/k head group (the q and k heads
+// and the Hv/Hk v heads that read them), so the block that reads a channel's
+// conv_state rows is the only one that rewrites them, after a block barrier.
 #include "common.cuh"
 #include "launch.h"
-#include "tc.cuh"
 
 namespace gdn {
 
-enum StepMode { VERIFY = 0, VERIFY_COMMIT_ALL = 1, COMMIT = 2 };
+enum StepMode { VERIFY_COMMIT_ALL = 1, COMMIT = 2 };
 
 constexpr int STEP_THREADS = 256;
 constexpr int MAX_HEADS = 16;                    // v heads per block (Hv / Hk limit)
@@ -116,19 +115,9 @@ __device__ __forceinline__ void rows_dot(const float4 (&S)[2][8], const float* v
   r1 = a1;
 }
 
-// Tensor-core variant (TC): the 2T state dot products of every value row come
-// from one tcgen05 product S0 [k_0..k_7 ; q_0..q_7]^T (M = 128 rows, N = 16,
-// K = 128) with S0 entering as bf16 hi + lo parts (two passes, relative error
-// near 2^-16) and the keys/queries exact in bf16; thread i < 128 then owns
-// value row i (TMEM lane i) for the deltas and outputs. The f32 copy of S0
-// stays in registers (coalesced layout) for the state commit.
-constexpr int TC_REGION = 32768 * 2 + 4096 + MAXT * D * 4;   // S hi, S lo, B tile, deltas
-
-template <int A, int MODE, bool TC>
+template <int A, int MODE>
 __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  float* smem = reinterpret_cast<float*>(smem_raw + (TC ? TC_REGION : 0));
-  constexpr bool COMMITS = MODE != VERIFY;
+  extern __shared__ __align__(16) float smem[];
   constexpr bool OUTPUTS = MODE != COMMIT;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.y;
@@ -164,10 +153,10 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
     if (n == 0) return;
   }
 
-  // Heads of this block: VERIFY one v head; the committing modes a whole group.
-  const int hq = (MODE == VERIFY) ? blockIdx.x / G : blockIdx.x;   // q/k head
-  const int h0 = (MODE == VERIFY) ? blockIdx.x : blockIdx.x * G;   // first v head
-  const int nh = (MODE == VERIFY) ? 1 : G;                         // v heads here
+  // Heads of this block: a whole q/k head group.
+  const int hq = blockIdx.x;                                       // q/k head
+  const int h0 = blockIdx.x * G;                                   // first v head
+  const int nh = G;                                                // v heads here
 
   // The first head's state rows go in flight before anything else, so the
   // 64 KiB read overlaps the conv and table phases (coalesced: 4 lanes cover
@@ -182,26 +171,6 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
 #pragma unroll
       for (int m = 0; m < 8; ++m)
         S[rr][m] = reinterpret_cast<const float4*>(Sg0 + (int64_t)(row0 + rr) * D)[4 * m + cg];
-  }
-
-  // tensor-core resources: TMEM accumulator (32 columns), completion barrier
-  uint8_t* SHI = smem_raw;
-  uint8_t* SLO = smem_raw + 32768;
-  uint8_t* BT = smem_raw + 65536;                          // [k ; q] 16 x 128 bf16
-  float* dtab = reinterpret_cast<float*>(smem_raw + 65536 + 4096);   // [8][128] deltas
-  __shared__ uint64_t tc_bar;
-  __shared__ uint32_t tc_slot;
-  uint32_t tbase = 0, tc_phase = 0;
-  if constexpr (TC) {
-    if (tid == 0) tc::mbar_init(&tc_bar, 1);
-    if (warp == 0) {
-      tc::tmem_alloc(&tc_slot, 32);
-      tc::tmem_relinquish();
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    tbase = tc_slot;
   }
 
   // shared memory: q[T][D], k[T][D], v[nh][T][D], o[T][D], small tables
@@ -266,7 +235,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
   __syncthreads();
 
   // ---- conv_state commit: last 3 rows of (old rows ++ draft rows 0..n-1)
-  if constexpr (COMMITS) {
+  {
     constexpr int MAXI = 4;                               // (2 + G) * 48 <= 4 * 256
     const int groups = (2 + nh) * 16;
     const int items = KS * groups;
@@ -304,24 +273,6 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
     else if (OUTPUTS) { const float d = warp_dot128(q_s + t * D, k_s + s * D); if (lane == 0) qk_s[t * MAXT + s] = d; }
   }
 
-
-  if constexpr (TC) {                                      // [k_0..k_7 ; q_0..q_7] as bf16
-    const int row = tid >> 4, w8 = tid & 15;               // 16 rows x 16 pieces
-    const int t = row & 7;
-    const bool live = t < n && (row < 8 || OUTPUTS);
-    const float* src = (row < 8 ? k_s : q_s) + t * D + 8 * w8;
-    float v8[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v8[j] = live ? src[j] : 0.f;
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v8[2 * j], v8[2 * j + 1]);
-      w[j] = *reinterpret_cast<const uint32_t*>(&b2);
-    }
-    *reinterpret_cast<uint4*>(BT + tc::kmajor_offset(row, 8 * w8, 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  bool tc_failed = false;
 
   for (int g = 0; g < nh; ++g) {
     const int h = h0 + g;
@@ -361,83 +312,12 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
         for (int m = 0; m < 8; ++m)
           S[rr][m] = reinterpret_cast<const float4*>(Sg + (int64_t)(row0 + rr) * D)[4 * m + cg];
     }
-    if constexpr (TC) {                                    // S0 as bf16 hi / lo K-major tiles
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const float4 f = S[rr][m];
-          const __nv_bfloat162 h01 = __floats2bfloat162_rn(f.x, f.y);
-          const __nv_bfloat162 h23 = __floats2bfloat162_rn(f.z, f.w);
-          const float2 g01 = __bfloat1622float2(h01), g23 = __bfloat1622float2(h23);
-          const __nv_bfloat162 l01 = __floats2bfloat162_rn(f.x - g01.x, f.y - g01.y);
-          const __nv_bfloat162 l23 = __floats2bfloat162_rn(f.z - g23.x, f.w - g23.y);
-          const uint32_t off = tc::kmajor_offset(row0 + rr, 16 * m + 4 * cg, 128);
-          *reinterpret_cast<uint2*>(SHI + off) =
-              make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
-          *reinterpret_cast<uint2*>(SLO + off) =
-              make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
-        }
-      tc::fence_async_smem();
-      tc::fence_before_sync();
-    }
     __syncthreads();                                      // tables ready
 
     float d0[MAXT], d1[MAXT];
     const float* vh = v_s + (size_t)g * MAXT * D;
-    if constexpr (TC) {
-      // S0 [k ; q]^T on the tensor core, then row i = tid (< 128) from TMEM lane i
-      if (tid == 0) {
-        tc::fence_after_sync();
-        const uint32_t sh = tc::smem_u32(SHI), sl = tc::smem_u32(SLO), bt = tc::smem_u32(BT);
-        const uint32_t id = tc::idesc_bf16_f32(128, 16);
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tbase, tc::smem_desc(sh + ks * 4096, 2048, 128),
-                       tc::smem_desc(bt + ks * 512, 256, 128), id, ks > 0);
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tbase, tc::smem_desc(sl + ks * 4096, 2048, 128),
-                       tc::smem_desc(bt + ks * 512, 256, 128), id, 1);
-        tc::mma_commit(&tc_bar);
-      }
-      const bool ok = tc::mbar_wait(&tc_bar, tc_phase, 1u << 24);
-      if (ok) tc_phase ^= 1;
-      tc::fence_after_sync();
-      if (__syncthreads_or(!ok)) { tc_failed = true; break; }
-      if (tid < 128) {
-        float acc[16];
-        tc::tmem_ld16(tbase + ((uint32_t)(32 * warp) << 16), acc);
-        const int i = tid;
-        float dr[MAXT];
-#pragma unroll
-        for (int t = 0; t < MAXT; ++t) {
-          if (t < n) {
-            const float bt = b_s[t], bgt = bg_s[t];
-            float r = __fmaf_rn(-bgt, acc[t], __fmul_rn(bt, vh[t * D + i]));
-#pragma unroll
-            for (int u = 0; u < t; ++u) r = __fmaf_rn(-A_s[t * MAXT + u], dr[u], r);
-            dr[t] = r;
-            dtab[t * D + i] = r;
-            if constexpr (OUTPUTS) {
-              float o = __fmul_rn(g_s[t], acc[8 + t]);
-#pragma unroll
-              for (int u = 0; u <= t; ++u) o = __fmaf_rn(Oc_s[t * MAXT + u], dr[u], o);
-              o_s[t * D + i] = __fmul_rn(o, p.q_scale);
-            }
-          }
-        }
-      }
-      tc::fence_before_sync();
-      __syncthreads();                                    // deltas and outputs in smem
-#pragma unroll
-      for (int t = 0; t < MAXT; ++t) {
-        if (t < n) { d0[t] = dtab[t * D + row0]; d1[t] = dtab[t * D + row0 + 1]; }
-      }
-    }
 #pragma unroll
     for (int t = 0; t < MAXT; ++t) {
-      if (TC) break;
       if (t < n) {
         float sk0, sk1;
         rows_dot(S, k_s + t * D, cg, sk0, sk1);
@@ -472,7 +352,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
     }
 
     // state commit: S_n = g_{n-1} S0 + sum_s r(n-1,s) d_s k_s^T, in place
-    if constexpr (COMMITS) {
+    {
       const float gl = g_s[n - 1];
       float e0[MAXT], e1[MAXT];
 #pragma unroll
@@ -529,57 +409,34 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
       }
     }
   }
-  if constexpr (TC) {
-    if (tc_failed) {
-      if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
-      tc::mbar_wait(&tc_bar, tc_phase, 1u << 24);          // the pending phase: work in flight
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tbase, 32);
-  }
 }
 
-size_t step_smem_bytes(int nh, bool tc) {
-  return (tc ? TC_REGION : 0) +
-         sizeof(float) * ((size_t)(3 + nh) * MAXT * D + 4 * MAXT * MAXT + 4 * MAXT +
+size_t step_smem_bytes(int nh) {
+  return sizeof(float) * ((size_t)(3 + nh) * MAXT * D + 4 * MAXT * MAXT + 4 * MAXT +
                           2 * MAXT * MAX_HEADS);
 }
 
-template <int A, int MODE, bool TC>
-static cudaError_t launch_variant(const StepArgs& a, dim3 grid, int nh, cudaStream_t stream) {
-  const size_t smem = step_smem_bytes(nh, TC);
+// Decode and the batched commit run the same body on the CUDA cores (n accepted
+// key dots per state row, no query dots for the commit), so decode and
+// verify + commit leave bitwise equal states.
+template <int A, int MODE>
+static cudaError_t launch_mode(const StepArgs& a, dim3 grid, int nh, cudaStream_t stream) {
+  const size_t smem = step_smem_bytes(nh);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(step_kernel<A, MODE, TC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(step_kernel<A, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
   }
-  step_kernel<A, MODE, TC><<<grid, STEP_THREADS, smem, stream>>>(a);
+  step_kernel<A, MODE><<<grid, STEP_THREADS, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
-// The read-only verify of two or more bf16 draft tokens uses the tensor-core
-// variant (its 2T dot products per state row dominate); the committing modes
-// (n accepted key dots per row, no query dots) and T = 1 use CUDA cores. The
-// two committing modes always share a variant, so decode and verify + commit
-// leave bitwise equal states; verify outputs at T >= 2 differ from decode's
-// by rounding only.
-template <int A, int MODE>
-static cudaError_t launch_mode(const StepArgs& a, dim3 grid, int nh, cudaStream_t stream) {
-  if (A == BF16 && MODE == VERIFY && a.T >= 2) return launch_variant<A, MODE, true>(a, grid, nh, stream);
-  return launch_variant<A, MODE, false>(a, grid, nh, stream);
-}
-
-cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, cudaStream_t stream) {
-  if (commit_all) {
-    dim3 grid(a.Hk, a.B, 1);
-    const int nh = a.Hv / a.Hk;
-    return act == GDN_BF16 ? launch_mode<BF16, VERIFY_COMMIT_ALL>(a, grid, nh, stream)
-                           : launch_mode<F32, VERIFY_COMMIT_ALL>(a, grid, nh, stream);
-  }
-  dim3 grid(a.Hv, a.B, 1);
-  return act == GDN_BF16 ? launch_mode<BF16, VERIFY>(a, grid, 1, stream)
-                         : launch_mode<F32, VERIFY>(a, grid, 1, stream);
+cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, void* ws, cudaStream_t stream) {
+  if (!commit_all) return launch_verify_readonly(a, act, ws, stream);
+  dim3 grid(a.Hk, a.B, 1);
+  const int nh = a.Hv / a.Hk;
+  return act == GDN_BF16 ? launch_mode<BF16, VERIFY_COMMIT_ALL>(a, grid, nh, stream)
+                         : launch_mode<F32, VERIFY_COMMIT_ALL>(a, grid, nh, stream);
 }
 
 cudaError_t launch_commit(const StepArgs& a, int L, int act, cudaStream_t stream) {

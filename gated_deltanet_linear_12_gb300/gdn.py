@@ -22,7 +22,8 @@ GDN_VERIFY_COMMIT_ALL = 1
 GDN_DEVERR_SLOT, GDN_DEVERR_NKEEP, GDN_DEVERR_SEQLENS, GDN_DEVERR_TIMEOUT = 1, 2, 4, 8
 HEAD_DIM, CONV_WIDTH, CHUNK, MAX_DRAFT = 128, 4, 64, 8
 
-EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_step",
+EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_workspace_bytes",
+           "gdn_verify_step",
            "gdn_commit_layers", "gdn_selftest_tc_gemm", "gdn_status_string"]
 
 
@@ -68,12 +69,14 @@ def load() -> ctypes.CDLL:
             L.gdn_postconv_norm.argtypes = [cfgp, i32, vp, i32, vp, i64, vp]
             L.gdn_delta_prefill.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64,
                                             i32, vp]
+            L.gdn_verify_workspace_bytes.argtypes = [cfgp, i32, i32]
             L.gdn_verify_step.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
-                                          u32, vp, vp]
+                                          u32, vp, vp, i64, vp]
             L.gdn_commit_layers.argtypes = [cfgp, vp, i32, vp, vp, i32, i32, vp]
             L.gdn_selftest_tc_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
             for f in EXPORTS[:-1]:
                 getattr(L, f).restype = ctypes.c_int
+            L.gdn_verify_workspace_bytes.restype = ctypes.c_int64
             L.gdn_status_string.argtypes = [ctypes.c_int]
             L.gdn_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -154,15 +157,36 @@ def gdn_delta_prefill(cfg, qkv, alpha, beta, z, norm_w, out, state, slot_idx, cu
         qkv.shape[0], chunk, _stream(qkv, stream)))
 
 
+def gdn_verify_workspace_bytes(cfg, B, T):
+    n = load().gdn_verify_workspace_bytes(ctypes.byref(cfg), B, T)
+    if n < 0:
+        raise GdnError("gdn_verify_workspace_bytes", GDN_ERR_INVALID, "invalid configuration")
+    return n
+
+
+def verify_workspace(cfg, B, T, device):
+    """A device buffer for gdn_verify_step's workspace argument."""
+    return torch.empty(gdn_verify_workspace_bytes(cfg, B, T), dtype=torch.uint8, device=device)
+
+
 def gdn_verify_step(cfg, x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, *,
-                    commit_all=False, postconv_out=None, stream=None):
-    """x [B][T][C]; alpha, beta [B][T][Hv]; z, out [B][T][Hv*128]."""
+                    commit_all=False, postconv_out=None, workspace=None, stream=None):
+    """x [B][T][C]; alpha, beta [B][T][Hv]; z, out [B][T][Hv*128]. workspace: a
+    uint8 CUDA tensor (verify_workspace); taken from the caching allocator when
+    omitted."""
     _dense(x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, postconv_out)
     B, T = x.shape[0], x.shape[1]
+    ws, ws_bytes = None, 0
+    if not commit_all:
+        if workspace is None:
+            workspace = verify_workspace(cfg, B, T, x.device)
+        _dense(workspace)
+        ws, ws_bytes = workspace, workspace.numel() * workspace.element_size()
     _check("gdn_verify_step", load().gdn_verify_step(
         ctypes.byref(cfg), _ptr(x), _ptr(conv_w), _ptr(conv_state), _ptr(state), _ptr(alpha),
         _ptr(beta), _ptr(z), _ptr(norm_w), _ptr(out), _ptr(slot_idx), B, T,
-        GDN_VERIFY_COMMIT_ALL if commit_all else 0, _ptr(postconv_out), _stream(x, stream)))
+        GDN_VERIFY_COMMIT_ALL if commit_all else 0, _ptr(postconv_out), _ptr(ws), ws_bytes,
+        _stream(x, stream)))
 
 
 def make_layer_views(layers, device):

@@ -154,6 +154,15 @@ gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const float
                              int32_t chunk, void* stream);
 
 /*
+ * gdn_verify_workspace_bytes — bytes of device workspace gdn_verify_step needs
+ * without GDN_VERIFY_COMMIT_ALL for B sequences of T draft tokens (post-conv
+ * rows, the tensor-core operand tiles and the gate tables of every head).
+ * Returns -1 for an invalid configuration. The pages have no counterpart: the
+ * read-only verify is split in two kernels that pass these through memory.
+ */
+int64_t gdn_verify_workspace_bytes(const gdn_config* cfg, int32_t B, int32_t T);
+
+/*
  * gdn_verify_step — speculative verify of T draft tokens for B sequences of one
  * layer: conv from conv_state (+SiLU, +L2 norm), the recurrence from the current
  * state, and the gated RMSNorm, for every draft token.
@@ -166,13 +175,20 @@ gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const float
  *           bitwise equal to this call without the flag followed by
  *           gdn_commit_layers with n_keep = T.
  *   postconv_out  nullable [B][T][C] act: the post-conv activations used
+ *   workspace     without GDN_VERIFY_COMMIT_ALL: caller-owned device memory of
+ *                 at least gdn_verify_workspace_bytes(cfg, B, T) bytes, 256-byte
+ *                 aligned, overlapping no argument; its contents on entry do not
+ *                 matter and on return are unspecified. Two calls in flight at
+ *                 once must not share it. With GDN_VERIFY_COMMIT_ALL it is unused
+ *                 (may be NULL, workspace_bytes 0).
  *   T in 1..GDN_MAX_DRAFT.
  */
 gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* conv_w,
                            void* conv_state, float* state, const float* alpha,
                            const float* beta, const void* z, const float* norm_w, void* out,
                            const int32_t* slot_idx, int32_t B, int32_t T, uint32_t flags,
-                           void* postconv_out, void* stream);
+                           void* postconv_out, void* workspace, int64_t workspace_bytes,
+                           void* stream);
 
 /*
  * gdn_commit_layers — commit the accepted prefix of a verify window in every
