@@ -21,9 +21,10 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_VERIFY_COMMIT_ALL = 1
 GDN_DEVERR_SLOT, GDN_DEVERR_NKEEP, GDN_DEVERR_SEQLENS, GDN_DEVERR_TIMEOUT = 1, 2, 4, 8
 HEAD_DIM, CONV_WIDTH, CHUNK, MAX_DRAFT = 128, 4, 64, 8
+VERIFY_NOALLOC_MAX_BYTES = 8 << 20
 
 EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_workspace_bytes",
-           "gdn_verify_step",
+           "gdn_verify_step", "gdn_verify_step_noalloc",
            "gdn_commit_layers", "gdn_selftest_tc_gemm", "gdn_status_string"]
 
 
@@ -72,6 +73,8 @@ def load() -> ctypes.CDLL:
             L.gdn_verify_workspace_bytes.argtypes = [cfgp, i32, i32]
             L.gdn_verify_step.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                           u32, vp, vp, i64, vp]
+            L.gdn_verify_step_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                  i32, vp, vp]
             L.gdn_commit_layers.argtypes = [cfgp, vp, i32, vp, vp, i32, i32, vp]
             L.gdn_selftest_tc_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
             for f in EXPORTS[:-1]:
@@ -200,6 +203,18 @@ def make_layer_views(layers, device):
     raw = bytes(arr)
     host = torch.frombuffer(bytearray(raw), dtype=torch.uint8)
     return host.to(device)
+
+
+def gdn_verify_step_noalloc(cfg, x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, *,
+                            postconv_out=None, stream=None):
+    """Read-only verify with the library's own fixed workspace: nothing is
+    allocated, here or in the library. Same arrays as gdn_verify_step."""
+    _dense(x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, postconv_out)
+    B, T = x.shape[0], x.shape[1]
+    _check("gdn_verify_step_noalloc", load().gdn_verify_step_noalloc(
+        ctypes.byref(cfg), _ptr(x), _ptr(conv_w), _ptr(conv_state), _ptr(state), _ptr(alpha),
+        _ptr(beta), _ptr(z), _ptr(norm_w), _ptr(out), _ptr(slot_idx), B, T, _ptr(postconv_out),
+        _stream(x, stream)))
 
 
 def gdn_commit_layers(cfg, views, n_layers, slot_idx, n_keep, T, *, stream=None):

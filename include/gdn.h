@@ -191,6 +191,38 @@ gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* con
                            void* stream);
 
 /*
+ * gdn_verify_step_noalloc — the read-only gdn_verify_step (no
+ * GDN_VERIFY_COMMIT_ALL) for callers that cannot allocate device memory: code
+ * hosted inside a framework or runtime that owns every device allocation and
+ * gives its plugins no allocator, services that run under a fixed device-memory
+ * budget, and loops that must not call cudaMalloc/cudaFree because those calls
+ * can synchronise the device. The pages have no counterpart; it exists only for
+ * such callers.
+ *
+ * The workspace is a buffer of GDN_VERIFY_NOALLOC_MAX_BYTES that the library
+ * keeps in the device memory of every GPU that loads it, until the process
+ * exits. Arguments are those of gdn_verify_step, minus flags, workspace and
+ * workspace_bytes; conv_state and state are only read.
+ *   - Returns GDN_ERR_UNSUPPORTED, with nothing enqueued, when
+ *     gdn_verify_workspace_bytes(cfg, B, T) exceeds GDN_VERIFY_NOALLOC_MAX_BYTES
+ *     (8 MiB: for example B = 32 sequences of T = 8 tokens with Hk = 16,
+ *     Hv = 32 heads in bf16 need 6.6 MiB); use gdn_verify_step then.
+ *   - The first call made with a device current looks up the buffer's address
+ *     on that device; make that first call before any stream capture.
+ *   - All calls share the one buffer per device, which keeps whatever the last
+ *     call left in it (nothing in it has to start at zero). Calls that overlap
+ *     on the GPU (on different streams, or from different host threads) race on
+ *     it and give wrong results: order them.
+ *   - Allocates nothing and frees nothing.
+ */
+#define GDN_VERIFY_NOALLOC_MAX_BYTES (8u << 20)
+gdn_status gdn_verify_step_noalloc(const gdn_config* cfg, const void* x, const void* conv_w,
+                                   const void* conv_state, const float* state, const float* alpha,
+                                   const float* beta, const void* z, const float* norm_w, void* out,
+                                   const int32_t* slot_idx, int32_t B, int32_t T, void* postconv_out,
+                                   void* stream);
+
+/*
  * gdn_commit_layers — commit the accepted prefix of a verify window in every
  * layer in one call: for each layer l and batch entry b with 0 < n = n_keep[b]
  * <= T, conv_state <- last 3 rows of (conv_state ++ x[b, 0:n]) and state <- the

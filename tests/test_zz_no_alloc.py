@@ -1,0 +1,62 @@
+"""The allocation-free verify entry point (gdn_verify_step_noalloc), for callers
+that cannot allocate device memory themselves, against gdn_verify_step with a
+caller-provided workspace. Two calls in a row of different shapes: the shared
+library buffer still holds the first call's data when the second runs, which
+must not matter. This file is collected last."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from gated_deltanet_linear_12_gb300 import synthetic as syn
+from tests.helpers import bits, check_bf16, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+D = 128
+
+
+@pytest.fixture(scope="module")
+def G():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_deltanet_linear_12_gb300 import gdn
+    gdn.load()
+    return gdn
+
+
+def _verify_both(G, inp):
+    act = torch.bfloat16
+    d = {k: to_dev(inp[k]) for k in ("x", "conv_w", "conv_state", "state", "alpha", "beta", "z",
+                                      "norm_w", "slot_idx")}
+    cfg = G.make_config(inp["Hk"], inp["Hv"], act, d["state"].shape[0])
+    B, T, Hv = inp["B"], inp["T"], inp["Hv"]
+    ref = torch.zeros(B, T, Hv * D, dtype=act, device="cuda")         # padding rows stay 0
+    new = torch.zeros_like(ref)
+    G.gdn_verify_step(cfg, d["x"], d["conv_w"], d["conv_state"], d["state"], d["alpha"], d["beta"],
+                      d["z"], d["norm_w"], ref, d["slot_idx"])
+    G.gdn_verify_step_noalloc(cfg, d["x"], d["conv_w"], d["conv_state"], d["state"], d["alpha"],
+                              d["beta"], d["z"], d["norm_w"], new, d["slot_idx"])
+    torch.cuda.synchronize()
+    # read-only: the pools are unchanged
+    assert np.array_equal(bits(d["state"]), inp["state"].view(np.int32))
+    return to_np(ref), to_np(new)
+
+
+def test_noalloc_matches_workspace_verify_two_calls(G):
+    # 1: the spec-verify window (6.6 MiB of the 8 MiB buffer); 2: a smaller one
+    first = syn.verify_inputs(32, 8, 16, 32, "bf16", seed=syn.seed_of("spec-verify-bf16"))
+    second = syn.verify_inputs(5, 3, 2, 4, "bf16", seed=901, pad_slots=1)
+    for inp in (first, second):
+        ref, new = _verify_both(G, inp)
+        check_bf16(new, ref, what=f"no-alloc verify B={inp['B']} T={inp['T']}")
+
+
+def test_noalloc_rejects_configurations_beyond_its_buffer(G):
+    cfg = G.make_config(16, 32, torch.bfloat16, 64)
+    B = 64                                               # 13 MiB of workspace at T = 8
+    assert G.gdn_verify_workspace_bytes(cfg, B, 8) > G.VERIFY_NOALLOC_MAX_BYTES
+    lib = G.load()
+    ptrs = [ctypes.c_void_p(0x7f0000000000 + i * 0x10000000) for i in range(10)]
+    assert lib.gdn_verify_step_noalloc(ctypes.byref(cfg), *ptrs, B, 8, None, None) == G.GDN_ERR_UNSUPPORTED
