@@ -120,49 +120,50 @@ __device__ __forceinline__ float2 conv4x2(float2 w0, float2 w1, float2 w2, float
 }
 
 // SiLU, two values at a time with Blackwell's paired f32 instructions, by
-// published schemes made only of correctly rounded IEEE operations, so the
-// result is reproducible bit for bit by any IEEE implementation of the same
-// steps (the post-conv activations then round to the same bf16 values
-// everywhere):
+// published schemes made only of correctly rounded IEEE operations and exact
+// integer operations on the bits, so the result is reproducible bit for bit by
+// any IEEE implementation of the same steps (the post-conv activations then
+// round to the same bf16 values everywhere):
 //   t = e^-|y|: Cody & Waite's reduction -|y| = n ln2 + r (ln 2 split in a
 //     16-bit high part, so n * high is exact, and a low part; the argument
-//     clamped at -87 keeps 2^n normal), degree-7 Taylor polynomial of e^r in
-//     Horner form, scaled by 2^n. n, the nearest integer to the exact
-//     a log2 e, comes from one fused multiply-add with 1.5 * 2^23 (which
-//     rounds to an integer) and an exact subtraction; 2^n is built from the
-//     integer left in the low bits of the sum;
+//     clamped at -86 keeps 2^n p normal), a degree-5 polynomial of e^r in Horner
+//     form (the near-minimax relative fit on |r| <= ln2/2 with float
+//     coefficients), scaled by 2^n by adding n to the exponent field. n, the
+//     nearest integer to the exact a log2 e, comes from one fused multiply-add
+//     with 1.5 * 2^23 (which rounds it to an integer) and an exact subtraction;
+//     n << 23 is read from the low bits of the sum;
 //   (Each multiply whose result feeds a single add is written as an explicit
 //   fused multiply-add, on both sides: the compiler is otherwise free to fuse
 //   paired f32 multiplies into the next add, which changes the rounding.)
-//   s = 1/(1 + t), d in [1, 2]: Newton-Raphson from 24/17 - 8/17 d (relative
-//     error <= 1/17), three steps x <- x + x (1 - d x);
+//   s = 1/(1 + t), d in [1, 2]: Newton-Raphson from the quadratic start
+//     2.1212120 - 1.4545449 d + 0.32323205 d^2 (relative error <= 0.0102), two
+//     steps x <- x + x (1 - d x);
 //   sigmoid = s (y >= 0) or t s (y < 0);  silu = y sigmoid.
+// Within 6 ulp of silu on [-86, 90].
 __device__ __forceinline__ float2 silu2(float2 y) {
   constexpr float kMagic = 12582912.0f;                 // 1.5 * 2^23
   constexpr float kLog2e = 1.44269504088896341f;
-  const float2 a = make_float2(fmaxf(-fabsf(y.x), -87.0f), fmaxf(-fabsf(y.y), -87.0f));
+  const float2 a = make_float2(fmaxf(-fabsf(y.x), -86.0f), fmaxf(-fabsf(y.y), -86.0f));
   const float2 tt = __ffma2_rn(a, make_float2(kLog2e, kLog2e), make_float2(kMagic, kMagic));
   const float2 n = __fadd2_rn(tt, make_float2(-kMagic, -kMagic));
   const float2 mn = make_float2(-n.x, -n.y);
   float2 r = __ffma2_rn(mn, make_float2(0.693145751953125f, 0.693145751953125f), a);
   r = __ffma2_rn(mn, make_float2(1.42860682030941723212e-6f, 1.42860682030941723212e-6f), r);
-  float2 p = make_float2(1.0f / 5040.0f, 1.0f / 5040.0f);
-  p = __ffma2_rn(p, r, make_float2(1.0f / 720.0f, 1.0f / 720.0f));
-  p = __ffma2_rn(p, r, make_float2(1.0f / 120.0f, 1.0f / 120.0f));
-  p = __ffma2_rn(p, r, make_float2(1.0f / 24.0f, 1.0f / 24.0f));
-  p = __ffma2_rn(p, r, make_float2(1.0f / 6.0f, 1.0f / 6.0f));
-  p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
-  p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
-  p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
-  const float2 sc = make_float2(__int_as_float((__float_as_int(tt.x) << 23) + 0x3f800000),
-                                __int_as_float((__float_as_int(tt.y) << 23) + 0x3f800000));
-  const float2 t = __fmul2_rn(p, sc);                   // e^-|y|
+  float2 p = make_float2(0.008297654800117016f, 0.008297654800117016f);
+  p = __ffma2_rn(p, r, make_float2(0.04191538318991661f, 0.04191538318991661f));
+  p = __ffma2_rn(p, r, make_float2(0.16667574644088745f, 0.16667574644088745f));
+  p = __ffma2_rn(p, r, make_float2(0.49998894333839417f, 0.49998894333839417f));
+  p = __ffma2_rn(p, r, make_float2(0.9999997019767761f, 0.9999997019767761f));
+  p = __ffma2_rn(p, r, make_float2(1.0000001192092896f, 1.0000001192092896f));
+  const float2 t = make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(tt.x) << 23)),
+                               __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(tt.y) << 23)));  // e^-|y|
   const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), t);
   const float2 md = make_float2(-d.x, -d.y);
-  float2 x = __ffma2_rn(make_float2(-8.0f / 17.0f, -8.0f / 17.0f), d,
-                        make_float2(24.0f / 17.0f, 24.0f / 17.0f));
+  float2 x = __ffma2_rn(make_float2(0.3232320547103882f, 0.3232320547103882f), d,
+                        make_float2(-1.4545449018478394f, -1.4545449018478394f));
+  x = __ffma2_rn(x, d, make_float2(2.1212120056152344f, 2.1212120056152344f));
 #pragma unroll
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < 2; ++i) {
     const float2 e = __ffma2_rn(md, x, make_float2(1.0f, 1.0f));
     x = __ffma2_rn(x, e, x);
   }

@@ -93,20 +93,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(map), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
       : "memory");
 }
-// Contiguous global -> shared copy (16-byte aligned, a multiple of 16 bytes).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   tc::smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
 // Programmatic dependent launch: let the next grid start / wait for the previous one.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -366,7 +352,7 @@ verify_state_kernel(StepArgs p, const __grid_constant__ CUtensorMap smap, const 
   if (tid == 0) {
     tc::mbar_init(&s_bar, 1);
     if constexpr (TC) tc::mbar_init(&tc_bar, 1);
-    fence_mbar_init();
+    tc::fence_mbar_init();
     tc::fence_async_smem();
   }
   if constexpr (TC) {
@@ -381,7 +367,7 @@ verify_state_kernel(StepArgs p, const __grid_constant__ CUtensorMap smap, const 
     if (lane == 0) {
       const uint32_t bytes =
           S_BYTES + (A == BF16 ? BT_BYTES : 2u * T * row_bytes) + 2u * T * row_bytes + TAB * 4 + D * 4;
-      mbar_arrive_expect_tx(&s_bar, bytes);
+      tc::mbar_arrive_expect_tx(&s_bar, bytes);
       const int row0 = (slot * Hv + h) * D;
 #pragma unroll
       for (int bx = 0; bx < 4; ++bx) tma_load_2d(SR + bx * 16384, &smap, 32 * bx, row0, &s_bar);
@@ -393,19 +379,19 @@ verify_state_kernel(StepArgs p, const __grid_constant__ CUtensorMap smap, const 
     if (lane < T) {
       const int t = lane;
       const int64_t tok = (int64_t)b * T + t;
-      bulk_load(VR + t * row_bytes, act + (tok * C + (int64_t)(2 * Hk + h) * D) * asz, row_bytes, &s_bar);
-      bulk_load(ZR + t * row_bytes, zp + (tok * Hv * D + (int64_t)h * D) * asz, row_bytes, &s_bar);
+      tc::bulk_load(VR + t * row_bytes, act + (tok * C + (int64_t)(2 * Hk + h) * D) * asz, row_bytes, &s_bar);
+      tc::bulk_load(ZR + t * row_bytes, zp + (tok * Hv * D + (int64_t)h * D) * asz, row_bytes, &s_bar);
       if constexpr (A != BF16) {
-        bulk_load(QK + t * row_bytes, act + (tok * C + (int64_t)(Hk + hq) * D) * asz, row_bytes, &s_bar);
-        bulk_load(QK + MAXT * row_bytes + t * row_bytes, act + (tok * C + (int64_t)hq * D) * asz, row_bytes,
+        tc::bulk_load(QK + t * row_bytes, act + (tok * C + (int64_t)(Hk + hq) * D) * asz, row_bytes, &s_bar);
+        tc::bulk_load(QK + MAXT * row_bytes + t * row_bytes, act + (tok * C + (int64_t)hq * D) * asz, row_bytes,
                   &s_bar);
       }
     } else if (lane == 8) {
-      bulk_load(tb, ws + wl.tab + ((int64_t)b * Hv + h) * TAB * 4, TAB * 4, &s_bar);
+      tc::bulk_load(tb, ws + wl.tab + ((int64_t)b * Hv + h) * TAB * 4, TAB * 4, &s_bar);
     } else if (lane == 9) {
-      if constexpr (A == BF16) bulk_load(QK, ws + wl.bt + ((int64_t)b * Hk + hq) * BT_BYTES, BT_BYTES, &s_bar);
+      if constexpr (A == BF16) tc::bulk_load(QK, ws + wl.bt + ((int64_t)b * Hk + hq) * BT_BYTES, BT_BYTES, &s_bar);
     } else if (lane == 10) {
-      bulk_load(nw, p.norm_w, D * 4, &s_bar);
+      tc::bulk_load(nw, p.norm_w, D * 4, &s_bar);
     }
   }
   const bool s_ok = tc::mbar_wait(&s_bar, 0, 1u << 24);

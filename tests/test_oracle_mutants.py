@@ -26,9 +26,9 @@ MUTANTS = {
                       "  acc = std::fma(w[2], xp_t[2], acc);\n  acc = std::fma(w[3], xp_t[3], acc);",
                       "T acc = w[3] * xp_t[0];\n  acc = std::fma(w[2], xp_t[1], acc);\n"
                       "  acc = std::fma(w[1], xp_t[2], acc);\n  acc = std::fma(w[0], xp_t[3], acc);"),
-    "exp_poly_term_dropped": ("  p = std::fma(p, r, 1.0f / 24.0f);\n", "  p = std::fma(p, r, 0.0f);\n"),
+    "exp_poly_term_dropped": ("  p = std::fma(p, r, 0.16667574644088745f);\n", "  p = std::fma(p, r, 0.0f);\n"),
     "exp_ln2_low_dropped": ("  r = std::fma(-n, 1.42860682030941723212e-6f, r);", "  r = r;"),
-    "recip_two_iterations": ("  for (int i = 0; i < 3; ++i) {", "  for (int i = 0; i < 2; ++i) {"),
+    "recip_one_iteration": ("  for (int i = 0; i < 2; ++i) {", "  for (int i = 0; i < 1; ++i) {"),
     "sigmoid_branch_swapped": ("const float sig = y >= 0.0f ? s : t * s;", "const float sig = y >= 0.0f ? t * s : s;"),
     "tail_off_by_one": ("int64_t idx = n + r;", "int64_t idx = n + r - 1;"),
     "tree_adjacent_pairs": ("T p0 = e[0] + e[4], p1 = e[1] + e[5], p2 = e[2] + e[6], p3 = e[3] + e[7];",

@@ -83,21 +83,21 @@ def test_p1_silu_applied_after_conv(orc):
     np.testing.assert_allclose(post, want, rtol=1e-15, atol=0)
 
 
-def test_p1_f32_silu_scheme_within_four_ulp(orc):
-    """The float instantiation's SiLU (exp by Cody-Waite + Taylor, reciprocal by
-    Newton-Raphson) against y / (1 + math.exp(-y)) in double."""
+def test_p1_f32_silu_scheme_within_six_ulp(orc):
+    """The float instantiation's SiLU (exp by Cody-Waite + a degree-5 polynomial,
+    reciprocal by Newton-Raphson) against y / (1 + math.exp(-y)) in double."""
     ys = np.concatenate([np.linspace(-90.0, 90.0, 400001, dtype=np.float32),
                          np.float32([0.0, -0.0, 1e-8, -1e-8, 0.34657359, -0.34657359, 1e-30])])
     got = orc.silu(ys, prec="f32").astype(np.float64)
     worst = 0.0
     for y, g in zip(ys[::37].astype(np.float64), got[::37]):
         want = y / (1.0 + math.exp(-y))
-        if y < -87.0:                          # exp argument clamped: saturated, negligible
-            assert abs(g) < 2e-36 and abs(want) < 2e-36
+        if y < -86.0:                          # exp argument clamped: saturated, negligible
+            assert abs(g) < 3e-35 and abs(want) < 3e-35
             continue
         ulp = float(np.spacing(np.float32(abs(want))))
         worst = max(worst, abs(g - want) / ulp)
-        assert abs(g - want) <= 4 * ulp, (y, g, want)
+        assert abs(g - want) <= 6 * ulp, (y, g, want)
     assert worst > 0.0                         # it is not an exact copy of the library
 
 
