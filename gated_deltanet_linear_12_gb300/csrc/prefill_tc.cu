@@ -5,22 +5,23 @@
 // o_t = S_t q_t, and the output norm after the recurrence ("Strata PR #3226").
 // Per chunk (chunk-local g_t = sum_{u<=t} log a_u, G_t = e^{g_t},
 // c_t = e^{g_last - g_t}):
-//   A_ts = b_t e^{g_t - g_s} k_t.k_s (s < t),     Tinv = (I + A)^-1
-//   R_t  = b_t v_t - b_t G_t S0 k_t,              d = Tinv R
+//   A_ts = b_t e^{g_t - g_s} k_t.k_s (s < t),     (I + A) d = R
+//   R_t  = b_t v_t - b_t G_t S0 k_t
 //   o_t  = G_t S0 q_t + sum_{s<=t} e^{g_t - g_s} (q_t.k_s) d_s
 //   S    = G_last S0 + sum_s c_s d_s k_s^T
 // Written transposed, value row i of S is TMEM lane i and the products are
 //   MMA1  P^T  = S0 [K;Q]^T     M=128 N=128 K=128   S0 as bf16 hi + lo (2 passes)
 //   MMA2  G    = [K;Q] K^T      M=128 N=64  K=128   exact bf16 products
-//   MMA4  D^T  = R^T Tinv^T     M=128 N=64  K=64    3 passes (hi hi, lo hi, hi lo)
-//   MMA5  O^T  = D^T X^T        M=128 N=64  K=64    3 passes
+//   MMA5  O^T  = D^T X^T        M=128 N=64  K=64    3 passes (hi hi, lo hi, hi lo)
 //   MMA3  dS   = (c D)^T K      M=128 N=128 K=64    (c D) as hi + lo (2 passes)
 // where X_ts = e^{g_t - g_s} q_t.k_s (s <= t). An f32 operand x enters as
 // hi = bf16(x), lo = bf16(x - hi): the dropped lo*lo term and the rounding of
 // lo leave a relative error near 2^-16 per product, far below the 1e-4 bound
 // on states. S stays in f32 in TMEM for the whole sequence; only its bf16
 // hi/lo copies (MMA operands) are rewritten per chunk. CUDA cores build the
-// decay tables, invert I + A (64 x 64, blocked) and do the RMSNorm epilogue.
+// decay tables and solve (I + A) d = R for each value row by forward
+// substitution in f32 (the row's R and d stay in one thread's registers),
+// while the other half of the block runs the previous chunk's RMSNorm.
 // One block of 256 threads per (sequence, v head); warps w and w + 4 share
 // TMEM lane quarter w % 4 (rows i = 32 (w % 4) + lane). Every wait is bounded.
 #include "common.cuh"
@@ -41,14 +42,13 @@ constexpr int SM_SLO = SM_SHI + 32768;             // S lo
 constexpr int SM_KQ = SM_SLO + 32768;              // [K;Q]  128x128 bf16 (MMA1 B, MMA2 A and B);
                                                    // then (cD)^T hi | lo, 128x64 each (MMA3 A)
 constexpr int SM_KT = SM_KQ + 32768;               // K^T    128x64 bf16 (MMA3 B)
-constexpr int SM_RD = SM_KT + 16384;               // R^T hi | lo, then D^T hi | lo, 128x64 each
-                                                   // (MMA4 / MMA5 A); then outputs [64][128] f32
-constexpr int SM_TI = SM_RD + 32768;               // Tinv hi | lo, 64x64 each (MMA4 B)
+constexpr int SM_RD = SM_KT + 16384;               // D^T hi | lo, 128x64 each (MMA5 A);
+                                                   // then outputs [64][128] f32
+constexpr int SM_TI = SM_RD + 32768;               // the chunk's values [64][128] bf16
 constexpr int SM_XB = SM_TI + 16384;               // X hi | lo, 64x64 each (MMA5 B)
-constexpr int SM_AB = SM_XB + 16384;               // A f32 [64][AP]
-constexpr int SM_TB = SM_AB + 64 * AP * 4;         // Tinv f32 [64][AP]
-constexpr int SM_TMP = SM_TB + 64 * AP * 4;        // inverse scratch [1024] f32
-constexpr int SM_VEC = SM_TMP + 1024 * 4;          // g2, G, b, c, la [64] f32
+constexpr int SM_AB = SM_XB + 16384;               // A^T f32 [64][AP]: column u of A is row u
+constexpr int SM_ZB = SM_AB + 64 * AP * 4;         // the previous chunk's z rows [64][128] bf16
+constexpr int SM_VEC = SM_ZB + 16384;              // g2, G, b, c, la [64] f32
 constexpr int SM_BAR = SM_VEC + 5 * 64 * 4;        // mbarrier (8 B) + TMEM slot
 constexpr int SM_TOTAL = SM_BAR + 16;
 
@@ -56,8 +56,7 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t TM_S = 0;         // S f32                    cols   0..127
 constexpr uint32_t TM_P = 128;       // P^T = [S0 k | S0 q]      cols 128..255
 constexpr uint32_t TM_G = 256;       // G = [K;Q] K^T            cols 256..319
-constexpr uint32_t TM_D = 320;       // D^T                      cols 320..383
-constexpr uint32_t TM_DS = 256;      // dS (after G and D^T are read)  256..383
+constexpr uint32_t TM_DS = 256;      // dS (after G is read)     cols 256..383
 constexpr uint32_t TM_O = 384;       // O^T                      cols 384..447
 constexpr uint32_t WAIT_POLLS = 1u << 24;
 
@@ -122,8 +121,7 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
   uint8_t* XB = sm + SM_XB;
   float* OB = reinterpret_cast<float*>(sm + SM_RD);
   float* AB = reinterpret_cast<float*>(sm + SM_AB);
-  float* TB = reinterpret_cast<float*>(sm + SM_TB);
-  float* tmp = reinterpret_cast<float*>(sm + SM_TMP);
+  uint8_t* ZB = sm + SM_ZB;
   float* g2_s = reinterpret_cast<float*>(sm + SM_VEC);   // chunk-local log2 decay
   float* G_s = g2_s + 64;
   float* b_s = G_s + 64;
@@ -217,7 +215,7 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
   const uint32_t id128 = tc::idesc_bf16_f32(128, 128);
   const uint32_t id64 = tc::idesc_bf16_f32(128, 64);
   const uint32_t a_SHI = tc::smem_u32(SHI), a_SLO = tc::smem_u32(SLO), a_KQ = tc::smem_u32(KQ);
-  const uint32_t a_KT = tc::smem_u32(KT), a_RD = tc::smem_u32(RD), a_TI = tc::smem_u32(TI);
+  const uint32_t a_KT = tc::smem_u32(KT), a_RD = tc::smem_u32(RD);
   const uint32_t a_XB = tc::smem_u32(XB);
 
   // Thread 0 commits the MMAs it issued; everyone waits (bounded). Returns
@@ -231,7 +229,7 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
   };
 
   // Copies of a chunk's keys and queries (into the K-major [K;Q] tile), values
-  // (row-major, into the Tinv tiles' space) and raw gates, in flight while the
+  // (row-major, into the values tile) and raw gates, in flight while the
   // previous chunk finishes. Rows past the sequence end are zero-filled.
   float* al_raw = la_s;                                  // raw alpha until log2 is taken
   auto prefetch = [&](int64_t pc0, int pm) {
@@ -257,35 +255,55 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     cp_async_commit();
   };
 
-  // z-gated RMSNorm of a chunk's outputs (16 lanes per token). It runs while
-  // the next chunk's first products are on the tensor core: it reads only the
-  // output buffer, which the next chunk overwrites after that wait.
+  // The chunk's z rows, for its epilogue during the next chunk; they land with
+  // the next chunk's inputs (rows past the end zero-filled).
+  auto prefetch_z = [&](int64_t zc0, int zm) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {                        // 64 tokens x 16 pieces of 16 bytes
+      const int iz = tid + k * PT, t = iz >> 4, w8 = iz & 15;
+      const int tt = t < zm ? t : 0;
+      cp_async16(ZB + (t * D + 8 * w8) * 2,
+                 static_cast<const uint16_t*>(p.z) + (zc0 + tt) * Hv * D + (int64_t)h * D + 8 * w8,
+                 t < zm ? 16u : 0u);
+    }
+  };
+
+  // z-gated RMSNorm of a chunk's outputs by the 128 owner threads (16 lanes per
+  // token, 8 tokens at a time). It runs while the helpers solve for the next
+  // chunk's deltas: it reads only the output buffer and the staged z rows.
   auto epilogue = [&](int64_t ec0, int em) {
-      constexpr int NIT = C64 / (PT / 16);
-      float zv[NIT][8];
-      const int l16 = tid & 15;
+      const int l16 = tid & 15, lane = tid & 31;
+      float nw[8];
 #pragma unroll
-      for (int it = 0; it < NIT; ++it) {
-        const int t = it * (PT / 16) + (tid >> 4);
-        if (t < em) load8<BF16>(p.z, (ec0 + t) * Hv * D + (int64_t)h * D + l16 * 8, zv[it]);
-      }
+      for (int j = 0; j < 8; ++j) nw[j] = p.norm_w[l16 * 8 + j];
 #pragma unroll
-      for (int it = 0; it < NIT; ++it) {
-        const int t = it * (PT / 16) + (tid >> 4);
-        const bool live = t < em;
-        float o[8];
-        const float4 u0 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16];
-        const float4 u1 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16 + 1];
-        o[0] = u0.x; o[1] = u0.y; o[2] = u0.z; o[3] = u0.w;
-        o[4] = u1.x; o[5] = u1.y; o[6] = u1.z; o[7] = u1.w;
-        const float ss = head_sum_sq16(o);
-        if (live) {
-          const float r = inv_norm(__fmul_rn(ss, 1.0f / D), p.eps);
-          float res[8];
+      for (int half = 0; half < 2; ++half) {
+        float zv[4][8], o[4][8], ss[4];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu_gate(zv[it][j]));
-          store8<BF16>(p.out, (ec0 + t) * Hv * D + (int64_t)h * D + l16 * 8, res);
+        for (int it = 0; it < 4; ++it) {
+          const int t = (4 * half + it) * 8 + (tid >> 4);
+          load8<BF16>(ZB, (int64_t)t * D + l16 * 8, zv[it]);
+          const float4 u0 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16];
+          const float4 u1 = reinterpret_cast<const float4*>(OB + t * D)[2 * l16 + 1];
+          o[it][0] = u0.x; o[it][1] = u0.y; o[it][2] = u0.z; o[it][3] = u0.w;
+          o[it][4] = u1.x; o[it][5] = u1.y; o[it][6] = u1.z; o[it][7] = u1.w;
+          ss[it] = head_sum_sq16(o[it]);
+        }
+        // lanes with l16 % 4 == it take the 1/sqrt of token it (same bits as every lane)
+        const int sel = l16 & 3;
+        const float ssel = sel == 0 ? ss[0] : sel == 1 ? ss[1] : sel == 2 ? ss[2] : ss[3];
+        const float rm = inv_norm(__fmul_rn(ssel, 1.0f / D), p.eps);
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int t = (4 * half + it) * 8 + (tid >> 4);
+          const float r = __shfl_sync(FULL, rm, (lane & ~3) | it);
+          if (t < em) {
+            float res[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[it][j], r), nw[j]), silu_gate(zv[it][j]));
+            store8<BF16>(p.out, (ec0 + t) * Hv * D + (int64_t)h * D + l16 * 8, res);
+          }
         }
       }
   };
@@ -330,19 +348,19 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     }
     __syncthreads();
     if (tid < C64) c_s[tid] = ex2(g2_s[C64 - 1] - g2_s[tid]);
-    if (prev_c0 >= 0) epilogue(prev_c0, prev_m);         // previous chunk, overlapped
     if (!commit_and_wait()) { timed_out = true; break; }
 
-    // ---- (c) tables from G (owners); R^T rows from P^T (helpers)
+    // ---- (c) tables from G (owners); R rows from P^T, kept in registers (helpers)
+    float r[64];                                         // R, then d, of value row i (helpers)
     if (owner) {
       float gr[64];
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) tc::tmem_ld16(lane_addr + TM_G + 16 * cb, gr + 16 * cb);
-      if (i < C64) {                                     // A row i (f32, strictly lower)
-        const float gi = g2_s[i], bi = b_s[i];
+      if (i < C64) {                                     // A row i (f32, strictly lower), stored
+        const float gi = g2_s[i], bi = b_s[i];           // as column i of A^T
 #pragma unroll
         for (int u = 0; u < C64; ++u)
-          AB[i * AP + u] = u < i ? __fmul_rn(__fmul_rn(bi, ex2(gi - g2_s[u])), gr[u]) : 0.f;
+          AB[u * AP + i] = u < i ? __fmul_rn(__fmul_rn(bi, ex2(gi - g2_s[u])), gr[u]) : 0.f;
       } else {                                           // X row t: the MMA5 B tile
         const int t = i - C64;
         const float gt = g2_s[t];
@@ -351,9 +369,8 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
         for (int u = 0; u < C64; ++u) x[u] = u <= t ? __fmul_rn(ex2(gt - g2_s[u]), gr[u]) : 0.f;
         put_row64(XB, XB + 8192, t, 64, x);
       }
-    } else {                                             // R^T row i: the MMA4 A tile
+    } else {
       const uint16_t* vcol = reinterpret_cast<const uint16_t*>(TI) + i;   // staged values
-      float r[64];
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         float pk[16];
@@ -366,118 +383,38 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
           r[t] = __fmaf_rn(-__fmul_rn(bt, G_s[t]), pk[u], __fmul_rn(bt, vt));
         }
       }
+    }
+    __syncthreads();                                     // A complete
+
+    // ---- (d) helpers: (I + A) d = R for value row i by right-looking forward
+    //          substitution: once d_u is final, d_t -= A[t][u] d_u for all t > u
+    //          (column u of A read as float4s from A^T; A[t][u] = 0 for t <= u);
+    //          owners: the previous chunk's z-gated RMSNorm
+    if (owner) {
+      if (prev_c0 >= 0) epilogue(prev_c0, prev_m);
+    } else {
+#pragma unroll
+      for (int u = 0; u < C64 - 1; ++u) {
+        const float4* acol = reinterpret_cast<const float4*>(AB + u * AP);
+        const float du = r[u];
+#pragma unroll
+        for (int t4 = (u + 1) / 4; t4 < C64 / 4; ++t4) {
+          const float4 a = acol[t4];
+          if (4 * t4 > u) r[4 * t4] = __fmaf_rn(-a.x, du, r[4 * t4]);
+          if (4 * t4 + 1 > u) r[4 * t4 + 1] = __fmaf_rn(-a.y, du, r[4 * t4 + 1]);
+          if (4 * t4 + 2 > u) r[4 * t4 + 2] = __fmaf_rn(-a.z, du, r[4 * t4 + 2]);
+          if (4 * t4 + 3 > u) r[4 * t4 + 3] = __fmaf_rn(-a.w, du, r[4 * t4 + 3]);
+        }
+      }
+    }
+    __syncthreads();                                     // the output buffer has been read
+
+    // ---- (f) helpers: D^T row i -> MMA5 A tile, (c D)^T row i -> MMA3 A tile
+    if (!owner) {
       put_row64(RD, RD + 16384, i, 128, r);
-    }
-    for (int e = tid; e < C64 * AP; e += PT) TB[e] = 0.f;
-    __syncthreads();
-
-    // ---- (d) Tinv = (I + A)^-1 by recursive doubling over 16/32/64 blocks
-    if (tid < C64) {                                     // column j of its 16x16 diagonal block,
-      const int j = tid, blk = j & ~15, jl = j & 15;     // kept in registers (zeros above jl)
-      float y[16];
 #pragma unroll
-      for (int tl = 0; tl < 16; ++tl) {
-        float acc = 0.f;
-#pragma unroll
-        for (int ul = 0; ul < tl; ++ul) acc = __fmaf_rn(AB[(blk + tl) * AP + blk + ul], y[ul], acc);
-        y[tl] = tl < jl ? 0.f : (tl == jl ? 1.f : -acc);
-      }
-#pragma unroll
-      for (int tl = 0; tl < 16; ++tl) TB[(blk + tl) * AP + j] = y[tl];
-    }
-    __syncthreads();
-    // levels 2 and 3: products with the left factor's rows read as float4
-    // (the zero parts of the block-triangular factors add exact zeros)
-    for (int e = tid; e < 512; e += PT) {                // level 2: A21 Y11 per 32-block
-      const int P = e >> 8, ent = e & 255, r = ent >> 4, j = ent & 15, base = 32 * P;
-      const float4* arow = reinterpret_cast<const float4*>(AB + (base + 16 + r) * AP + base);
-      float acc = 0.f;
-#pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const float4 a = arow[u4];
-        acc = __fmaf_rn(a.x, TB[(base + 4 * u4) * AP + base + j], acc);
-        acc = __fmaf_rn(a.y, TB[(base + 4 * u4 + 1) * AP + base + j], acc);
-        acc = __fmaf_rn(a.z, TB[(base + 4 * u4 + 2) * AP + base + j], acc);
-        acc = __fmaf_rn(a.w, TB[(base + 4 * u4 + 3) * AP + base + j], acc);
-      }
-      tmp[e] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < 512; e += PT) {
-      const int P = e >> 8, ent = e & 255, r = ent >> 4, j = ent & 15, base = 32 * P;
-      const float4* yrow = reinterpret_cast<const float4*>(TB + (base + 16 + r) * AP + base + 16);
-      float acc = 0.f;
-#pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const float4 a = yrow[u4];
-        acc = __fmaf_rn(a.x, tmp[P * 256 + (4 * u4) * 16 + j], acc);
-        acc = __fmaf_rn(a.y, tmp[P * 256 + (4 * u4 + 1) * 16 + j], acc);
-        acc = __fmaf_rn(a.z, tmp[P * 256 + (4 * u4 + 2) * 16 + j], acc);
-        acc = __fmaf_rn(a.w, tmp[P * 256 + (4 * u4 + 3) * 16 + j], acc);
-      }
-      TB[(base + 16 + r) * AP + base + j] = -acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < 1024; e += PT) {               // level 3: A[32:,:32] Y[:32,:32]
-      const int r = e >> 5, j = e & 31;
-      const float4* arow = reinterpret_cast<const float4*>(AB + (32 + r) * AP);
-      float acc = 0.f;
-#pragma unroll
-      for (int u4 = 0; u4 < 8; ++u4) {
-        const float4 a = arow[u4];
-        acc = __fmaf_rn(a.x, TB[(4 * u4) * AP + j], acc);
-        acc = __fmaf_rn(a.y, TB[(4 * u4 + 1) * AP + j], acc);
-        acc = __fmaf_rn(a.z, TB[(4 * u4 + 2) * AP + j], acc);
-        acc = __fmaf_rn(a.w, TB[(4 * u4 + 3) * AP + j], acc);
-      }
-      tmp[e] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < 1024; e += PT) {
-      const int r = e >> 5, j = e & 31;
-      const float4* yrow = reinterpret_cast<const float4*>(TB + (32 + r) * AP + 32);
-      float acc = 0.f;
-#pragma unroll
-      for (int u4 = 0; u4 < 8; ++u4) {
-        const float4 a = yrow[u4];
-        acc = __fmaf_rn(a.x, tmp[(4 * u4) * 32 + j], acc);
-        acc = __fmaf_rn(a.y, tmp[(4 * u4 + 1) * 32 + j], acc);
-        acc = __fmaf_rn(a.z, tmp[(4 * u4 + 2) * 32 + j], acc);
-        acc = __fmaf_rn(a.w, tmp[(4 * u4 + 3) * 32 + j], acc);
-      }
-      TB[(32 + r) * AP + j] = -acc;
-    }
-    __syncthreads();
-    if (tid < C64) {                                     // Tinv row t: the MMA4 B tile
-      float x[64];
-#pragma unroll
-      for (int u = 0; u < C64; ++u) x[u] = TB[tid * AP + u];
-      put_row64(TI, TI + 8192, tid, 64, x);
-    }
-    tc::fence_async_smem();
-    __syncthreads();
-
-    // ---- (e) MMA4: D^T = R^T Tinv^T
-    if (tid == 0) {
-      tc::fence_after_sync();
-      mma_pass(tbase + TM_D, a_RD, 128, a_TI, 64, 4, id64, false);               // hi hi
-      mma_pass(tbase + TM_D, a_RD + 16384, 128, a_TI, 64, 4, id64, true);        // lo hi
-      mma_pass(tbase + TM_D, a_RD, 128, a_TI + 8192, 64, 4, id64, true);         // hi lo
-    }
-    if (!commit_and_wait()) { timed_out = true; break; }
-
-    // ---- (f) D^T row i -> MMA5 A tile (owners); (c D)^T row i -> MMA3 A tile (helpers)
-    {
-      float d[64];
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::tmem_ld16(lane_addr + TM_D + 16 * cb, d + 16 * cb);
-      if (owner) {
-        put_row64(RD, RD + 16384, i, 128, d);
-      } else {
-#pragma unroll
-        for (int u = 0; u < C64; ++u) d[u] = __fmul_rn(c_s[u], d[u]);
-        put_row64(KQ, KQ + 16384, i, 128, d);
-      }
+      for (int u = 0; u < C64; ++u) r[u] = __fmul_rn(c_s[u], r[u]);
+      put_row64(KQ, KQ + 16384, i, 128, r);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -494,9 +431,12 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     }
     if (!commit_and_wait()) { timed_out = true; break; }
 
+    prefetch_z(c0, m);                                   // this chunk's z: X has been consumed
     if (c0 + C64 < seq1) {                               // next chunk's inputs: KQ and TI are free
       const int64_t n0 = c0 + C64;
       prefetch(n0, (int)(seq1 - n0 < C64 ? seq1 - n0 : C64));
+    } else {
+      cp_async_commit();
     }
 
     // ---- (h) owners: o = G (S0 q) + O^T into the output buffer (the RD region
@@ -538,7 +478,11 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     prev_c0 = c0;
     prev_m = m;
   }
-  if (!timed_out && prev_c0 >= 0) epilogue(prev_c0, prev_m);   // the last chunk
+  if (!timed_out && prev_c0 >= 0) {                     // the last chunk
+    cp_async_wait_all();
+    __syncthreads();
+    if (owner) epilogue(prev_c0, prev_m);
+  }
 
   if (timed_out) {
     if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
