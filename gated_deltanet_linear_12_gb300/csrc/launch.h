@@ -1,6 +1,7 @@
 // Internal launcher interface between the C ABI (gdn_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -44,6 +45,16 @@ struct PrefillArgs {
   float eps, q_scale;
   uint32_t* dev_err;
 };
+
+// Encodes a 2-D row-major bf16 tensor map (rows x cols, row pitch in elements)
+// copied in boxes of box_cols x box_rows, without swizzle; out-of-range rows
+// read as zeros.
+cudaError_t encode_bf16_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                                 uint64_t pitch, uint32_t box_cols, uint32_t box_rows);
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 cudaError_t launch_conv_fwd(const gdn_config& cfg, const void* x, int64_t ld_x, void* y,
                             int64_t ld_y, const void* conv_w, void* conv_state,

@@ -49,8 +49,8 @@ constexpr int SM_XB = SM_TI + 16384;               // X hi | lo, 64x64 each (MMA
 constexpr int SM_AB = SM_XB + 16384;               // A^T f32 [64][AP]: column u of A is row u
 constexpr int SM_ZB = SM_AB + 64 * AP * 4;         // the previous chunk's z rows [64][128] bf16
 constexpr int SM_VEC = SM_ZB + 16384;              // g2, G, b, c, la [64] f32
-constexpr int SM_BAR = SM_VEC + 5 * 64 * 4;        // mbarrier (8 B) + TMEM slot
-constexpr int SM_TOTAL = SM_BAR + 16;
+constexpr int SM_BAR = SM_VEC + 5 * 64 * 4;        // MMA mbarrier (8 B), TMEM slot, rank pick,
+constexpr int SM_TOTAL = SM_BAR + 24;              // row-tile mbarrier (8 B at +16)
 
 constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t TM_S = 0;         // S f32                    cols   0..127
@@ -110,7 +110,19 @@ __device__ __forceinline__ void mma_pass(uint32_t d_tmem, uint32_t a, int a_rows
 
 }  // namespace
 
-__global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
+// 2-D TMA copy of a box of a row-major bf16 tensor (x = column, y = row).
+__device__ __forceinline__ void tma_rows(uint8_t* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          tc::smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+// vmap: the qkv rows [n_tok][C], zmap: the z rows [n_tok][Hv * 128], both in
+// boxes of 128 columns x 64 rows (one head of one chunk).
+__global__ void __launch_bounds__(PT, 1)
+prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap zmap) {
   extern __shared__ __align__(1024) uint8_t sm[];
   uint8_t* SHI = sm + SM_SHI;
   uint8_t* SLO = sm + SM_SLO;
@@ -129,6 +141,7 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
   float* la_s = c_s + 64;
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + SM_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SM_BAR + 8);
+  uint64_t* rbar = reinterpret_cast<uint64_t*>(sm + SM_BAR + 16);   // value / z row tiles
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int h = blockIdx.x;
@@ -167,7 +180,11 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
   }
   const uint16_t* qkv = static_cast<const uint16_t*>(p.qkv);
 
-  if (tid == 0) tc::mbar_init(mbar, 1);
+  if (tid == 0) {
+    tc::mbar_init(mbar, 1);
+    tc::mbar_init(rbar, 1);
+    tc::fence_mbar_init();
+  }
   if (warp == 0) {
     tc::tmem_alloc(tslot, TM_COLS);
     tc::tmem_relinquish();
@@ -210,7 +227,7 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     tc::tmem_st_wait();
   }
 
-  uint32_t phase = 0;
+  uint32_t phase = 0, rphase = 0;
   bool timed_out = false;
   const uint32_t id128 = tc::idesc_bf16_f32(128, 128);
   const uint32_t id64 = tc::idesc_bf16_f32(128, 64);
@@ -228,10 +245,20 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     return __syncthreads_or(!ok) == 0;
   };
 
-  // Copies of a chunk's keys and queries (into the K-major [K;Q] tile), values
-  // (row-major, into the values tile) and raw gates, in flight while the
-  // previous chunk finishes. Rows past the sequence end are zero-filled.
+  // Copies of a chunk's keys and queries (into the K-major [K;Q] tile, zero
+  // past the sequence end) and raw gates, in flight while the previous chunk
+  // finishes. Its value rows and the finished chunk's z rows come as one TMA
+  // box each (64 rows x 128 columns) on the row barrier; rows past the sequence
+  // end hold other tokens (zeros past n_tok) and are never used.
   float* al_raw = la_s;                                  // raw alpha until log2 is taken
+  auto copy_rows = [&](bool v, int64_t vc0, bool zz, int64_t zc0) {
+    if (tid == 0) {
+      tc::fence_async_smem();                            // earlier reads of TI / ZB come first
+      tc::mbar_arrive_expect_tx(rbar, (v ? 16384u : 0u) + (zz ? 16384u : 0u));
+      if (v) tma_rows(TI, &vmap, (2 * Hk + h) * D, (int)vc0, rbar);
+      if (zz) tma_rows(ZB, &zmap, h * D, (int)zc0, rbar);
+    }
+  };
   auto prefetch = [&](int64_t pc0, int pm) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {                        // keys / queries: a warp = 32 tokens
@@ -240,32 +267,12 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
       cp_async16(KQ + tc::kmajor_offset(isq * 64 + t, 8 * w8, 128),
                  qkv + (pc0 + tt) * C + (isq ? hq : Hk + hq) * D + 8 * w8, t < pm ? 16u : 0u);
     }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {                        // values: a warp = 2 tokens
-      const int iv = tid + k * PT, t = iv >> 4, w8 = iv & 15;
-      const int tt = t < pm ? t : 0;
-      cp_async16(TI + (t * D + 8 * w8) * 2, qkv + (pc0 + tt) * C + (2 * Hk + h) * D + 8 * w8,
-                 t < pm ? 16u : 0u);
-    }
     if (tid < C64) {
       const int t = tid, tt = t < pm ? t : 0;
       cp_async4(al_raw + t, p.alpha + (pc0 + tt) * Hv + h, t < pm ? 4u : 0u);
       cp_async4(b_s + t, p.beta + (pc0 + tt) * Hv + h, t < pm ? 4u : 0u);
     }
     cp_async_commit();
-  };
-
-  // The chunk's z rows, for its epilogue during the next chunk; they land with
-  // the next chunk's inputs (rows past the end zero-filled).
-  auto prefetch_z = [&](int64_t zc0, int zm) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {                        // 64 tokens x 16 pieces of 16 bytes
-      const int iz = tid + k * PT, t = iz >> 4, w8 = iz & 15;
-      const int tt = t < zm ? t : 0;
-      cp_async16(ZB + (t * D + 8 * w8) * 2,
-                 static_cast<const uint16_t*>(p.z) + (zc0 + tt) * Hv * D + (int64_t)h * D + 8 * w8,
-                 t < zm ? 16u : 0u);
-    }
   };
 
   // z-gated RMSNorm of a chunk's outputs by the 128 owner threads (16 lanes per
@@ -310,7 +317,10 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
 
   int64_t prev_c0 = -1;
   int prev_m = 0;
-  if (seq0 < seq1) prefetch(seq0, (int)(seq1 - seq0 < C64 ? seq1 - seq0 : C64));
+  if (seq0 < seq1) {
+    prefetch(seq0, (int)(seq1 - seq0 < C64 ? seq1 - seq0 : C64));
+    copy_rows(true, seq0, false, 0);
+  }
   for (int64_t c0 = seq0; c0 < seq1; c0 += C64) {
     const int m = (int)(seq1 - c0 < C64 ? seq1 - c0 : C64);
 
@@ -318,7 +328,11 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     //          take log2 of the gates (alpha = 1 past the end: zero-filled raw
     //          alpha is mapped to log2 = 0)
     cp_async_wait_all();
-    __syncthreads();
+    {
+      const bool ok = tc::mbar_wait(rbar, rphase, WAIT_POLLS);
+      if (__syncthreads_or(!ok)) { timed_out = true; break; }
+      rphase ^= 1;
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {                        // key pieces: a warp = 32 tokens
       const int it = tid + k * PT, t = it & 63, w8 = it >> 6;
@@ -378,7 +392,7 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int t = 16 * cb + u;
-          const float vt = bf2f(vcol[t * D]);            // zero past m
+          const float vt = t < m ? bf2f(vcol[t * D]) : 0.f;   // rows past m: other tokens
           const float bt = b_s[t];
           r[t] = __fmaf_rn(-__fmul_rn(bt, G_s[t]), pk[u], __fmul_rn(bt, vt));
         }
@@ -431,12 +445,12 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     }
     if (!commit_and_wait()) { timed_out = true; break; }
 
-    prefetch_z(c0, m);                                   // this chunk's z: X has been consumed
     if (c0 + C64 < seq1) {                               // next chunk's inputs: KQ and TI are free
       const int64_t n0 = c0 + C64;
       prefetch(n0, (int)(seq1 - n0 < C64 ? seq1 - n0 : C64));
+      copy_rows(true, n0, true, c0);                     // and this chunk's z rows
     } else {
-      cp_async_commit();
+      copy_rows(false, 0, true, c0);
     }
 
     // ---- (h) owners: o = G (S0 q) + O^T into the output buffer (the RD region
@@ -479,14 +493,19 @@ __global__ void __launch_bounds__(PT, 1) prefill_tc_kernel(PrefillArgs p) {
     prev_m = m;
   }
   if (!timed_out && prev_c0 >= 0) {                     // the last chunk
-    cp_async_wait_all();
-    __syncthreads();
-    if (owner) epilogue(prev_c0, prev_m);
+    const bool ok = tc::mbar_wait(rbar, rphase, WAIT_POLLS);
+    if (__syncthreads_or(!ok)) timed_out = true;
+    else {
+      rphase ^= 1;
+      if (owner) epilogue(prev_c0, prev_m);
+    }
   }
 
   if (timed_out) {
     if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
     tc::mbar_wait(mbar, phase, WAIT_POLLS);              // the pending phase: work in flight
+    tc::mbar_wait(rbar, rphase, WAIT_POLLS);             // row tiles in flight
+    cp_async_wait_all();
   } else {
     const int cb0 = owner ? 0 : 4;                       // final state: row i from TMEM
 #pragma unroll 1
@@ -511,8 +530,14 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  CUtensorMap vmap, zmap;
+  const uint64_t C = (uint64_t)(2 * a.Hk + a.Hv) * D;
+  e = encode_bf16_rows_map(&vmap, a.qkv, (uint64_t)a.n_tok, C, C, D, C64);
+  if (e != cudaSuccess) return e;
+  e = encode_bf16_rows_map(&zmap, a.z, (uint64_t)a.n_tok, (uint64_t)a.Hv * D, (uint64_t)a.Hv * D, D, C64);
+  if (e != cudaSuccess) return e;
   dim3 grid(a.Hv, a.n_seq);
-  prefill_tc_kernel<<<grid, PT, smem, stream>>>(a);
+  prefill_tc_kernel<<<grid, PT, smem, stream>>>(a, vmap, zmap);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,35 @@
 
 namespace gdn {
 
+// The driver's tensor-map encoder, looked up once through the runtime.
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+cudaError_t encode_bf16_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                                 uint64_t pitch, uint32_t box_cols, uint32_t box_rows) {
+  const EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 VerifyWs verify_ws_layout(int B, int T, int Hk, int Hv, int act) {
   auto up = [](int64_t n) { return (n + 255) & ~(int64_t)255; };
   const int64_t C = (int64_t)(2 * Hk + Hv) * D;
@@ -564,29 +593,11 @@ verify_state_kernel(StepArgs p, const __grid_constant__ CUtensorMap smap, const 
 }
 
 // ------------------------------------------------------------------ host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The driver's tensor-map encoder, looked up once through the runtime.
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
 
 // The state pool as a 2-D f32 tensor of 128 columns and n_slots * Hv * 128 rows,
 // copied in boxes of 32 columns x 128 rows with the 128-byte swizzle.
 cudaError_t state_map(const StepArgs& a, CUtensorMap* m) {
-  const EncodeTiledFn enc = encode_fn();
+  const EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const uint64_t rows = (uint64_t)a.n_slots * (uint64_t)a.Hv * D;
   if (rows > 0x7fffffffull) return cudaErrorInvalidValue;        // TMA row coordinates are int32
