@@ -48,6 +48,33 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
        | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor: kind::tf32 (32-bit containers, tf32 arithmetic),
+// f32 accumulate, both operands K-major, dense, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+  return (1u << 4)                 // D format f32
+       | (2u << 7)                 // A format tf32
+       | (2u << 10)                // B format tf32
+       | ((uint32_t)(N >> 3) << 17)
+       | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A * B^T for one K = 8 slice of tf32 operands; issued by one thread.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Byte offset of 32-bit element (row, k) of a no-swizzle K-major tile with
+// `rows` rows: core matrices of 8 rows x 4 elements (16 bytes per row).
+__device__ __forceinline__ uint32_t kmajor32_offset(int row, int k, int rows) {
+  return (uint32_t)(((k >> 2) * (rows >> 3) + (row >> 3)) * 128 + (row & 7) * 16 + (k & 3) * 4);
+}
+
 // D[tmem] (+)= A * B^T for one K = 16 slice; issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {

@@ -25,7 +25,7 @@ VERIFY_NOALLOC_MAX_BYTES = 8 << 20
 
 EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_workspace_bytes",
            "gdn_verify_step", "gdn_verify_step_noalloc",
-           "gdn_commit_layers", "gdn_selftest_tc_gemm", "gdn_status_string"]
+           "gdn_commit_layers", "gdn_selftest_tc_gemm", "gdn_selftest_tc_gemm_tf32", "gdn_status_string"]
 
 
 class GdnError(RuntimeError):
@@ -77,6 +77,7 @@ def load() -> ctypes.CDLL:
                                                   i32, vp, vp]
             L.gdn_commit_layers.argtypes = [cfgp, vp, i32, vp, vp, i32, i32, vp]
             L.gdn_selftest_tc_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+            L.gdn_selftest_tc_gemm_tf32.argtypes = [vp, vp, vp, i32, i32, vp, vp]
             for f in EXPORTS[:-1]:
                 getattr(L, f).restype = ctypes.c_int
             L.gdn_verify_workspace_bytes.restype = ctypes.c_int64
@@ -232,3 +233,10 @@ def gdn_selftest_tc_gemm(A, B, D, *, starve_wait=False, dev_err=None, stream=Non
     _check("gdn_selftest_tc_gemm", load().gdn_selftest_tc_gemm(
         _ptr(A), _ptr(B), _ptr(D), B.shape[0], A.shape[1], int(bool(starve_wait)),
         _ptr(dev_err), _stream(A, stream)))
+
+
+def gdn_selftest_tc_gemm_tf32(A, B, D, *, dev_err=None, stream=None):
+    """Diagnostic: D[128][N] = A[128][K] @ B[N][K]^T, f32 operands on the tf32 path."""
+    _dense(A, B, D)
+    _check("gdn_selftest_tc_gemm_tf32", load().gdn_selftest_tc_gemm_tf32(
+        _ptr(A), _ptr(B), _ptr(D), B.shape[0], A.shape[1], _ptr(dev_err), _stream(A, stream)))

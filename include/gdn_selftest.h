@@ -29,6 +29,15 @@ extern "C" {
 gdn_status gdn_selftest_tc_gemm(const uint16_t* A, const uint16_t* B, float* D, int32_t N,
                                 int32_t K, int32_t starve_wait, uint32_t* dev_err, void* stream);
 
+/*
+ * D[128][N] = A[128][K] * B[N][K]^T with f32 A, B and D (row-major, device) on
+ * the tf32 tensor-core path (tcgen05.mma kind::tf32), one thread block.
+ * N in {16, 32, ..., 256}, K in {8, 16, ..., 128}. dev_err (device, nullable)
+ * receives bit 1 if the completion wait timed out. Same error returns as above.
+ */
+gdn_status gdn_selftest_tc_gemm_tf32(const float* A, const float* B, float* D, int32_t N,
+                                     int32_t K, uint32_t* dev_err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
