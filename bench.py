@@ -246,7 +246,7 @@ class PrefillWorkload:
 
 
 class StepWorkload:
-    """Verify windows (spec-verify-bf16: per window 36 verify calls of two launches each, then one
+    """Verify windows (spec-verify-bf16: per window 36 verify calls of one launch each, then one
     batched commit of the accepted prefixes of all 36 layers) or decode
     (decode-bf16: 36 verify launches with every token accepted). Each layer has
     its own conv_state and state pools; inputs are seeded and generated on the
@@ -285,8 +285,8 @@ class StepWorkload:
                                                              "conv_state", "state")}
                                          for l in self.layers], device)
         self.tokens = B * T                                 # per layer per step
-        # read-only verify: a prep and a state kernel per layer, then one commit launch
-        self.launches_per_step = L if decode else 2 * L + 1
+        # read-only verify: one cooperative launch per layer, then one commit launch
+        self.launches_per_step = L if decode else L + 1
         self.ws = None if decode else G.verify_workspace(self.cfg, B, T, device)
         nk = self.n_keep.cpu().numpy()
         S_head = D * D * 4

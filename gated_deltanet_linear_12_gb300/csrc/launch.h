@@ -62,18 +62,8 @@ cudaError_t launch_conv_fwd(const gdn_config& cfg, const void* x, int64_t ld_x, 
                             int n_seq, int64_t n_tok, int fuse_norm, cudaStream_t stream);
 cudaError_t launch_postconv_norm(const gdn_config& cfg, int in_t, const void* yin, int out_t,
                                  void* yout, int64_t n_tok, int n_sm, cudaStream_t stream);
-// Workspace of the read-only verify (byte offsets; every part 256-byte aligned):
-// post-conv rows [B][T][C] act, the [k ; q] operand tiles [B][Hk][4096 B], the
-// gate tables [B][Hv][VERIFY_TAB_FLOATS] f32.
-constexpr int VERIFY_BT_BYTES = 2 * 8 * 128 * 2;
-constexpr int VERIFY_TAB_FLOATS = 160;
-struct VerifyWs {
-  int64_t act, bt, tab, total;
-};
-VerifyWs verify_ws_layout(int B, int T, int Hk, int Hv, int act);
-
-cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, void* ws, cudaStream_t stream);
-cudaError_t launch_verify_readonly(const StepArgs& a, int act, void* ws, cudaStream_t stream);
+cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, cudaStream_t stream);
+cudaError_t launch_verify_readonly(const StepArgs& a, int act, cudaStream_t stream);
 cudaError_t launch_commit(const StepArgs& a, int L, int act, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, int act, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);

@@ -69,20 +69,10 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 16-byte global -> shared copy that bypasses registers; src_bytes = 0 fills
-// the destination with zeros (padding past the sequence end).
-__device__ __forceinline__ void cp_async16(uint8_t* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+using tc::cp_async16;
+using tc::cp_async4;
+using tc::cp_async_commit;
+using tc::cp_async_wait_all;
 
 // One row (K = 64 values) of a K-major tile with `rows` rows, as bf16 hi | lo.
 __device__ __forceinline__ void put_row64(uint8_t* hi_tile, uint8_t* lo_tile, int row, int rows,

@@ -431,8 +431,8 @@ static cudaError_t launch_mode(const StepArgs& a, dim3 grid, int nh, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, void* ws, cudaStream_t stream) {
-  if (!commit_all) return launch_verify_readonly(a, act, ws, stream);
+cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, cudaStream_t stream) {
+  if (!commit_all) return launch_verify_readonly(a, act, stream);
   dim3 grid(a.Hk, a.B, 1);
   const int nh = a.Hv / a.Hk;
   return act == GDN_BF16 ? launch_mode<BF16, VERIFY_COMMIT_ALL>(a, grid, nh, stream)

@@ -77,32 +77,18 @@ cudaError_t encode_bf16_rows_map(CUtensorMap* m, const void* base, uint64_t rows
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-VerifyWs verify_ws_layout(int B, int T, int Hk, int Hv, int act) {
-  auto up = [](int64_t n) { return (n + 255) & ~(int64_t)255; };
-  const int64_t C = (int64_t)(2 * Hk + Hv) * D;
-  const int64_t asz = act == GDN_BF16 ? 2 : 4;
-  VerifyWs w;
-  w.act = 0;
-  w.bt = up((int64_t)B * T * C * asz);
-  w.tab = w.bt + up((int64_t)B * Hk * VERIFY_BT_BYTES);
-  w.total = w.tab + up((int64_t)B * Hv * VERIFY_TAB_FLOATS * 4);
-  return w;
-}
-
 namespace {
 
 constexpr int VT = 128;                          // state kernel: thread r owns value row r
-constexpr int PT = 128;                          // prep kernel threads
 constexpr int S_BYTES = D * D * 4;               // one f32 state
-constexpr int BT_BYTES = VERIFY_BT_BYTES;        // [k_0..7 ; q_0..7] bf16, K-major
-constexpr int TAB = VERIFY_TAB_FLOATS;           // per (sequence, v head):
+constexpr int BT_BYTES = 2 * 8 * 128 * 2;        // [k_0..7 ; q_0..7] bf16, K-major
+constexpr int TAB = 160;                         // per (sequence, v head):
 constexpr int TAB_A = 0;                         //   [8][8] b_t r(t,s) (k_t.k_s), s < t
 constexpr int TAB_OC = 64;                       //   [8][8] r(t,s) (q_t.k_s), s <= t
 constexpr int TAB_G = 128;                       //   [8] g_t
 constexpr int TAB_BG = 136;                      //   [8] b_t g_t
 constexpr int TAB_B = 144;                       //   [8] b_t
 constexpr int QK_STRIDE = D + 4;                 // prep: padded f32 rows of q and k
-constexpr int MAX_GROUP = 16;                    // v heads per q/k head (checked by the API)
 
 // Byte offset of 16-byte chunk c (0..7) of line `line` (0..3) of row r: the
 // state's box `line` holds columns 32 line .. 32 line + 31 (chunk c = columns
@@ -122,11 +108,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(map), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
       : "memory");
 }
-// Programmatic dependent launch: let the next grid start / wait for the previous one.
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Shared-memory descriptor of a bf16 K-major operand in the 128-byte swizzle
 // layout (8-row groups 1024 bytes apart; the start address steps 32 bytes per
@@ -140,455 +121,531 @@ __device__ __forceinline__ float4 unpack4(uint2 u) {
                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
 }
 
-// ============================================================ prep kernel
-// The dot product of two 128-vectors (padded f32 rows in shared memory) with the
-// rounding of a warp dot product (lane l: x[4l] y[4l], then three fused
-// multiply-adds; then an xor butterfly 16, 8, 4, 2, 1), evaluated by one thread.
-__device__ __forceinline__ float dot128_as_warp(const float* a, const float* b) {
-  float part[32];
-#pragma unroll
-  for (int l = 0; l < 32; ++l) {
-    const float4 x = reinterpret_cast<const float4*>(a)[l];
-    const float4 y = reinterpret_cast<const float4*>(b)[l];
-    float p = __fmul_rn(x.x, y.x);
-    p = __fmaf_rn(x.y, y.y, p);
-    p = __fmaf_rn(x.z, y.z, p);
-    p = __fmaf_rn(x.w, y.w, p);
-    part[l] = p;
-  }
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1)
-#pragma unroll
-    for (int l = 0; l < m; ++l) part[l] = __fadd_rn(part[l], part[l + m]);
-  return part[0];
+// ============================================================ the verify kernel
+// Shared memory (no static shared variables, so the dynamic region starts at a
+// 1024-byte boundary):
+//   QK  q and k of every draft token; after the products the outputs o_t
+//       (f32 [T][128]):
+//         tensor-core variant: f32 [k_0..k_7 ; q_0..q_7], K-major, 128-byte
+//                              swizzle (the tf32 operand)
+//         CUDA-core, bf16:     bf16 [k_0..k_7 ; q_0..q_7], K-major
+//         CUDA-core, f32:      padded f32 rows [k | q][8][QK_STRIDE]
+//   SR  the state, four TMA boxes [32 columns][128 rows] f32, 128-byte swizzle
+//       (1024-byte aligned)
+//   VS  v rows [8][128] (activation dtype)
+//   TB  the table of gate products and dot products (TAB floats)
+//   GS  alpha, beta of this head [2][8]
+//   BR  the state, product and Gram barriers, the TMEM address
+template <int A, bool TC> __host__ __device__ constexpr int qk_bytes() {
+  return TC ? 2 * MAXT * D * 4 : A == BF16 ? BT_BYTES : 2 * MAXT * QK_STRIDE * 4;
 }
-
-template <int A>
-__global__ void __launch_bounds__(PT, 4) verify_prep_kernel(StepArgs p, uint8_t* __restrict__ ws, VerifyWs wl,
-                                                            void* __restrict__ act_rows) {
-  pdl_launch_dependents();                               // the state kernel may start its copies
-  __shared__ __align__(16) float q_s[MAXT * QK_STRIDE];
-  __shared__ __align__(16) float k_s[MAXT * QK_STRIDE];
-  __shared__ float kk_s[MAXT * MAXT], qk_s[MAXT * MAXT];
-  __shared__ float al_s[MAX_GROUP * MAXT], be_s[MAX_GROUP * MAXT];
-  const int tid = threadIdx.x;
-  const int hq = blockIdx.x, b = blockIdx.y;
-  const int T = p.T, Hk = p.Hk, Hv = p.Hv, G = Hv / Hk, h0 = hq * G, nh = 2 + G;
-  const int C = (2 * Hk + Hv) * D;
-  const int slot = p.slot_idx[b];
-  if (slot < 0) return;                                   // padding entry
-  if (slot >= p.n_slots) {
-    if (tid == 0 && hq == 0) report(p.dev_err, GDN_DEVERR_SLOT);
-    return;
-  }
-
-  // ---- post-conv activations. Item (part, head, l16): 8 channels of head `head`
-  // (0 q, 1 k, 2.. v) for tokens 4 part .. 4 part + 3; rows t..t+3 of
-  // (conv_state rows ++ draft rows) feed token t. 16-lane groups share (part, head).
-  // The gates are loaded behind the rows and staged after the conv.
-  {
-    const int n_parts = (T + 3) / 4;
-    const int n_items = n_parts * nh * 16;
-    const int64_t xb = (int64_t)b * T * C;
-    const int64_t cs = (int64_t)slot * KS * C;
-    for (int base = 0; base < n_items; base += PT) {      // uniform trip count
-      const int item = base + tid;
-      const bool grp = item < n_items;                    // uniform per 16 lanes
-      const int l16 = item & 15, head = (item >> 4) % nh, part = (item >> 4) / nh;
-      const int t0 = 4 * part;
-      const int c = (head == 0 ? hq * D : head == 1 ? (Hk + hq) * D : (2 * Hk + h0 + head - 2) * D) + l16 * 8;
-      Raw8<A> wr[4], rw[7];
-      if (grp) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) raw_load<A>(p.conv_w, (int64_t)c * KW + 8 * q, wr[q]);
-#pragma unroll
-        for (int j = 0; j < 7; ++j) {
-          const int idx = t0 + j;
-          if (idx < KS) raw_load<A>(p.conv_state, cs + (int64_t)idx * C + c, rw[j]);
-          else if (idx - KS < T) raw_load<A>(p.x, xb + (int64_t)(idx - KS) * C + c, rw[j]);
-          else raw_zero<A>(rw[j]);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) raw_zero<A>(wr[q]);
-#pragma unroll
-        for (int j = 0; j < 7; ++j) raw_zero<A>(rw[j]);
-      }
-      float ga = 0.f, gb = 0.f;                           // this thread's gate pair, if any
-      const bool gate = base == 0 && tid < G * T;         // G * T <= 128 = PT
-      if (gate) {
-        const int64_t gi = ((int64_t)b * T + tid % T) * Hv + h0 + tid / T;
-        ga = p.alpha[gi];
-        gb = p.beta[gi];
-      }
-      float2 w[4][4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float t8[8];
-        raw_unpack<A>(wr[q], t8);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w[q][j] = make_float2(t8[j], t8[4 + j]);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = t0 + u;
-        const bool live = grp && t < T;
-        float v[8];
-        if (live) {
-          float r0[8], r1[8], r2[8], r3[8];
-          raw_unpack<A>(rw[u], r0);
-          raw_unpack<A>(rw[u + 1], r1);
-          raw_unpack<A>(rw[u + 2], r2);
-          raw_unpack<A>(rw[u + 3], r3);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 a = silu2(conv4x2(w[q][0], w[q][1], w[q][2], w[q][3],
-                                           make_float2(r0[2 * q], r0[2 * q + 1]),
-                                           make_float2(r1[2 * q], r1[2 * q + 1]),
-                                           make_float2(r2[2 * q], r2[2 * q + 1]),
-                                           make_float2(r3[2 * q], r3[2 * q + 1])));
-            v[2 * q] = a.x;
-            v[2 * q + 1] = a.y;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = 0.f;
-        }
-        const float ss = head_sum_sq16(v);                // all 32 lanes of the warp
-        if (live && head < 2) {
-          const float r = inv_norm(ss, p.eps);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], r);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = round_act<A>(v[j]);
-        if (live) {
-          store8<A>(act_rows, xb + (int64_t)t * C + c, v);
-          if (head < 2) {
-            float* dst = (head == 0 ? q_s : k_s) + t * QK_STRIDE + l16 * 8;
-            reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
-            reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
-          }
-        }
-      }
-      if (gate) {
-        al_s[(tid / T) * MAXT + tid % T] = ga;
-        be_s[(tid / T) * MAXT + tid % T] = gb;
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- k.k and q.k dot products (one pair per thread), the operand tile
-  {
-    const int which = tid >> 6, t = (tid >> 3) & 7, s = tid & 7;   // 0: k.k (s < t), 1: q.k (s <= t)
-    if (t < T && (which == 0 ? s < t : s <= t)) {
-      const float d = dot128_as_warp((which == 0 ? k_s : q_s) + t * QK_STRIDE, k_s + s * QK_STRIDE);
-      (which == 0 ? kk_s : qk_s)[t * MAXT + s] = d;
-    }
-  }
-  if constexpr (A == BF16) {                              // 16 rows x 16 chunks of 8, K-major
-    for (int e = tid; e < 256; e += PT) {
-      const int row = e >> 4, kc = e & 15, t = row & 7;
-      uint32_t wd[4] = {0u, 0u, 0u, 0u};
-      if (t < T) {
-        const float* src = (row < 8 ? k_s : q_s) + t * QK_STRIDE + 8 * kc;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(src[2 * j], src[2 * j + 1]);
-          wd[j] = *reinterpret_cast<const uint32_t*>(&h2);
-        }
-      }
-      uint8_t* bt = ws + wl.bt + ((int64_t)b * Hk + hq) * BT_BYTES;
-      *reinterpret_cast<uint4*>(bt + tc::kmajor_offset(row, 8 * kc, 16)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-    }
-  }
-  __syncthreads();
-
-  // ---- gate tables of each v head of the group; products in ascending order
-  // (r(t,s) = a_{s+1} ... a_t, g_t = a_0 ... a_t)
-  for (int e = tid; e < G * MAXT * MAXT; e += PT) {
-    const int g = e >> 6, t = (e >> 3) & 7, s = e & 7;
-    if (t >= T || s > t) continue;
-    const float* al = al_s + g * MAXT;
-    float* tab = reinterpret_cast<float*>(ws + wl.tab) + ((int64_t)b * Hv + h0 + g) * TAB;
-    float r = 1.f;
-    for (int u = s + 1; u <= t; ++u) r = __fmul_rn(r, al[u]);
-    const float bt = be_s[g * MAXT + t];
-    if (s < t) tab[TAB_A + t * MAXT + s] = __fmul_rn(__fmul_rn(bt, r), kk_s[t * MAXT + s]);
-    tab[TAB_OC + t * MAXT + s] = __fmul_rn(r, qk_s[t * MAXT + s]);
-    if (s == 0) {
-      float gt = al[0];
-      for (int u = 1; u <= t; ++u) gt = __fmul_rn(gt, al[u]);
-      tab[TAB_G + t] = gt;
-      tab[TAB_BG + t] = __fmul_rn(bt, gt);
-      tab[TAB_B + t] = bt;
-    }
-  }
-}
-
-// ============================================================ state kernel
-// Shared memory: the state (then its hi | lo parts, then the outputs), the
-// operand tile (bf16) or k and q rows (f32), v rows, z rows, the table row, norm_w.
-template <int A> __host__ __device__ constexpr int qk_bytes() { return A == BF16 ? BT_BYTES : 2 * MAXT * D * 4; }
+template <int A, bool TC> __host__ __device__ constexpr int qk_region() { return (qk_bytes<A, TC>() + 1023) & ~1023; }
 template <int A> __host__ __device__ constexpr int rows_bytes() { return MAXT * D * (A == BF16 ? 2 : 4); }
-template <int A> __host__ __device__ constexpr int state_smem() {
-  return S_BYTES + qk_bytes<A>() + 2 * rows_bytes<A>() + TAB * 4 + D * 4;
+template <int A, bool TC> __host__ __device__ constexpr int verify_smem() {
+  return qk_region<A, TC>() + S_BYTES + rows_bytes<A>() + TAB * 4 + 2 * MAXT * 4 + 32;
 }
 
-// Activations k_t (which = 0) or q_t (which = 1), columns 4j..4j+3: bf16 from
-// the operand tile (k_t row t, q_t row 8 + t), f32 from the k | q rows.
-template <int A>
+// Byte offset of f32 element (row, k) of the [16][128] tf32 operand in the
+// 128-byte-swizzled K-major layout: K blocks of 32 columns, 2048 bytes each (two
+// 8-row groups of 1024 bytes), 128 bytes per row, 16-byte chunk c of row r at
+// chunk c ^ (r mod 8).
+__device__ __forceinline__ uint32_t bsw_off(int row, int k) {
+  return (uint32_t)((k >> 5) * 2048 + (row >> 3) * 1024 + (row & 7) * 128 + ((((k & 31) >> 2) ^ (row & 7)) << 4) +
+                    (k & 3) * 4);
+}
+
+// Activations k_t (which = 0) or q_t (which = 1), columns 4j..4j+3.
+template <int A, bool TC>
 __device__ __forceinline__ float4 act4(const uint8_t* QK, int which, int t, int j) {
-  if constexpr (A == BF16) {
+  if constexpr (TC) {
+    return *reinterpret_cast<const float4*>(QK + bsw_off(8 * which + t, 4 * j));
+  } else if constexpr (A == BF16) {
     return unpack4(*reinterpret_cast<const uint2*>(QK + tc::kmajor_offset(8 * which + t, 4 * j, 16)));
   } else {
-    return reinterpret_cast<const float4*>(QK + which * MAXT * D * 4)[t * (D / 4) + j];
+    return reinterpret_cast<const float4*>(QK + (which * MAXT + t) * QK_STRIDE * 4)[j];
   }
 }
+
+// Stores 8 rounded activations (columns c .. c + 7) of k_t (which = 0) or q_t.
+template <int A, bool TC>
+__device__ __forceinline__ void put_act8(uint8_t* QK, int which, int t, int c, const float v[8]) {
+  if constexpr (TC) {
+    *reinterpret_cast<float4*>(QK + bsw_off(8 * which + t, c)) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(QK + bsw_off(8 * which + t, c + 4)) = make_float4(v[4], v[5], v[6], v[7]);
+  } else if constexpr (A == BF16) {
+    store8<A>(QK + tc::kmajor_offset(8 * which + t, c, 16), 0, v);
+  } else {
+    float4* dst = reinterpret_cast<float4*>(QK + ((which * MAXT + t) * QK_STRIDE + c) * 4);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
 template <int A> __device__ __forceinline__ float row_at(const uint8_t* R, int t, int i) {
   if constexpr (A == BF16) return bf2f(reinterpret_cast<const uint16_t*>(R)[t * D + i]);
   else return reinterpret_cast<const float*>(R)[t * D + i];
 }
 
+// Programmatic dependent launch: let the next grid start / wait for the previous one.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// A hint: start bringing a box of the state pool into L2 (no completion, no fault
+// on out-of-range boxes).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
+}
+
+// The sum (a0 + a1) + (a2 + a3) of four TMEM accumulators of 16 columns each at
+// taddr, taddr + 16, taddr + 32, taddr + 48 (this warp's 32 lanes).
+__device__ __forceinline__ void sum4_ld16(uint32_t taddr, float v[16]) {
+  float a[16], b2[16], c[16], d[16];
+  tc::tmem_ld16(taddr, a);
+  tc::tmem_ld16(taddr + 16, b2);
+  tc::tmem_ld16(taddr + 32, c);
+  tc::tmem_ld16(taddr + 48, d);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(__fadd_rn(a[i], b2[i]), __fadd_rn(c[i], d[i]));
+}
+
+// A hint: start bringing `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// L2 hints for unit u = b Hv + h (sequence b, v head h); the slot index read
+// here may still change: nothing but these hints depends on it.
+// hint_state: box `box` (0..3) of its state.
+__device__ __forceinline__ void hint_state(const StepArgs& p, const CUtensorMap* smap, int u, int box) {
+  const int Hv = p.Hv, b = u / Hv, h = u % Hv;
+  const int slot = *reinterpret_cast<const volatile int32_t*>(p.slot_idx + b);
+  if (slot >= 0 && slot < p.n_slots) tma_prefetch_2d(smap, 32 * box, (slot * Hv + h) * D);
+}
+// hint_rows: row w (0 <= w < 3 (T + 3) + T) of its conv rows (conv_state and x
+// rows of its q, k and v heads), then its z rows.
+template <int A>
+__device__ __forceinline__ void hint_rows(const StepArgs& p, int u, int T, int w) {
+  const int Hk = p.Hk, Hv = p.Hv, G = Hv / Hk, C = (2 * Hk + Hv) * D;
+  const int b = u / Hv, h = u % Hv, hq = h / G;
+  const int n_x = (T + KS) * 3;
+  if (w < 0 || w >= n_x + T) return;
+  const int slot = *reinterpret_cast<const volatile int32_t*>(p.slot_idx + b);
+  if (slot < 0 || slot >= p.n_slots) return;
+  constexpr int esz = A == BF16 ? 2 : 4;
+  if (w < n_x) {
+    const int row = w / 3, hd = w % 3;
+    const int64_t c = hd == 0 ? (int64_t)hq * D : hd == 1 ? (int64_t)(Hk + hq) * D : (int64_t)(2 * Hk + h) * D;
+    const int64_t e = row < KS ? ((int64_t)slot * KS + row) * C + c : ((int64_t)b * T + row - KS) * C + c;
+    l2_prefetch((row < KS ? static_cast<const char*>(p.conv_state) : static_cast<const char*>(p.x)) + e * esz,
+                D * esz);
+  } else {
+    const int t = w - n_x;
+    l2_prefetch(static_cast<const char*>(p.z) + (((int64_t)b * T + t) * Hv + h) * D * esz, D * esz);
+  }
+}
+
+// Resident blocks per SM (shared memory: bf16 76.5 KB, f32 79.6 KB per block).
+template <int A> __host__ __device__ constexpr int blocks_per_sm() { return A == BF16 ? 3 : 2; }
+
+// One block per (sequence b, v head h), launched as a programmatic dependent of
+// the previous grid on the stream; thread r owns value row r of the state.
+// Before waiting for the previous grid the block sets up its barriers (and TMEM)
+// and gives L2 hints: its own state (for the blocks that become resident while
+// the previous grid drains) and the rows of the unit one wave of resident blocks
+// later. Everything the block reads is read after the wait (a hint only uses a
+// slot index that may still change). Then thread 0 starts the four TMA copies of
+// the state, and per block:
+//   - the conv + SiLU of the unit's q, k and v heads for the T draft rows (rows
+//     t..t+3 of conv_state ++ x feed token t) and the L2 norms of q and k; q, k, v
+//     rounded to the activation dtype are kept in shared memory;
+//   - the dot products k_t.k_s (s < t), q_t.k_s (s <= t) and the table
+//     b_t r(t,s) (k_t.k_s), r(t,s) (q_t.k_s), g_t, b_t g_t, b_t, with
+//     r(t,s) = a_{s+1} ... a_t and g_t = a_0 ... a_t;
+//   - the 2T products S0 k_t, S0 q_t of every value row;
+//   - deltas, outputs and the z-gated RMSNorm of every draft token.
+// Two variants of the products:
+//   - CUDA cores (T = 1, and f32 activations): thread r reads its swizzled f32
+//     row with the step kernel's rounding; the dot products are warp dot
+//     products with the step kernel's rounding;
+//   - tensor core (TC: bf16 activations, T >= 2): one tcgen05 kind::tf32 product
+//     S0 [k_0..k_7 ; q_0..q_7]^T (M = 128, N = 16, K = 128) straight from the TMA
+//     boxes, and the Gram product [k ; q] [k ; q]^T of the same operand tile (its
+//     rows 16..127 are whatever follows the tile and land in unused TMEM lanes)
+//     for the dot products. The state is read as tf32; k and q, bf16 values, are
+//     exact in tf32.
 // NT > 0: the number of draft tokens as a compile-time constant (CUDA-core
-// variants; keeps the unrolled code small enough for the instruction cache);
-// NT = 0: read from the arguments.
+// variants; keeps the unrolled code small); NT = 0: read from the arguments.
 template <int A, bool TC, int NT>
-__global__ void __launch_bounds__(VT, 3)
-verify_state_kernel(StepArgs p, const __grid_constant__ CUtensorMap smap, const uint8_t* __restrict__ ws,
-                    VerifyWs wl, const void* __restrict__ act_rows) {
+__global__ void __launch_bounds__(VT, blocks_per_sm<A>())
+    verify_kernel(StepArgs p, const __grid_constant__ CUtensorMap smap, int ahead) {
+  pdl_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x, b = blockIdx.y;
   const int T = NT > 0 ? NT : p.T;
-  const int Hk = p.Hk, Hv = p.Hv, G = Hv / Hk, hq = h / G;
-  const int C = (2 * Hk + Hv) * D;
-  const int slot = p.slot_idx[b];
-  if (slot < 0 || slot >= p.n_slots) return;              // padding, or reported by the prep kernel
+  const int Hk = p.Hk, Hv = p.Hv, G = Hv / Hk, C = (2 * Hk + Hv) * D;
+  const int b = blockIdx.x / Hv, h = blockIdx.x % Hv, hq = h / G;
 
-  uint8_t* SR = smem;                                     // state -> hi | lo -> outputs
-  uint8_t* QK = SR + S_BYTES;                             // operand tile (bf16) / k, q rows (f32)
-  uint8_t* VR = QK + qk_bytes<A>();                       // v rows [T][128]
-  uint8_t* ZR = VR + rows_bytes<A>();                     // z rows [T][128]
-  float* tb = reinterpret_cast<float*>(ZR + rows_bytes<A>());       // the table row
-  float* nw = tb + TAB;                                              // norm_w
-  constexpr int asz = A == BF16 ? 2 : 4;
-  constexpr uint32_t row_bytes = D * asz;
+  uint8_t* QK = smem;                                     // q, k; then the outputs
+  uint8_t* SR = smem + qk_region<A, TC>();                // the state
+  uint8_t* VS = SR + S_BYTES;                             // v rows
+  float* tb = reinterpret_cast<float*>(VS + rows_bytes<A>());       // the table
+  float* al_s = tb + TAB;                                           // alpha, beta
+  float* be_s = al_s + MAXT;
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(be_s + MAXT);      // 8-byte aligned
+  uint64_t* tc_bar = s_bar + 1;
+  uint64_t* g_bar = s_bar + 2;
+  uint32_t* tc_slot = reinterpret_cast<uint32_t*>(s_bar + 3);
 
-  __shared__ uint64_t s_bar, tc_bar;
-  __shared__ uint32_t tc_slot;
   if (tid == 0) {
-    tc::mbar_init(&s_bar, 1);
-    if constexpr (TC) tc::mbar_init(&tc_bar, 1);
+    tc::mbar_init(s_bar, 1);
+    if constexpr (TC) {
+      tc::mbar_init(tc_bar, 1);
+      tc::mbar_init(g_bar, 1);
+    }
     tc::fence_mbar_init();
-    tc::fence_async_smem();
+  } else if (warp == 3) {
+    // L2 hints (warp 3 has no conv item): this unit's state, and the rows of the
+    // unit one wave of resident blocks later, so that its small loads hit L2
+    if (lane < 4) hint_state(p, &smap, b * Hv + h, lane);
+    const int u2 = (int)blockIdx.x + ahead;
+    if (u2 < (int)gridDim.x) {
+      hint_rows<A>(p, u2, T, lane);
+      hint_rows<A>(p, u2, T, lane + 32);
+    }
   }
   if constexpr (TC) {
     if (warp == 1) {
-      tc::tmem_alloc(&tc_slot, 32);
+      tc::tmem_alloc(tc_slot, 128);                       // product: 4 x 16 columns, Gram: 4 x 16
       tc::tmem_relinquish();
     }
   }
-  __syncthreads();                                        // barriers initialised before any wait
-  // ---- the state first (independent of the prep kernel), then the rest
-  if (warp == 0) {
-    if (lane == 0) {
-      const uint32_t bytes =
-          S_BYTES + (A == BF16 ? BT_BYTES : 2u * T * row_bytes) + 2u * T * row_bytes + TAB * 4 + D * 4;
-      tc::mbar_arrive_expect_tx(&s_bar, bytes);
-      const int row0 = (slot * Hv + h) * D;
+
+  pdl_wait();                                             // inputs of the previous grid are visible
+  const int slot = *reinterpret_cast<const volatile int32_t*>(p.slot_idx + b);
+  const bool valid = slot >= 0 && slot < p.n_slots;
+  if (slot >= p.n_slots && tid == 0 && h == 0) report(p.dev_err, GDN_DEVERR_SLOT);
+  if (tid == 0 && valid) {                                // thread 0 initialised the barrier
+    tc::mbar_arrive_expect_tx(s_bar, S_BYTES);
 #pragma unroll
-      for (int bx = 0; bx < 4; ++bx) tma_load_2d(SR + bx * 16384, &smap, 32 * bx, row0, &s_bar);
-    }
-    __syncwarp();
-    pdl_wait();                                           // the prep kernel's rows and tables
-    const char* act = static_cast<const char*>(act_rows);
-    const char* zp = static_cast<const char*>(p.z);
-    if (lane < T) {
-      const int t = lane;
-      const int64_t tok = (int64_t)b * T + t;
-      tc::bulk_load(VR + t * row_bytes, act + (tok * C + (int64_t)(2 * Hk + h) * D) * asz, row_bytes, &s_bar);
-      tc::bulk_load(ZR + t * row_bytes, zp + (tok * Hv * D + (int64_t)h * D) * asz, row_bytes, &s_bar);
-      if constexpr (A != BF16) {
-        tc::bulk_load(QK + t * row_bytes, act + (tok * C + (int64_t)(Hk + hq) * D) * asz, row_bytes, &s_bar);
-        tc::bulk_load(QK + MAXT * row_bytes + t * row_bytes, act + (tok * C + (int64_t)hq * D) * asz, row_bytes,
-                  &s_bar);
+    for (int bx = 0; bx < 4; ++bx) tma_load_2d(SR + bx * 16384, &smap, 32 * bx, (slot * Hv + h) * D, s_bar);
+  }
+  int fail = 0;                                           // 1: before the product, 2: the product
+
+  // z rows and norm_w of this thread's part of the epilogue
+  const int et = tid >> 4, el16 = tid & 15;
+  Raw8<A> zr;
+  float nwr[8];
+  if (valid && et < T) raw_load<A>(p.z, (((int64_t)b * T + et) * Hv + h) * D + el16 * 8, zr);
+  else raw_zero<A>(zr);
+  load8<F32>(p.norm_w, el16 * 8, nwr);
+
+  // ---- post-conv activations. Item (part, head, l16) = thread: 8 channels of
+  // head `head` (0 q, 1 k, 2 v) for tokens 4 part .. 4 part + 3 (at most 96
+  // items). 16-lane groups share (part, head).
+  auto conv_heads = [&]() {
+    const int n_items = (T + 3) / 4 * 3 * 16;
+    const int64_t xb = (int64_t)b * T * C;
+    const int64_t cs = (int64_t)slot * KS * C;
+    const bool write_qk = p.postconv && (h % G) == 0;     // one v head of the group writes q, k
+    const bool grp = tid < n_items;                       // uniform per 16 lanes
+    const int l16 = tid & 15, head = (tid >> 4) % 3, part = (tid >> 4) / 3;
+    const int t0 = 4 * part;
+    const int c = (head == 0 ? hq * D : head == 1 ? (Hk + hq) * D : (2 * Hk + h) * D) + l16 * 8;
+    Raw8<A> wr[4], rw[7];
+    if (grp) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) raw_load<A>(p.conv_w, (int64_t)c * KW + 8 * q, wr[q]);
+#pragma unroll
+      for (int j = 0; j < 7; ++j) {
+        const int idx = t0 + j;
+        if (idx < KS) raw_load<A>(p.conv_state, cs + (int64_t)idx * C + c, rw[j]);
+        else if (idx - KS < T) raw_load<A>(p.x, xb + (int64_t)(idx - KS) * C + c, rw[j]);
+        else raw_zero<A>(rw[j]);
       }
-    } else if (lane == 8) {
-      tc::bulk_load(tb, ws + wl.tab + ((int64_t)b * Hv + h) * TAB * 4, TAB * 4, &s_bar);
-    } else if (lane == 9) {
-      if constexpr (A == BF16) tc::bulk_load(QK, ws + wl.bt + ((int64_t)b * Hk + hq) * BT_BYTES, BT_BYTES, &s_bar);
-    } else if (lane == 10) {
-      tc::bulk_load(nw, p.norm_w, D * 4, &s_bar);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) raw_zero<A>(wr[q]);
+#pragma unroll
+      for (int j = 0; j < 7; ++j) raw_zero<A>(rw[j]);
+    }
+    float2 w[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float t8[8];
+      raw_unpack<A>(wr[q], t8);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[q][j] = make_float2(t8[j], t8[4 + j]);
+    }
+#pragma unroll
+    for (int uu = 0; uu < 4; ++uu) {
+      const int t = t0 + uu;
+      const bool live = grp && t < T;
+      float v[8];
+      if (live) {
+        float r0[8], r1[8], r2[8], r3[8];
+        raw_unpack<A>(rw[uu], r0);
+        raw_unpack<A>(rw[uu + 1], r1);
+        raw_unpack<A>(rw[uu + 2], r2);
+        raw_unpack<A>(rw[uu + 3], r3);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 a = silu2(conv4x2(w[q][0], w[q][1], w[q][2], w[q][3], make_float2(r0[2 * q], r0[2 * q + 1]),
+                                         make_float2(r1[2 * q], r1[2 * q + 1]), make_float2(r2[2 * q], r2[2 * q + 1]),
+                                         make_float2(r3[2 * q], r3[2 * q + 1])));
+          v[2 * q] = a.x;
+          v[2 * q + 1] = a.y;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.f;
+      }
+      const float ss = head_sum_sq16(v);                  // all 32 lanes of the warp
+      if (live && head < 2) {
+        const float rr = inv_norm(ss, p.eps);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], rr);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = round_act<A>(v[j]);
+      if (live) {
+        if (p.postconv && (head == 2 || write_qk)) store8<A>(p.postconv, xb + (int64_t)t * C + c, v);
+        if (head == 2) store8<A>(VS, (int64_t)t * D + l16 * 8, v);
+        else put_act8<A, TC>(QK, head ^ 1, t, l16 * 8, v);   // k rows 0..7, q rows 8..15
+      }
+    }
+    if constexpr (TC) {                                   // rows of absent tokens are zero operands
+      for (int e = tid; e < 16 * (D / 4); e += VT) {
+        const int row = e >> 5, kc = e & 31;
+        if ((row & 7) >= T) *reinterpret_cast<float4*>(QK + bsw_off(row, 4 * kc)) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  };
+
+  if (valid) {
+    float ga = 0.f, gb = 0.f;
+    if (tid < T) {
+      const int64_t gi = ((int64_t)b * T + tid) * Hv + h;
+      ga = p.alpha[gi];
+      gb = p.beta[gi];
+    }
+    conv_heads();
+    if (tid < T) {
+      al_s[tid] = ga;
+      be_s[tid] = gb;
     }
   }
-  const bool s_ok = tc::mbar_wait(&s_bar, 0, 1u << 24);
-  if constexpr (TC) tc::fence_before_sync();
-  const bool s_failed = __syncthreads_or(!s_ok);
-  bool failed = s_failed;
 
-  const int r = tid;                                      // value row
-  float sk[MAXT], sq[MAXT];
-  uint32_t tbase = 0;
-  if (failed) {
-    // error exit below
-  } else if constexpr (TC) {
-    // row r as bf16 hi | lo in place: columns 0..63 (lines 0, 1) give hi -> line 0
-    // and lo -> line 2; columns 64..127 (lines 2, 3) give hi -> line 1 and
-    // lo -> line 3. Every line is read before it is overwritten.
-    float x[64];
-    uint4 hi[8], lo[8];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const float4 f = *reinterpret_cast<const float4*>(SR + line_off(c >> 3, r, c & 7));
-      x[4 * c] = f.x; x[4 * c + 1] = f.y; x[4 * c + 2] = f.z; x[4 * c + 3] = f.w;
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) tc::split8(x + 8 * c, hi[c], lo[c]);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(SR + line_off(0, r, c)) = hi[c];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const float4 f = *reinterpret_cast<const float4*>(SR + line_off(2 + (c >> 3), r, c & 7));
-      x[4 * c] = f.x; x[4 * c + 1] = f.y; x[4 * c + 2] = f.z; x[4 * c + 3] = f.w;
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(SR + line_off(2, r, c)) = lo[c];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) tc::split8(x + 8 * c, hi[c], lo[c]);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      *reinterpret_cast<uint4*>(SR + line_off(1, r, c)) = hi[c];
-      *reinterpret_cast<uint4*>(SR + line_off(3, r, c)) = lo[c];
-    }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    tbase = tc_slot;
-    if (tid == 0) {
-      const uint32_t sh = tc::smem_u32(SR), sl = sh + 32768, bt = tc::smem_u32(QK);
-      const uint32_t id = tc::idesc_bf16_f32(128, 16);
+  if constexpr (TC) tc::fence_async_smem();               // the operand rows -> tensor core
+  if constexpr (TC) tc::fence_before_sync();
+  __syncthreads();                                        // also: barriers and TMEM address visible
+  if constexpr (TC) tc::fence_after_sync();
+  const uint32_t tbase = TC ? *tc_slot : 0u;
+
+  do {                                                    // once; left early on a failed wait
+    if (!valid) break;                                    // padding entry or bad slot: no outputs
+    bool ok = true;
+    if constexpr (TC) {
+      // ---- warp 0: thread 0 issues the Gram product and, as soon as the state is
+      // in, the state product (the tensor core runs
+      // them in order); the warp moves the Gram values into the table while the
+      // state product runs. Four independent accumulators (one per 32-column
+      // block of K) keep the accumulation chains short; their sum is formed on the
+      // CUDA cores.
+      if (warp == 0) {
+        if (lane == 0) {
+          const uint32_t bq = tc::smem_u32(QK), sa = tc::smem_u32(SR);
+          const uint32_t id = tc::idesc_tf32_f32(128, 16);
 #pragma unroll 1
-      for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tbase, smem_desc_sw128(sh + (ks >> 2) * 16384 + (ks & 3) * 32),
-                     tc::smem_desc(bt + ks * 512, 256, 128), id, ks > 0);
+          for (int ks = 0; ks < 16; ++ks) {
+            const uint64_t dq = smem_desc_sw128(bq + (ks >> 2) * 2048 + (ks & 3) * 32);
+            tc::mma_tf32(tbase + 64 + 16 * (ks & 3), dq, dq, id, ks > 3);
+          }
+          tc::mma_commit(g_bar);
+          ok = tc::mbar_wait(s_bar, 0, 1u << 24);
+          if (ok) {
 #pragma unroll 1
-      for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16(tbase, smem_desc_sw128(sl + (ks >> 2) * 16384 + (ks & 3) * 32),
-                     tc::smem_desc(bt + ks * 512, 256, 128), id, 1);
-      tc::mma_commit(&tc_bar);
+            for (int ks = 0; ks < 16; ++ks)
+              tc::mma_tf32(tbase + 16 * (ks & 3), smem_desc_sw128(sa + (ks >> 2) * 16384 + (ks & 3) * 32),
+                           smem_desc_sw128(bq + (ks >> 2) * 2048 + (ks & 3) * 32), id, ks > 3);
+            tc::mma_commit(tc_bar);
+          }
+        }
+        const bool ok0 = __shfl_sync(0xffffffffu, ok, 0);   // thread 0's state wait
+        const bool okg = tc::mbar_wait(g_bar, 0, 1u << 24);
+        tc::fence_after_sync();
+        ok = ok0 && okg;
+        if (__all_sync(0xffffffffu, okg)) {
+          float gv[16];
+          sum4_ld16(tbase + 64, gv);                      // lane l: row l (k_l, or q_{l-8})
+          const int t = lane & 7;
+          if (lane < 16 && t < T) {
+#pragma unroll
+            for (int s = 0; s < MAXT; ++s)
+              if (lane < 8 ? s < t : s <= t) tb[(lane < 8 ? TAB_A : TAB_OC) + t * MAXT + s] = gv[s];
+          }
+        }
+      }
+    } else {
+      // ---- dot products: warp w takes the pairs w, w + 4, ... of the order
+      // t = 0, 1, ...: (k_t.k_s, s < t) then (q_t.k_s, s <= t); the pairs of the
+      // first T tokens are the first T^2. Lane l holds columns 4l..4l+3 (a product
+      // and three fused multiply-adds), then an xor butterfly 16, 8, 4, 2, 1: the
+      // step kernel's warp dot product.
+#pragma unroll 1
+      for (int i = warp; i < T * T; i += VT / 32) {
+        const int t = (i >= 1) + (i >= 4) + (i >= 9) + (i >= 16) + (i >= 25) + (i >= 36) + (i >= 49);
+        const int j = i - t * t, which = j >= t, s = which ? j - t : j;
+        const float4 x = act4<A, TC>(QK, which, t, lane);
+        const float4 y = act4<A, TC>(QK, 0, s, lane);
+        float d = __fmul_rn(x.x, y.x);
+        d = __fmaf_rn(x.y, y.y, d);
+        d = __fmaf_rn(x.z, y.z, d);
+        d = __fmaf_rn(x.w, y.w, d);
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, m));
+        if (lane == 0) tb[(which ? TAB_OC : TAB_A) + t * MAXT + s] = d;
+      }
     }
-    const bool ok = tc::mbar_wait(&tc_bar, 0, 1u << 24);
-    tc::fence_after_sync();
-    failed = __syncthreads_or(!ok);
-    if (!failed) {
-      float acc[16];
-      tc::tmem_ld16(tbase + ((uint32_t)(32 * warp) << 16), acc);
-#pragma unroll
-      for (int t = 0; t < MAXT; ++t) { sk[t] = acc[t]; sq[t] = acc[8 + t]; }
-    }
-  } else {
-    // row r on the CUDA cores, with the step kernel's rounding: four partial sums
-    // over the chunks j = 4m + cg (m ascending), then (p0 + p1) + (p2 + p3)
-    float pk[MAXT][4], pq[MAXT][4];
-#pragma unroll
-    for (int t = 0; t < MAXT; ++t)
-#pragma unroll
-      for (int cg = 0; cg < 4; ++cg) { pk[t][cg] = 0.f; pq[t][cg] = 0.f; }
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int cg = j & 3;
-      const float4 s4 = *reinterpret_cast<const float4*>(SR + line_off(j >> 3, r, j & 7));
-#pragma unroll
-      for (int t = 0; t < MAXT; ++t) {
-        if (t < T) {
-          const float4 k = act4<A>(QK, 0, t, j);
-          float a = pk[t][cg];
-          a = __fmaf_rn(s4.x, k.x, a); a = __fmaf_rn(s4.y, k.y, a);
-          a = __fmaf_rn(s4.z, k.z, a); a = __fmaf_rn(s4.w, k.w, a);
-          pk[t][cg] = a;
-          const float4 q = act4<A>(QK, 1, t, j);
-          float c = pq[t][cg];
-          c = __fmaf_rn(s4.x, q.x, c); c = __fmaf_rn(s4.y, q.y, c);
-          c = __fmaf_rn(s4.z, q.z, c); c = __fmaf_rn(s4.w, q.w, c);
-          pq[t][cg] = c;
+    if (__syncthreads_or(!ok)) { fail = 1; break; }     // also: the dot products are in
+
+    // ---- the table, one entry per thread (which, t, s), from the dot products in
+    // place; products in ascending order
+    {
+      const int which = tid >> 6, t = (tid >> 3) & 7, s = tid & 7;
+      if (t < T && (which == 0 ? s < t : s <= t)) {
+        float rr = 1.f;
+        for (int w = s + 1; w <= t; ++w) rr = __fmul_rn(rr, al_s[w]);
+        const float bt = be_s[t];
+        if (which == 0) {
+          tb[TAB_A + t * MAXT + s] = __fmul_rn(__fmul_rn(bt, rr), tb[TAB_A + t * MAXT + s]);
+        } else {
+          tb[TAB_OC + t * MAXT + s] = __fmul_rn(rr, tb[TAB_OC + t * MAXT + s]);
+          if (s == 0) {
+            float gt = al_s[0];
+            for (int w = 1; w <= t; ++w) gt = __fmul_rn(gt, al_s[w]);
+            tb[TAB_G + t] = gt;
+            tb[TAB_BG + t] = __fmul_rn(bt, gt);
+            tb[TAB_B + t] = bt;
+          }
         }
       }
     }
-#pragma unroll
-    for (int t = 0; t < MAXT; ++t) {
-      sk[t] = __fadd_rn(__fadd_rn(pk[t][0], pk[t][1]), __fadd_rn(pk[t][2], pk[t][3]));
-      sq[t] = __fadd_rn(__fadd_rn(pq[t][0], pq[t][1]), __fadd_rn(pq[t][2], pq[t][3]));
-    }
-  }
 
-  if (failed) {                    // a completion wait gave up: no outputs for this state
-    if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
-    if (s_failed) tc::mbar_wait(&s_bar, 0, 1u << 24);   // the copies, if still in flight
+    // ---- the products
+    const int r = tid;                                    // value row
+    float sk[MAXT], sq[MAXT];
     if constexpr (TC) {
-      if (!s_failed) tc::mbar_wait(&tc_bar, 0, 1u << 24);   // the product in flight
-      tc::fence_before_sync();
-      __syncthreads();
-      if (warp == 1) tc::tmem_dealloc(tc_slot, 32);
-    }
-    return;
-  }
-
-  // ---- deltas and outputs of row r (the step kernel's order)
-  float o[MAXT];
-  {
-    float dr[MAXT];
+      ok = tc::mbar_wait(tc_bar, 0, 1u << 24);
+      tc::fence_after_sync();
+      if (__syncthreads_or(!ok)) { fail = 2; break; }     // also: the table is complete
+      float acc[16];
+      sum4_ld16(tbase + ((uint32_t)(32 * warp) << 16), acc);
 #pragma unroll
-    for (int t = 0; t < MAXT; ++t) {
-      if (t < T) {
-        float x = __fmaf_rn(-tb[TAB_BG + t], sk[t], __fmul_rn(tb[TAB_B + t], row_at<A>(VR, t, r)));
+      for (int t = 0; t < MAXT; ++t) { sk[t] = acc[t]; sq[t] = acc[8 + t]; }
+    } else {
+      ok = tc::mbar_wait(s_bar, 0, 1u << 24);
+      if (__syncthreads_or(!ok)) { fail = 1; break; }     // also: the table is complete
+      // row r with the step kernel's rounding: four partial sums over the chunks
+      // j = 4m + cg (m ascending), then (p0 + p1) + (p2 + p3)
+      float pk[MAXT][4], pq[MAXT][4];
 #pragma unroll
-        for (int u = 0; u < t; ++u) x = __fmaf_rn(-tb[TAB_A + t * MAXT + u], dr[u], x);
-        dr[t] = x;
-        float y = __fmul_rn(tb[TAB_G + t], sq[t]);
+      for (int t = 0; t < MAXT; ++t)
 #pragma unroll
-        for (int u = 0; u <= t; ++u) y = __fmaf_rn(tb[TAB_OC + t * MAXT + u], dr[u], y);
-        o[t] = __fmul_rn(y, p.q_scale);
+        for (int cg = 0; cg < 4; ++cg) { pk[t][cg] = 0.f; pq[t][cg] = 0.f; }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int cg = j & 3;
+        const float4 s4 = *reinterpret_cast<const float4*>(SR + line_off(j >> 3, r, j & 7));
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t) {
+          if (t < T) {
+            const float4 k = act4<A, TC>(QK, 0, t, j);
+            float a = pk[t][cg];
+            a = __fmaf_rn(s4.x, k.x, a); a = __fmaf_rn(s4.y, k.y, a);
+            a = __fmaf_rn(s4.z, k.z, a); a = __fmaf_rn(s4.w, k.w, a);
+            pk[t][cg] = a;
+            const float4 q = act4<A, TC>(QK, 1, t, j);
+            float c = pq[t][cg];
+            c = __fmaf_rn(s4.x, q.x, c); c = __fmaf_rn(s4.y, q.y, c);
+            c = __fmaf_rn(s4.z, q.z, c); c = __fmaf_rn(s4.w, q.w, c);
+            pq[t][cg] = c;
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < MAXT; ++t) {
+        sk[t] = __fadd_rn(__fadd_rn(pk[t][0], pk[t][1]), __fadd_rn(pk[t][2], pk[t][3]));
+        sq[t] = __fadd_rn(__fadd_rn(pq[t][0], pq[t][1]), __fadd_rn(pq[t][2], pq[t][3]));
       }
     }
-  }
-  if constexpr (TC) tc::fence_before_sync();
-  __syncthreads();                                        // the state region is free
-  float* o_s = reinterpret_cast<float*>(SR);
-#pragma unroll
-  for (int t = 0; t < MAXT; ++t)
-    if (t < T) o_s[t * D + r] = o[t];
-  __syncthreads();
+    if constexpr (TC) tc::fence_before_sync();
+    __syncthreads();                                      // q and k are no longer needed
 
-  // ---- z-gated RMSNorm: one 16-lane group per token
-  {
-    const int t = tid >> 4, l16 = tid & 15;
-    const bool live = t < T;
-    float ov[8];
-    if (live) {
-      const float4 u0 = reinterpret_cast<const float4*>(o_s + t * D)[2 * l16];
-      const float4 u1 = reinterpret_cast<const float4*>(o_s + t * D)[2 * l16 + 1];
-      ov[0] = u0.x; ov[1] = u0.y; ov[2] = u0.z; ov[3] = u0.w;
-      ov[4] = u1.x; ov[5] = u1.y; ov[6] = u1.z; ov[7] = u1.w;
-    } else {
+    // ---- deltas and outputs of row r (the step kernel's order)
+    float o[MAXT];
+    {
+      float dr[MAXT];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ov[j] = 0.f;
+      for (int t = 0; t < MAXT; ++t) {
+        if (t < T) {
+          float xx = __fmaf_rn(-tb[TAB_BG + t], sk[t], __fmul_rn(tb[TAB_B + t], row_at<A>(VS, t, r)));
+#pragma unroll
+          for (int w = 0; w < t; ++w) xx = __fmaf_rn(-tb[TAB_A + t * MAXT + w], dr[w], xx);
+          dr[t] = xx;
+          float y = __fmul_rn(tb[TAB_G + t], sq[t]);
+#pragma unroll
+          for (int w = 0; w <= t; ++w) y = __fmaf_rn(tb[TAB_OC + t * MAXT + w], dr[w], y);
+          o[t] = __fmul_rn(y, p.q_scale);
+        }
+      }
     }
-    const float ss = head_sum_sq16(ov);
-    if (live) {
-      const float rn = inv_norm(__fmul_rn(ss, 1.0f / D), p.eps);
-      float zv[8], res[8];
-      load8<A>(ZR, (int64_t)t * D + l16 * 8, zv);
+    float* o_s = reinterpret_cast<float*>(QK);            // [T][128] f32
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        res[j] = __fmul_rn(__fmul_rn(__fmul_rn(ov[j], rn), nw[l16 * 8 + j]), silu_gate(zv[j]));
-      store8<A>(p.out, ((int64_t)b * T + t) * Hv * D + (int64_t)h * D + l16 * 8, res);
+    for (int t = 0; t < MAXT; ++t)
+      if (t < T) o_s[t * D + r] = o[t];
+    __syncthreads();
+
+    // ---- z-gated RMSNorm: one 16-lane group per token
+    {
+      const bool live = et < T;
+      float ov[8];
+      if (live) {
+        const float4 u0 = reinterpret_cast<const float4*>(o_s + et * D)[2 * el16];
+        const float4 u1 = reinterpret_cast<const float4*>(o_s + et * D)[2 * el16 + 1];
+        ov[0] = u0.x; ov[1] = u0.y; ov[2] = u0.z; ov[3] = u0.w;
+        ov[4] = u1.x; ov[5] = u1.y; ov[6] = u1.z; ov[7] = u1.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ov[j] = 0.f;
+      }
+      const float ss = head_sum_sq16(ov);
+      if (live) {
+        const float rn = inv_norm(__fmul_rn(ss, 1.0f / D), p.eps);
+        float zv[8], res[8];
+        raw_unpack<A>(zr, zv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          res[j] = __fmul_rn(__fmul_rn(__fmul_rn(ov[j], rn), nwr[j]), silu_gate(zv[j]));
+        store8<A>(p.out, ((int64_t)b * T + et) * Hv * D + (int64_t)h * D + el16 * 8, res);
+      }
+    }
+  } while (false);
+
+  if (fail) {                       // a wait gave up: no outputs for this (sequence, head)
+    if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
+    tc::mbar_wait(s_bar, 0, 1u << 24);                    // the state copy, if still in flight
+    if constexpr (TC) {
+      tc::mbar_wait(g_bar, 0, 1u << 24);                  // the Gram product, if still running
+      if (fail == 2) tc::mbar_wait(tc_bar, 0, 1u << 24);  // the state product, if still running
     }
   }
   if constexpr (TC) {
-    if (warp == 1) tc::tmem_dealloc(tbase, 32);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) tc::tmem_dealloc(tbase, 128);
   }
 }
 
@@ -612,51 +669,49 @@ cudaError_t state_map(const StepArgs& a, CUtensorMap* m) {
 }
 
 template <int A, bool TC, int NT>
-cudaError_t launch_state(const StepArgs& a, const CUtensorMap& smap, const uint8_t* ws, const VerifyWs& wl,
-                         const void* act_rows, cudaStream_t stream) {
-  auto kern = verify_state_kernel<A, TC, NT>;
-  const int smem = state_smem<A>();
+cudaError_t launch_kernel(const StepArgs& a, const CUtensorMap& smap, cudaStream_t stream) {
+  auto kern = verify_kernel<A, TC, NT>;
+  const int smem = verify_smem<A, TC>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
+  int dev = 0, n_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int ahead = blocks_per_sm<A>() * n_sm;              // blocks resident at once
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.Hv, a.B);
+  cfg.gridDim = dim3((unsigned)((int64_t)a.B * a.Hv));
   cfg.blockDim = dim3(VT);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, smap, ws, wl, act_rows);
+  return cudaLaunchKernelEx(&cfg, kern, a, smap, ahead);
 }
 
 template <int A>
-cudaError_t launch_pair(const StepArgs& a, uint8_t* ws, cudaStream_t stream) {
-  const VerifyWs wl = verify_ws_layout(a.B, a.T, a.Hk, a.Hv, A);
-  void* act_rows = a.postconv ? a.postconv : static_cast<void*>(ws + wl.act);
+cudaError_t launch_verify_impl(const StepArgs& a, cudaStream_t stream) {
   CUtensorMap smap;
   cudaError_t e = state_map(a, &smap);
   if (e != cudaSuccess) return e;
-  verify_prep_kernel<A><<<dim3(a.Hk, a.B), PT, 0, stream>>>(a, ws, wl, act_rows);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   if constexpr (A == BF16) {
-    return a.T >= 2 ? launch_state<A, true, 0>(a, smap, ws, wl, act_rows, stream)
-                    : launch_state<A, false, 1>(a, smap, ws, wl, act_rows, stream);
+    return a.T >= 2 ? launch_kernel<A, true, 0>(a, smap, stream)
+                    : launch_kernel<A, false, 1>(a, smap, stream);
   } else {
     switch (a.T) {
-      case 1: return launch_state<A, false, 1>(a, smap, ws, wl, act_rows, stream);
-      case 2: return launch_state<A, false, 2>(a, smap, ws, wl, act_rows, stream);
-      case 3: return launch_state<A, false, 3>(a, smap, ws, wl, act_rows, stream);
-      case 4: return launch_state<A, false, 4>(a, smap, ws, wl, act_rows, stream);
-      case 5: return launch_state<A, false, 5>(a, smap, ws, wl, act_rows, stream);
-      case 6: return launch_state<A, false, 6>(a, smap, ws, wl, act_rows, stream);
-      case 7: return launch_state<A, false, 7>(a, smap, ws, wl, act_rows, stream);
-      default: return launch_state<A, false, 8>(a, smap, ws, wl, act_rows, stream);
+      case 1: return launch_kernel<A, false, 1>(a, smap, stream);
+      case 2: return launch_kernel<A, false, 2>(a, smap, stream);
+      case 3: return launch_kernel<A, false, 3>(a, smap, stream);
+      case 4: return launch_kernel<A, false, 4>(a, smap, stream);
+      case 5: return launch_kernel<A, false, 5>(a, smap, stream);
+      case 6: return launch_kernel<A, false, 6>(a, smap, stream);
+      case 7: return launch_kernel<A, false, 7>(a, smap, stream);
+      default: return launch_kernel<A, false, 8>(a, smap, stream);
     }
   }
 }
@@ -665,9 +720,8 @@ cudaError_t launch_pair(const StepArgs& a, uint8_t* ws, cudaStream_t stream) {
 
 // bf16 activations with two or more draft tokens take the tensor-core product;
 // T = 1 and f32 activations the CUDA-core rows.
-cudaError_t launch_verify_readonly(const StepArgs& a, int act, void* ws, cudaStream_t stream) {
-  return act == GDN_BF16 ? launch_pair<BF16>(a, static_cast<uint8_t*>(ws), stream)
-                         : launch_pair<F32>(a, static_cast<uint8_t*>(ws), stream);
+cudaError_t launch_verify_readonly(const StepArgs& a, int act, cudaStream_t stream) {
+  return act == GDN_BF16 ? launch_verify_impl<BF16>(a, stream) : launch_verify_impl<F32>(a, stream);
 }
 
 }  // namespace gdn

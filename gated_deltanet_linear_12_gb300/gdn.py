@@ -21,7 +21,6 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_VERIFY_COMMIT_ALL = 1
 GDN_DEVERR_SLOT, GDN_DEVERR_NKEEP, GDN_DEVERR_SEQLENS, GDN_DEVERR_TIMEOUT = 1, 2, 4, 8
 HEAD_DIM, CONV_WIDTH, CHUNK, MAX_DRAFT = 128, 4, 64, 8
-VERIFY_NOALLOC_MAX_BYTES = 8 << 20
 
 EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_workspace_bytes",
            "gdn_verify_step", "gdn_verify_step_noalloc",
@@ -169,23 +168,26 @@ def gdn_verify_workspace_bytes(cfg, B, T):
 
 
 def verify_workspace(cfg, B, T, device):
-    """A device buffer for gdn_verify_step's workspace argument."""
-    return torch.empty(gdn_verify_workspace_bytes(cfg, B, T), dtype=torch.uint8, device=device)
+    """A device buffer for gdn_verify_step's workspace argument, or None when the
+    configuration needs none (the current kernel needs none)."""
+    n = gdn_verify_workspace_bytes(cfg, B, T)
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n > 0 else None
 
 
 def gdn_verify_step(cfg, x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, *,
                     commit_all=False, postconv_out=None, workspace=None, stream=None):
     """x [B][T][C]; alpha, beta [B][T][Hv]; z, out [B][T][Hv*128]. workspace: a
-    uint8 CUDA tensor (verify_workspace); taken from the caching allocator when
-    omitted."""
+    uint8 CUDA tensor from verify_workspace, or None (sized by the library when
+    omitted; the current kernel needs none)."""
     _dense(x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, postconv_out)
     B, T = x.shape[0], x.shape[1]
     ws, ws_bytes = None, 0
     if not commit_all:
         if workspace is None:
             workspace = verify_workspace(cfg, B, T, x.device)
-        _dense(workspace)
-        ws, ws_bytes = workspace, workspace.numel() * workspace.element_size()
+        if workspace is not None:
+            _dense(workspace)
+            ws, ws_bytes = workspace, workspace.numel() * workspace.element_size()
     _check("gdn_verify_step", load().gdn_verify_step(
         ctypes.byref(cfg), _ptr(x), _ptr(conv_w), _ptr(conv_state), _ptr(state), _ptr(alpha),
         _ptr(beta), _ptr(z), _ptr(norm_w), _ptr(out), _ptr(slot_idx), B, T,

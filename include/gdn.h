@@ -155,10 +155,10 @@ gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const float
 
 /*
  * gdn_verify_workspace_bytes — bytes of device workspace gdn_verify_step needs
- * without GDN_VERIFY_COMMIT_ALL for B sequences of T draft tokens (post-conv
- * rows, the tensor-core operand tiles and the gate tables of every head).
- * Returns -1 for an invalid configuration. The pages have no counterpart: the
- * read-only verify is split in two kernels that pass these through memory.
+ * for B sequences of T draft tokens: 0 for every valid configuration (the
+ * verify kernel keeps its intermediate results on chip), -1 for an invalid one.
+ * Kept so that callers size the workspace argument from the library. The pages
+ * have no counterpart: it is a property of this implementation.
  */
 int64_t gdn_verify_workspace_bytes(const gdn_config* cfg, int32_t B, int32_t T);
 
@@ -175,12 +175,10 @@ int64_t gdn_verify_workspace_bytes(const gdn_config* cfg, int32_t B, int32_t T);
  *           bitwise equal to this call without the flag followed by
  *           gdn_commit_layers with n_keep = T.
  *   postconv_out  nullable [B][T][C] act: the post-conv activations used
- *   workspace     without GDN_VERIFY_COMMIT_ALL: caller-owned device memory of
- *                 at least gdn_verify_workspace_bytes(cfg, B, T) bytes, 256-byte
- *                 aligned, overlapping no argument; its contents on entry do not
- *                 matter and on return are unspecified. Two calls in flight at
- *                 once must not share it. With GDN_VERIFY_COMMIT_ALL it is unused
- *                 (may be NULL, workspace_bytes 0).
+ *   workspace, workspace_bytes  gdn_verify_workspace_bytes(cfg, B, T) bytes of
+ *                 caller-owned device memory; that is 0, so both may be NULL / 0
+ *                 (a non-NULL pointer is not accessed). GDN_ERR_INVALID for
+ *                 workspace_bytes < 0, or NULL with workspace_bytes != 0.
  *   T in 1..GDN_MAX_DRAFT.
  */
 gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* conv_w,
@@ -199,23 +197,13 @@ gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* con
  * can synchronise the device. The pages have no counterpart; it exists only for
  * such callers.
  *
- * The workspace is a buffer of GDN_VERIFY_NOALLOC_MAX_BYTES that the library
- * keeps in the device memory of every GPU that loads it, until the process
- * exits. Arguments are those of gdn_verify_step, minus flags, workspace and
- * workspace_bytes; conv_state and state are only read.
- *   - Returns GDN_ERR_UNSUPPORTED, with nothing enqueued, when
- *     gdn_verify_workspace_bytes(cfg, B, T) exceeds GDN_VERIFY_NOALLOC_MAX_BYTES
- *     (8 MiB: for example B = 32 sequences of T = 8 tokens with Hk = 16,
- *     Hv = 32 heads in bf16 need 6.6 MiB); use gdn_verify_step then.
- *   - The first call made with a device current looks up the buffer's address
- *     on that device; make that first call before any stream capture.
- *   - All calls share the one buffer per device, which keeps whatever the last
- *     call left in it (nothing in it has to start at zero). Calls that overlap
- *     on the GPU (on different streams, or from different host threads) race on
- *     it and give wrong results: order them.
- *   - Allocates nothing and frees nothing.
+ * Arguments are those of gdn_verify_step, minus flags, workspace and
+ * workspace_bytes; conv_state and state are only read; errors as for
+ * gdn_verify_step. It allocates nothing and frees nothing, and uses no memory
+ * of its own: the verify kernel needs no workspace, so this is gdn_verify_step
+ * with that guarantee stated. Calls may overlap on the GPU (they share nothing
+ * but their arguments).
  */
-#define GDN_VERIFY_NOALLOC_MAX_BYTES (8u << 20)
 gdn_status gdn_verify_step_noalloc(const gdn_config* cfg, const void* x, const void* conv_w,
                                    const void* conv_state, const float* state, const float* alpha,
                                    const float* beta, const void* z, const float* norm_w, void* out,

@@ -97,17 +97,16 @@ def test_verify_and_commit_host_validation(lib):
     c = _cfg()
     v = [P[i] for i in range(10)]
     ws = P[10]
-    need = lib.gdn_verify_workspace_bytes(ctypes.byref(c), 4, 2)
-    assert 0 < need < 0x10000000
+    assert lib.gdn_verify_workspace_bytes(ctypes.byref(c), 4, 2) == 0       # the kernel needs none
     assert lib.gdn_verify_workspace_bytes(ctypes.byref(c), 4, 9) == -1
-    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 9, 0, None, ws, need, None) == 1   # T > 8
-    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 0, 0, None, ws, need, None) == 1   # T < 1
-    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 2, 4, None, ws, need, None) == 1   # bad flag
-    assert lib.gdn_verify_step(ctypes.byref(c), *v, 0, 2, 0, None, None, 0, None) == 0    # B = 0
-    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 2, 0, None, None, 0, None) == 1    # no workspace
-    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 2, 0, None, ws, need - 1, None) == 1   # too small
-    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 2, 0, None, ws + 16, need, None) == 1  # misaligned
-    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 2, 0, None, P[0], need, None) == 1     # overlaps x
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 9, 0, None, None, 0, None) == 1   # T > 8
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 0, 0, None, None, 0, None) == 1   # T < 1
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 2, 4, None, None, 0, None) == 1   # bad flag
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 0, 2, 0, None, None, 0, None) == 0   # B = 0
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 2, 0, None, ws, -1, None) == 1    # negative size
+    assert lib.gdn_verify_step(ctypes.byref(c), *v, 4, 2, 0, None, None, 256, None) == 1  # NULL, size != 0
+    assert lib.gdn_verify_step_noalloc(ctypes.byref(c), *v, 4, 9, None, None) == 1       # T > 8
+    assert lib.gdn_verify_step_noalloc(ctypes.byref(c), *v, 0, 2, None, None) == 0       # B = 0
     assert lib.gdn_commit_layers(ctypes.byref(c), P[0], 36, P[1], P[2], 4, 0, None) == 1
     assert lib.gdn_commit_layers(ctypes.byref(c), 0, 36, P[1], P[2], 4, 2, None) == 1
     assert lib.gdn_commit_layers(ctypes.byref(c), P[0], 0, P[1], P[2], 4, 2, None) == 0
