@@ -12,32 +12,25 @@
 // system and o_t = g_t S0 q_t + sum_{s<=t} r(t,s) (k_s.q_t) d_s.
 //
 // Design (GB300). The step is a stream of 64 KiB f32 states, one per
-// (sequence, v head), each read once; everything else is small. Two kernels:
-//   verify_prep_kernel (one block of 128 threads per sequence and q/k head
-//     group; all blocks fit on the GPU at once) does the state-independent
-//     part: conv + SiLU + L2 norm of the group's q, k and v heads, the k.k and
-//     q.k dot products and the gate tables of each v head. It writes the
-//     post-conv rows, the tables and, for bf16 activations, the
-//     [k_0..k_7 ; q_0..q_7] operand tile of the tensor-core product, all to a
-//     caller-provided workspace.
-//   verify_state_kernel (one block of 128 threads per sequence and v head;
-//     thread r owns value row r) starts the four TMA copies of its state (boxes
-//     of 32 columns x 128 rows, 128-byte swizzle) first, then waits for the prep
-//     grid (programmatic dependent launch: the copies overlap the prep kernel)
-//     and bulk-copies its small inputs behind them, all counted on one
-//     mbarrier. Its critical path is one memory latency plus the arithmetic,
-//     and three blocks fit on an SM. In the swizzled boxes row r of each box is
-//     one 128-byte line whose 16-byte chunk c sits at c ^ (r mod 8), which
-//     serves both arithmetic paths without a bank conflict:
-//       - T = 1 (and f32 activations): thread r reads its row's chunks for the
-//         dot products on the CUDA cores;
-//       - T >= 2 with bf16 activations: thread r rewrites its own four lines in
-//         place as bf16 hi | lo parts in the 128-byte-swizzled K-major operand
-//         layout, and one tcgen05 product S0 [k_0..k_7 ; q_0..q_7]^T (M = 128,
-//         N = 16, K = 128, two passes) gives all 2T dot products in TMEM.
-// The dot products, the triangular solve and the epilogue are evaluated in the
-// same order as the step kernel's, so at T = 1 the outputs are bitwise equal to
-// those of the decode mode.
+// (sequence, v head), each read once; everything else is small. One kernel per
+// layer, one block of 128 threads per (sequence, v head), three blocks per SM
+// (76.5 KB of shared memory each); thread r owns value row r. The state comes
+// in four TMA boxes of 32 columns x 128 rows with the 128-byte swizzle: row r of
+// a box is one 128-byte line whose 16-byte chunk c sits at c ^ (r mod 8), which
+// is both a bank-conflict-free row for thread r and the canonical K-major
+// operand layout of the tensor core. The block computes its q, k and v conv rows
+// itself (the two v heads of a q/k head each redo the q, k part: sharing it
+// through memory was measured slower), and
+//   - T = 1 (and f32 activations): the 2T dot products of every row on the CUDA
+//     cores, in the step kernel's order, so that at T = 1 the outputs are
+//     bitwise equal to those of the decode mode;
+//   - T >= 2 with bf16 activations: one tcgen05 kind::tf32 product
+//     S0 [k_0..k_7 ; q_0..q_7]^T straight from the boxes (the state is read as
+//     tf32: 10 explicit mantissa bits) and a Gram product of the q, k tile for
+//     the k.k and q.k dot products.
+// Launched as a programmatic dependent launch: a block that becomes resident
+// while the previous grid drains sets up and asks L2 for its state before it
+// waits, and every block asks L2 for the rows of the block one wave later.
 #include <cuda.h>
 
 #include <mutex>
