@@ -337,18 +337,31 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
     tc::fence_async_smem();
     __syncthreads();
 
-    // ---- (b) MMA1 (S0 hi, lo) and MMA2, while the decay tables are built
+    // ---- (b) MMA1 (S0 hi, lo) and MMA2, while warp 4 builds the decay tables
+    //          (prefix sums of log2 alpha by a warp scan: lane l holds tokens 2l,
+    //          2l + 1)
     if (tid == 0) {
       tc::fence_after_sync();
       mma_pass(tbase + TM_P, a_SHI, 128, a_KQ, 128, 8, id128, false);
       mma_pass(tbase + TM_P, a_SLO, 128, a_KQ, 128, 8, id128, true);
       mma_pass(tbase + TM_G, a_KQ, 128, a_KQ, 128, 8, id64, false);
     }
-    if (tid < C64) {                                     // prefix sums in a fixed order
-      float acc = 0.f;
-      for (int u = 0; u <= tid; ++u) acc += la_s[u];
-      g2_s[tid] = acc;
-      G_s[tid] = ex2(acc);
+    if (warp == 4) {
+      const int l = tid & 31;
+      const float x0 = la_s[2 * l], x1 = la_s[2 * l + 1];
+      float v = x0 + x1;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float n = __shfl_up_sync(FULL, v, off);
+        if (l >= off) v += n;
+      }
+      float before = __shfl_up_sync(FULL, v, 1);        // sum of the tokens before 2l
+      if (l == 0) before = 0.f;
+      const float e0 = before + x0, e1 = e0 + x1;       // inclusive sums at 2l, 2l + 1
+      g2_s[2 * l] = e0;
+      g2_s[2 * l + 1] = e1;
+      G_s[2 * l] = ex2(e0);
+      G_s[2 * l + 1] = ex2(e1);
     }
     __syncthreads();
     if (tid < C64) c_s[tid] = ex2(g2_s[C64 - 1] - g2_s[tid]);
@@ -360,11 +373,11 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
       float gr[64];
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) tc::tmem_ld16(lane_addr + TM_G + 16 * cb, gr + 16 * cb);
-      if (i < C64) {                                     // A row i (f32, strictly lower), stored
-        const float gi = g2_s[i], bi = b_s[i];           // as column i of A^T
+      if (i < C64) {                                     // -A row i (f32, strictly lower), stored
+        const float gi = g2_s[i], bi = b_s[i];           // as column i of -A^T
 #pragma unroll
         for (int u = 0; u < C64; ++u)
-          AB[u * AP + i] = u < i ? __fmul_rn(__fmul_rn(bi, ex2(gi - g2_s[u])), gr[u]) : 0.f;
+          AB[u * AP + i] = u < i ? -__fmul_rn(__fmul_rn(bi, ex2(gi - g2_s[u])), gr[u]) : 0.f;
       } else {                                           // X row t: the MMA5 B tile
         const int t = i - C64;
         const float gt = g2_s[t];
@@ -390,24 +403,45 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
     }
     __syncthreads();                                     // A complete
 
-    // ---- (d) helpers: (I + A) d = R for value row i by right-looking forward
-    //          substitution: once d_u is final, d_t -= A[t][u] d_u for all t > u
-    //          (column u of A read as float4s from A^T; A[t][u] = 0 for t <= u);
-    //          owners: the previous chunk's z-gated RMSNorm
+    // ---- (d) helpers: (I + A) d = R for value row i, in blocks of 16 tokens:
+    //          block k first takes the updates d_t += (-A[t][s]) d_s of every
+    //          finished token s < 16k in ascending s (a rolled loop reading d_s
+    //          back from shared memory), then solves its diagonal block by
+    //          right-looking substitution. Every d_t gets the same fused
+    //          multiply-adds in the same order (ascending s) as a plain forward
+    //          substitution; the rolled loop keeps the code small enough for the
+    //          instruction cache. Column s of -A is read as float4s from -A^T.
+    //          Owners: the previous chunk's z-gated RMSNorm
     if (owner) {
       if (prev_c0 >= 0) epilogue(prev_c0, prev_m);
     } else {
+      float* DS = reinterpret_cast<float*>(KQ);          // d values [token][value row]; KQ is free
 #pragma unroll
-      for (int u = 0; u < C64 - 1; ++u) {
-        const float4* acol = reinterpret_cast<const float4*>(AB + u * AP);
-        const float du = r[u];
+      for (int k = 0; k < 4; ++k) {
+#pragma unroll 4
+        for (int sv = 0; sv < 16 * k; ++sv) {
+          const float ds = DS[sv * D + i];
+          const float2 d2 = make_float2(ds, ds);
+          const float4* acol = reinterpret_cast<const float4*>(AB + sv * AP) + 4 * k;
 #pragma unroll
-        for (int t4 = (u + 1) / 4; t4 < C64 / 4; ++t4) {
-          const float4 a = acol[t4];
-          if (4 * t4 > u) r[4 * t4] = __fmaf_rn(-a.x, du, r[4 * t4]);
-          if (4 * t4 + 1 > u) r[4 * t4 + 1] = __fmaf_rn(-a.y, du, r[4 * t4 + 1]);
-          if (4 * t4 + 2 > u) r[4 * t4 + 2] = __fmaf_rn(-a.z, du, r[4 * t4 + 2]);
-          if (4 * t4 + 3 > u) r[4 * t4 + 3] = __fmaf_rn(-a.w, du, r[4 * t4 + 3]);
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 a = acol[j4];
+            const int t = 16 * k + 4 * j4;
+            const float2 lo = __ffma2_rn(make_float2(a.x, a.y), d2, make_float2(r[t], r[t + 1]));
+            const float2 hi = __ffma2_rn(make_float2(a.z, a.w), d2, make_float2(r[t + 2], r[t + 3]));
+            r[t] = lo.x; r[t + 1] = lo.y; r[t + 2] = hi.x; r[t + 3] = hi.y;
+          }
+        }
+#pragma unroll
+        for (int u = 16 * k; u < 16 * k + 15; ++u) {
+          const float du = r[u];
+          const float* acol = AB + u * AP;
+#pragma unroll
+          for (int t = u + 1; t < 16 * k + 16; ++t) r[t] = __fmaf_rn(acol[t], du, r[t]);
+        }
+        if (k < 3) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) DS[(16 * k + j) * D + i] = r[16 * k + j];
         }
       }
     }
