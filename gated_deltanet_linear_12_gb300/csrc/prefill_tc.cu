@@ -372,7 +372,8 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
     if (owner) {
       float gr[64];
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::tmem_ld16(lane_addr + TM_G + 16 * cb, gr + 16 * cb);
+      tc::tmem_ld16x4(lane_addr + TM_G, gr, lane_addr + TM_G + 16, gr + 16, lane_addr + TM_G + 32, gr + 32,
+                      lane_addr + TM_G + 48, gr + 48);
       if (i < C64) {                                     // -A row i (f32, strictly lower), stored
         const float gi = g2_s[i], bi = b_s[i];           // as column i of -A^T
 #pragma unroll
@@ -389,15 +390,15 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
     } else {
       const uint16_t* vcol = reinterpret_cast<const uint16_t*>(TI) + i;   // staged values
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        float pk[16];
-        tc::tmem_ld16(lane_addr + TM_P + 16 * cb, pk);
+      for (int cb = 0; cb < 4; cb += 2) {
+        float pk[2][16];
+        tc::tmem_ld16x2(lane_addr + TM_P + 16 * cb, pk[0], lane_addr + TM_P + 16 * cb + 16, pk[1]);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 32; ++u) {
           const int t = 16 * cb + u;
           const float vt = t < m ? bf2f(vcol[t * D]) : 0.f;   // rows past m: other tokens
           const float bt = b_s[t];
-          r[t] = __fmaf_rn(-__fmul_rn(bt, G_s[t]), pk[u], __fmul_rn(bt, vt));
+          r[t] = __fmaf_rn(-__fmul_rn(bt, G_s[t]), pk[u >> 4][u & 15], __fmul_rn(bt, vt));
         }
       }
     }
@@ -483,8 +484,7 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         float pq[16], ov[16];
-        tc::tmem_ld16(lane_addr + TM_P + 64 + 16 * cb, pq);
-        tc::tmem_ld16(lane_addr + TM_O + 16 * cb, ov);
+        tc::tmem_ld16x2(lane_addr + TM_P + 64 + 16 * cb, pq, lane_addr + TM_O + 16 * cb, ov);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int t = 16 * cb + u;
@@ -496,8 +496,7 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
 #pragma unroll 1
       for (int cb = 0; cb < 8; ++cb) {
         float sv[16], dv[16];
-        tc::tmem_ld16(lane_addr + TM_S + 16 * cb, sv);
-        tc::tmem_ld16(lane_addr + TM_DS + 16 * cb, dv);
+        tc::tmem_ld16x2(lane_addr + TM_S + 16 * cb, sv, lane_addr + TM_DS + 16 * cb, dv);
 #pragma unroll
         for (int u = 0; u < 16; ++u) sv[u] = __fmaf_rn(gl, sv[u], dv[u]);
         tc::tmem_st16(lane_addr + TM_S + 16 * cb, sv);

@@ -137,6 +137,54 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Several tcgen05 loads in flight before one wait: tmem_ld16_issue starts a
+// load into raw registers, tmem_ld_wait waits for all of this thread's loads,
+// and take16 passes the registers through an empty asm that follows the wait,
+// so that no use of a loaded value is scheduled before the wait.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t r[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void take16(uint32_t r[16], float v[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Two / four 16-column loads with one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t a0, float v0[16], uint32_t a1, float v1[16]) {
+  uint32_t r0[16], r1[16];
+  tmem_ld16_issue(a0, r0);
+  tmem_ld16_issue(a1, r1);
+  tmem_ld_wait();
+  take16(r0, v0);
+  take16(r1, v1);
+}
+__device__ __forceinline__ void tmem_ld16x4(uint32_t a0, float v0[16], uint32_t a1, float v1[16], uint32_t a2,
+                                            float v2[16], uint32_t a3, float v3[16]) {
+  uint32_t r0[16], r1[16], r2[16], r3[16];
+  tmem_ld16_issue(a0, r0);
+  tmem_ld16_issue(a1, r1);
+  tmem_ld16_issue(a2, r2);
+  tmem_ld16_issue(a3, r3);
+  tmem_ld_wait();
+  take16(r0, v0);
+  take16(r1, v1);
+  take16(r2, v2);
+  take16(r3, v3);
+}
+
 // 32 lanes x 16 columns of f32 into TMEM (same lane rule as tmem_ld16).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float v[16]) {
   asm volatile(

@@ -196,10 +196,7 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
 // taddr, taddr + 16, taddr + 32, taddr + 48 (this warp's 32 lanes).
 __device__ __forceinline__ void sum4_ld16(uint32_t taddr, float v[16]) {
   float a[16], b2[16], c[16], d[16];
-  tc::tmem_ld16(taddr, a);
-  tc::tmem_ld16(taddr + 16, b2);
-  tc::tmem_ld16(taddr + 32, c);
-  tc::tmem_ld16(taddr + 48, d);
+  tc::tmem_ld16x4(taddr, a, taddr + 16, b2, taddr + 32, c, taddr + 48, d);
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(__fadd_rn(a[i], b2[i]), __fadd_rn(c[i], d[i]));
 }
