@@ -21,10 +21,10 @@
 // operand layout of the tensor core. The block computes its q, k and v conv rows
 // itself (the two v heads of a q/k head each redo the q, k part: sharing it
 // through memory was measured slower), and
-//   - T = 1 (and f32 activations): the 2T dot products of every row on the CUDA
+//   - T <= 3 (and f32 activations): the 2T dot products of every row on the CUDA
 //     cores, in the step kernel's order, so that at T = 1 the outputs are
 //     bitwise equal to those of the decode mode;
-//   - T >= 2 with bf16 activations: one tcgen05 kind::tf32 product
+//   - T >= 4 with bf16 activations: one tcgen05 kind::tf32 product
 //     S0 [k_0..k_7 ; q_0..q_7]^T straight from the boxes (the state is read as
 //     tf32: 10 explicit mantissa bits) and a Gram product of the q, k tile for
 //     the k.k and q.k dot products.
@@ -257,10 +257,10 @@ template <int A> __host__ __device__ constexpr int blocks_per_sm() { return A ==
 //   - the 2T products S0 k_t, S0 q_t of every value row;
 //   - deltas, outputs and the z-gated RMSNorm of every draft token.
 // Two variants of the products:
-//   - CUDA cores (T = 1, and f32 activations): thread r reads its swizzled f32
+//   - CUDA cores (T <= 3, and f32 activations): thread r reads its swizzled f32
 //     row with the step kernel's rounding; the dot products are warp dot
 //     products with the step kernel's rounding;
-//   - tensor core (TC: bf16 activations, T >= 2): one tcgen05 kind::tf32 product
+//   - tensor core (TC: bf16 activations, T >= 4): one tcgen05 kind::tf32 product
 //     S0 [k_0..k_7 ; q_0..q_7]^T (M = 128, N = 16, K = 128) straight from the TMA
 //     boxes, and the Gram product [k ; q] [k ; q]^T of the same operand tile (its
 //     rows 16..127 are whatever follows the tile and land in unused TMEM lanes)
@@ -690,8 +690,12 @@ cudaError_t launch_verify_impl(const StepArgs& a, cudaStream_t stream) {
   cudaError_t e = state_map(a, &smap);
   if (e != cudaSuccess) return e;
   if constexpr (A == BF16) {
-    return a.T >= 2 ? launch_kernel<A, true, 0>(a, smap, stream)
-                    : launch_kernel<A, false, 1>(a, smap, stream);
+    switch (a.T) {
+      case 1: return launch_kernel<A, false, 1>(a, smap, stream);
+      case 2: return launch_kernel<A, false, 2>(a, smap, stream);
+      case 3: return launch_kernel<A, false, 3>(a, smap, stream);
+      default: return launch_kernel<A, true, 0>(a, smap, stream);
+    }
   } else {
     switch (a.T) {
       case 1: return launch_kernel<A, false, 1>(a, smap, stream);
