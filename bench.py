@@ -9,7 +9,8 @@ delta rule + z-gated RMSNorm), through the C ABI.
 
 metric: GDN tokens/s per layer (whole job: tokens of all ranks / max time).
 Other workloads (--workload): tiny-f32, long-prefill-bf16, spec-verify-bf16
-(36 verify launches + 1 batched commit per window), decode-bf16 (36 layers,
+(36 verify launches + 1 batched commit per window), spec-verify-bf16-h48 (the same
+window for one sequence with Hk = 16, Hv = 48), decode-bf16 (36 layers,
 T = 1, every token accepted).
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference];
@@ -258,9 +259,10 @@ class StepWorkload:
         self.name, self.torch, self.G, self.dev = name, torch, G, device
         decode = name == "decode-bf16"
         self.decode = decode
-        self.B = 256 if decode else 32
+        h48 = name == "spec-verify-bf16-h48"
+        self.B = 256 if decode else 1 if h48 else 32
         self.T = 1 if decode else (T or 8)
-        self.Hk, self.Hv = 16, 32
+        self.Hk, self.Hv = 16, 48 if h48 else 32
         self.C = (2 * self.Hk + self.Hv) * D
         B, T, Hv, C, L = self.B, self.T, self.Hv, self.C, self.LAYERS
         g = torch.Generator(device=device)
@@ -303,18 +305,42 @@ class StepWorkload:
     def reset(self):
         pass                                                # state evolution does not change work
 
-    def step(self, ev=None):
+    def verify_layers(self):
         G = self.G
-        if ev:
-            ev[0].record()
         for lay in self.layers:
             G.gdn_verify_step(self.cfg, lay["x"], lay["conv_w"], lay["conv_state"], lay["state"],
                               lay["alpha"], lay["beta"], lay["z"], self.norm_w, self.out, self.slot,
                               commit_all=self.decode, workspace=self.ws)
+
+    def commit(self):
+        if not self.decode:
+            self.G.gdn_commit_layers(self.cfg, self.views, self.LAYERS, self.slot, self.n_keep, self.T)
+
+    def capture(self):
+        """The window's launches as two CUDA graphs (the 36 verify calls, the
+        commit), as a serving loop replays them: the per-call host cost of the
+        C ABI (about 15 us through the Python binding) then stays off the GPU's
+        timeline. Captured through the same public calls."""
+        torch = self.torch
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        self.g_verify, self.g_commit = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(self.g_verify, stream=s):
+                self.verify_layers()
+            with torch.cuda.graph(self.g_commit, stream=s):
+                self.commit()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+
+    def step(self, ev=None):
+        graphs = hasattr(self, "g_verify")
+        if ev:
+            ev[0].record()
+        self.g_verify.replay() if graphs else self.verify_layers()
         if ev:
             ev[1].record()
-        if not self.decode:
-            G.gdn_commit_layers(self.cfg, self.views, self.LAYERS, self.slot, self.n_keep, self.T)
+        self.g_commit.replay() if graphs else self.commit()
         if ev:
             ev[2].record()
 
@@ -326,9 +352,11 @@ class StepWorkload:
         self.d2h = self.h_out.numel() * self.h_out.element_size()
 
     def step_e2e(self):
+        """Direct calls through the public API (no graph), host copies included."""
         for h, l in zip(self.h_x, self.layers):
             l["x"].copy_(h, non_blocking=True)
-        self.step()
+        self.verify_layers()
+        self.commit()
         self.h_out.copy_(self.out, non_blocking=True)
 
     def config(self):
@@ -336,6 +364,7 @@ class StepWorkload:
                 "layers": self.LAYERS, "qk_heads": self.Hk, "v_heads": self.Hv, "head_dim": D,
                 "channels": self.C, "state_dtype": "f32", "act_dtype": "bf16",
                 "n_keep": "uniform in [0, T]" if not self.decode else "all",
+                "launch": "CUDA graphs of the window's public calls (value); direct calls (e2e)",
                 "l2": "state pools of all layers exceed L2; flush 256 MiB between timed steps"}
 
 
@@ -404,7 +433,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    if args.workload in ("spec-verify-bf16", "decode-bf16"):
+    if args.workload in ("spec-verify-bf16", "spec-verify-bf16-h48", "decode-bf16"):
         W = StepWorkload(args.workload, torch, G, dev, T=args.T)
     else:
         W = PrefillWorkload(args.workload, torch, G, dev)
@@ -415,6 +444,11 @@ def main():
         W.reset()
         W.step()
     torch.cuda.synchronize()
+    if isinstance(W, StepWorkload):
+        W.capture()
+        for _ in range(2):
+            W.step()
+        torch.cuda.synchronize()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)

@@ -240,7 +240,7 @@ postconv_norm_kernel(const void* __restrict__ yin, void* __restrict__ yout, int6
 template <int A, bool NORM, typename... Args>
 static cudaError_t launch_conv_variant(dim3 grid, cudaStream_t stream, Args... args) {
   const int smem = conv_tile_bytes<A>();
-  cudaError_t e = cudaFuncSetAttribute(conv_fwd_kernel<A, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once<conv_fwd_kernel<A, NORM>>(smem);
   if (e != cudaSuccess) return e;
   conv_fwd_kernel<A, NORM><<<grid, CONV_THREADS, smem, stream>>>(args...);
   return cudaSuccess;

@@ -89,10 +89,8 @@ gdn_status gdn_postconv_norm(const gdn_config* cfg, int32_t in_t, const void* y_
   const size_t ni = (size_t)n_tok * C * esize(in_t), no = (size_t)n_tok * C * esize(out_t);
   const bool same = y_in == y_out && in_t == out_t;
   if (!same && overlap(y_in, ni, y_out, no)) return GDN_ERR_INVALID;
-  int dev = 0, n_sm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return GDN_ERR_CUDA;
+  int n_sm = 0;
+  if (gdn::sm_count(&n_sm) != cudaSuccess) return GDN_ERR_CUDA;
   return from_cuda(gdn::launch_postconv_norm(*cfg, in_t, y_in, out_t, y_out, n_tok, n_sm,
                                              static_cast<cudaStream_t>(stream)));
 }

@@ -6,9 +6,50 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "gdn.h"
 
 namespace gdn {
+
+// Kernel attributes (the dynamic shared memory limit, optionally the largest
+// shared-memory carveout), set once per kernel and device, and again only when a
+// launch needs a larger limit than any before: each call costs host time that a
+// small launch cannot hide.
+template <auto Kern>
+cudaError_t set_smem_once(int smem_bytes, bool max_carveout = false) {
+  static std::atomic<int> limit[64];                     // per device: the limit set so far
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && limit[dev].load(std::memory_order_acquire) >= smem_bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess && max_carveout)
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess && cached) {
+    int cur = limit[dev].load(std::memory_order_relaxed);
+    while (cur < smem_bytes && !limit[dev].compare_exchange_weak(cur, smem_bytes, std::memory_order_acq_rel)) {
+    }
+  }
+  return e;
+}
+
+// Number of SMs of the current device, looked up once per device.
+inline cudaError_t sm_count(int* n) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) { *n = c; return cudaSuccess; }
+  }
+  e = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) cache[dev].store(*n, std::memory_order_relaxed);
+  return e;
+}
 
 struct StepArgs {
   const void* x;            // [B][T][C]

@@ -550,8 +550,7 @@ size_t prefill_tc_smem_bytes() { return SM_TOTAL; }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   const int smem = (int)SM_TOTAL;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once<prefill_tc_kernel>(smem);
   if (e != cudaSuccess) return e;
   CUtensorMap vmap, zmap;
   const uint64_t C = (uint64_t)(2 * a.Hk + a.Hv) * D;

@@ -423,8 +423,7 @@ template <int A, int MODE>
 static cudaError_t launch_mode(const StepArgs& a, dim3 grid, int nh, cudaStream_t stream) {
   const size_t smem = step_smem_bytes(nh);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(step_kernel<A, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = set_smem_once<step_kernel<A, MODE>>((int)smem);
     if (e != cudaSuccess) return e;
   }
   step_kernel<A, MODE><<<grid, STEP_THREADS, smem, stream>>>(a);

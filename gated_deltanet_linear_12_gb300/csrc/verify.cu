@@ -662,14 +662,10 @@ template <int A, bool TC, int NT>
 cudaError_t launch_kernel(const StepArgs& a, const CUtensorMap& smap, cudaStream_t stream) {
   auto kern = verify_kernel<A, TC, NT>;
   const int smem = verify_smem<A, TC>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_smem_once<verify_kernel<A, TC, NT>>(smem, true);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  int dev = 0, n_sm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  int n_sm = 0;
+  if ((e = sm_count(&n_sm)) != cudaSuccess) return e;
   const int ahead = blocks_per_sm<A>() * n_sm;              // blocks resident at once
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((int64_t)a.B * a.Hv));

@@ -22,6 +22,7 @@ Workloads (names used across the repository):
   spec-verify-bf16      batch 32, T = 1..8 draft tokens, 36 layers
   long-prefill-bf16     4 sequences x 16384 tokens
   decode-bf16           batch 256, T = 1, 36 layers
+  spec-verify-bf16-h48  one sequence, T = 1..8, Hk=16, Hv=48 (C=10240), 36 layers
 """
 from __future__ import annotations
 
@@ -38,6 +39,7 @@ WORKLOADS = [
     "spec-verify-bf16",
     "long-prefill-bf16",
     "decode-bf16",
+    "spec-verify-bf16-h48",
 ]
 
 

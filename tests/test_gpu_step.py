@@ -188,6 +188,26 @@ def test_verify_group_of_three_v_heads(G, orc, T):
     check_states(to_np(L.S), st, _used_slots(inp), 1e-4, "state G=3")
 
 
+@pytest.mark.parametrize("T", [1, 3, 5, 8])
+def test_verify_window_geometry_48_v_heads(G, orc, T):
+    """The verify window of "Strata PR #3226" ("Benchmark Evidence"): one sequence,
+    Hk = 16, Hv = 48 (C = 10240), read-only verify then the commit of n tokens."""
+    inp = syn.verify_inputs(1, T, 16, 48, "bf16", seed=440 + T, n_slots=2)
+    L = Layer(inp)
+    L.verify(G)
+    torch.cuda.synchronize()
+    out, pc, _, _ = _oracle_verify(orc, inp)
+    check_bf16(to_np(L.out), out, what=f"verify Hv=48 T={T}")
+    assert np.array_equal(bits(L.pc), _act_bits(pc, "bf16")), "post-conv bitwise"
+    assert np.array_equal(bits(L.S), inp["state"].view(np.int32))
+    L.verify(G, commit_all=True)
+    torch.cuda.synchronize()
+    out2, _, cs, st = _oracle_verify(orc, inp, commit_all=True)
+    check_bf16(to_np(L.out), out2, what=f"decode Hv=48 T={T}")
+    assert np.array_equal(to_np(L.cs), cs)
+    check_states(to_np(L.S), st, _used_slots(inp), 1e-4, f"state Hv=48 T={T}")
+
+
 def test_verify_postconv_matches_conv_fwd_bitwise(G):
     """The activations verify uses equal gdn_conv_fwd's on the same rows."""
     T = 6
