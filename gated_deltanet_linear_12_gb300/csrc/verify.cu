@@ -201,11 +201,6 @@ __device__ __forceinline__ void sum4_ld16(uint32_t taddr, float v[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(__fadd_rn(a[i], b2[i]), __fadd_rn(c[i], d[i]));
 }
 
-// A hint: start bringing `bytes` (a multiple of 16, 16-byte aligned) into L2.
-__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // L2 hints for unit u = b Hv + h (sequence b, v head h); the slot index read
 // here may still change: nothing but these hints depends on it.
 // hint_state: box `box` (0..3) of its state.
@@ -229,11 +224,11 @@ __device__ __forceinline__ void hint_rows(const StepArgs& p, int u, int T, int w
     const int row = w / 3, hd = w % 3;
     const int64_t c = hd == 0 ? (int64_t)hq * D : hd == 1 ? (int64_t)(Hk + hq) * D : (int64_t)(2 * Hk + h) * D;
     const int64_t e = row < KS ? ((int64_t)slot * KS + row) * C + c : ((int64_t)b * T + row - KS) * C + c;
-    l2_prefetch((row < KS ? static_cast<const char*>(p.conv_state) : static_cast<const char*>(p.x)) + e * esz,
+    tc::prefetch_l2((row < KS ? static_cast<const char*>(p.conv_state) : static_cast<const char*>(p.x)) + e * esz,
                 D * esz);
   } else {
     const int t = w - n_x;
-    l2_prefetch(static_cast<const char*>(p.z) + (((int64_t)b * T + t) * Hv + h) * D * esz, D * esz);
+    tc::prefetch_l2(static_cast<const char*>(p.z) + (((int64_t)b * T + t) * Hv + h) * D * esz, D * esz);
   }
 }
 
