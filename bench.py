@@ -66,6 +66,22 @@ def state_bytes_per_layer(Hv, C, dv=D, dk=D, conv_rows=3, state_es=4, conv_es=4)
     return Hv * dv * dk * state_es + C * conv_rows * conv_es
 
 
+def max_over_ranks(value, device, world):
+    """The largest value over the ranks (every rank gets it): with independent
+    replicas the job is done when the slowest one is."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms_max):
+    """Units processed by all ranks per second, from the slowest rank's time."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 def fp32_alu_peak_tflops(sm_mhz, n_sm=152, lanes=128):
     """FP32 FMA peak: SMs x FP32 lanes per SM x 2 FLOP x clock."""
     return n_sm * lanes * 2 * sm_mhz * 1e6 / 1e12
@@ -467,10 +483,7 @@ def main():
     pf_ms = [evs[k][1].elapsed_time(evs[k][2]) for k in range(args.steps)]
     step_ms = [c + p for c, p in zip(conv_ms, pf_ms)]
     ms = statistics.mean(step_ms)
-    ms_t = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, dev, world)
 
     # end-to-end through the public API with host buffers
     W.setup_e2e()
@@ -489,14 +502,11 @@ def main():
         e1.record()
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_t = torch.tensor([statistics.mean(e2e_ms)], device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_max = max_over_ranks(statistics.mean(e2e_ms), dev, world)
 
     if rank == 0:
         peaks, peak_src = load_peaks()
         a_avg, b_avg = statistics.mean(conv_ms), statistics.mean(pf_ms)
-        tokens_total = W.tokens * world
         if isinstance(W, StepWorkload):
             vk = "step_kernel" if W.decode else "verify_kernel"
             names = (f"{vk} ({'decode' if W.decode else 'verify'})", "step_kernel (commit)")
@@ -513,7 +523,7 @@ def main():
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ka["frac_hbm"],
                     "traffic": ncu_traffic(vk, W.name + f"/T{W.T}"),
                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
-            value = tokens_total * W.LAYERS / (ms_max * 1e-3)
+            value = whole_job_rate(W.tokens * W.LAYERS, world, ms_max)
         else:
             alu_peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
             pf_tflops = W.flops["prefill"] / (b_avg * 1e-3) / 1e12
@@ -551,8 +561,8 @@ def main():
                 pf_name: {"ms": round(b_avg, 4), "bytes": W.bytes["prefill"],
                           "GB/s": round(pf_gbs, 1), "TFLOP/s": round(pf_tflops, 3)},
             }
-            value = tokens_total / (ms_max * 1e-3)
-        e2e_val = value * ms_max / float(e2e_t.item())
+            value = whole_job_rate(W.tokens, world, ms_max)
+        e2e_val = value * ms_max / e2e_max
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
