@@ -21,10 +21,10 @@
 // operand layout of the tensor core. The block computes its q, k and v conv rows
 // itself (the two v heads of a q/k head each redo the q, k part: sharing it
 // through memory was measured slower), and
-//   - T <= 3 (and f32 activations): the 2T dot products of every row on the CUDA
+//   - T <= 4 (and f32 activations): the 2T dot products of every row on the CUDA
 //     cores, in the step kernel's order, so that at T = 1 the outputs are
 //     bitwise equal to those of the decode mode;
-//   - T >= 4 with bf16 activations: one tcgen05 kind::tf32 product
+//   - T >= 5 with bf16 activations: one tcgen05 kind::tf32 product
 //     S0 [k_0..k_7 ; q_0..q_7]^T straight from the boxes (the state is read as
 //     tf32: 10 explicit mantissa bits) and a Gram product of the q, k tile for
 //     the k.k and q.k dot products.
@@ -74,14 +74,12 @@ namespace {
 
 constexpr int VT = 128;                          // state kernel: thread r owns value row r
 constexpr int S_BYTES = D * D * 4;               // one f32 state
-constexpr int BT_BYTES = 2 * 8 * 128 * 2;        // [k_0..7 ; q_0..7] bf16, K-major
 constexpr int TAB = 160;                         // per (sequence, v head):
 constexpr int TAB_A = 0;                         //   [8][8] b_t r(t,s) (k_t.k_s), s < t
 constexpr int TAB_OC = 64;                       //   [8][8] r(t,s) (q_t.k_s), s <= t
 constexpr int TAB_G = 128;                       //   [8] g_t
 constexpr int TAB_BG = 136;                      //   [8] b_t g_t
 constexpr int TAB_B = 144;                       //   [8] b_t
-constexpr int QK_STRIDE = D + 4;                 // prep: padded f32 rows of q and k
 
 // Byte offset of 16-byte chunk c (0..7) of line `line` (0..3) of row r: the
 // state's box `line` holds columns 32 line .. 32 line + 31 (chunk c = columns
@@ -109,29 +107,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return tc::smem_desc(addr, 16, 1024) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ float4 unpack4(uint2 u) {
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
-
 // ============================================================ the verify kernel
 // Shared memory (no static shared variables, so the dynamic region starts at a
 // 1024-byte boundary):
-//   QK  q and k of every draft token; after the products the outputs o_t
-//       (f32 [T][128]):
-//         tensor-core variant: f32 [k_0..k_7 ; q_0..q_7], K-major, 128-byte
-//                              swizzle (the tf32 operand)
-//         CUDA-core, bf16:     bf16 [k_0..k_7 ; q_0..q_7], K-major
-//         CUDA-core, f32:      padded f32 rows [k | q][8][QK_STRIDE]
+//   QK  q and k of every draft token, f32 [k_0..k_7 ; q_0..q_7], K-major with the
+//       128-byte swizzle (the tf32 operand of the tensor-core variant; float4
+//       reads without conversion for the CUDA-core ones); after the products
+//       the outputs o_t (f32 [T][128])
 //   SR  the state, four TMA boxes [32 columns][128 rows] f32, 128-byte swizzle
 //       (1024-byte aligned)
 //   VS  v rows [8][128] (activation dtype)
 //   TB  the table of gate products and dot products (TAB floats)
 //   GS  alpha, beta of this head [2][8]
 //   BR  the state, product and Gram barriers, the TMEM address
-template <int A, bool TC> __host__ __device__ constexpr int qk_bytes() {
-  return TC ? 2 * MAXT * D * 4 : A == BF16 ? BT_BYTES : 2 * MAXT * QK_STRIDE * 4;
-}
+template <int A, bool TC> __host__ __device__ constexpr int qk_bytes() { return 2 * MAXT * D * 4; }
 template <int A, bool TC> __host__ __device__ constexpr int qk_region() { return (qk_bytes<A, TC>() + 1023) & ~1023; }
 template <int A> __host__ __device__ constexpr int rows_bytes() { return MAXT * D * (A == BF16 ? 2 : 4); }
 template <int A, bool TC> __host__ __device__ constexpr int verify_smem() {
@@ -150,28 +139,14 @@ __device__ __forceinline__ uint32_t bsw_off(int row, int k) {
 // Activations k_t (which = 0) or q_t (which = 1), columns 4j..4j+3.
 template <int A, bool TC>
 __device__ __forceinline__ float4 act4(const uint8_t* QK, int which, int t, int j) {
-  if constexpr (TC) {
-    return *reinterpret_cast<const float4*>(QK + bsw_off(8 * which + t, 4 * j));
-  } else if constexpr (A == BF16) {
-    return unpack4(*reinterpret_cast<const uint2*>(QK + tc::kmajor_offset(8 * which + t, 4 * j, 16)));
-  } else {
-    return reinterpret_cast<const float4*>(QK + (which * MAXT + t) * QK_STRIDE * 4)[j];
-  }
+  return *reinterpret_cast<const float4*>(QK + bsw_off(8 * which + t, 4 * j));
 }
 
 // Stores 8 rounded activations (columns c .. c + 7) of k_t (which = 0) or q_t.
 template <int A, bool TC>
 __device__ __forceinline__ void put_act8(uint8_t* QK, int which, int t, int c, const float v[8]) {
-  if constexpr (TC) {
-    *reinterpret_cast<float4*>(QK + bsw_off(8 * which + t, c)) = make_float4(v[0], v[1], v[2], v[3]);
-    *reinterpret_cast<float4*>(QK + bsw_off(8 * which + t, c + 4)) = make_float4(v[4], v[5], v[6], v[7]);
-  } else if constexpr (A == BF16) {
-    store8<A>(QK + tc::kmajor_offset(8 * which + t, c, 16), 0, v);
-  } else {
-    float4* dst = reinterpret_cast<float4*>(QK + ((which * MAXT + t) * QK_STRIDE + c) * 4);
-    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-  }
+  *reinterpret_cast<float4*>(QK + bsw_off(8 * which + t, c)) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(QK + bsw_off(8 * which + t, c + 4)) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
 template <int A> __device__ __forceinline__ float row_at(const uint8_t* R, int t, int i) {
@@ -252,10 +227,10 @@ template <int A> __host__ __device__ constexpr int blocks_per_sm() { return A ==
 //   - the 2T products S0 k_t, S0 q_t of every value row;
 //   - deltas, outputs and the z-gated RMSNorm of every draft token.
 // Two variants of the products:
-//   - CUDA cores (T <= 3, and f32 activations): thread r reads its swizzled f32
+//   - CUDA cores (T <= 4, and f32 activations): thread r reads its swizzled f32
 //     row with the step kernel's rounding; the dot products are warp dot
 //     products with the step kernel's rounding;
-//   - tensor core (TC: bf16 activations, T >= 4): one tcgen05 kind::tf32 product
+//   - tensor core (TC: bf16 activations, T >= 5): one tcgen05 kind::tf32 product
 //     S0 [k_0..k_7 ; q_0..q_7]^T (M = 128, N = 16, K = 128) straight from the TMA
 //     boxes, and the Gram product [k ; q] [k ; q]^T of the same operand tile (its
 //     rows 16..127 are whatever follows the tile and land in unused TMEM lanes)
@@ -685,6 +660,7 @@ cudaError_t launch_verify_impl(const StepArgs& a, cudaStream_t stream) {
       case 1: return launch_kernel<A, false, 1>(a, smap, stream);
       case 2: return launch_kernel<A, false, 2>(a, smap, stream);
       case 3: return launch_kernel<A, false, 3>(a, smap, stream);
+      case 4: return launch_kernel<A, false, 4>(a, smap, stream);
       default: return launch_kernel<A, true, 0>(a, smap, stream);
     }
   } else {
@@ -693,7 +669,6 @@ cudaError_t launch_verify_impl(const StepArgs& a, cudaStream_t stream) {
       case 2: return launch_kernel<A, false, 2>(a, smap, stream);
       case 3: return launch_kernel<A, false, 3>(a, smap, stream);
       case 4: return launch_kernel<A, false, 4>(a, smap, stream);
-      case 5: return launch_kernel<A, false, 5>(a, smap, stream);
       case 6: return launch_kernel<A, false, 6>(a, smap, stream);
       case 7: return launch_kernel<A, false, 7>(a, smap, stream);
       default: return launch_kernel<A, false, 8>(a, smap, stream);
