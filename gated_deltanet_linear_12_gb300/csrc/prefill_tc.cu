@@ -494,18 +494,23 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
     } else {
       const float gl = G_s[C64 - 1];
 #pragma unroll 1
-      for (int cb = 0; cb < 8; ++cb) {
-        float sv[16], dv[16];
-        tc::tmem_ld16x2(lane_addr + TM_S + 16 * cb, sv, lane_addr + TM_DS + 16 * cb, dv);
+      for (int cb0 = 0; cb0 < 8; cb0 += 2) {             // two 16-column blocks per TMEM wait
+        float sv[2][16], dv[2][16];
+        tc::tmem_ld16x4(lane_addr + TM_S + 16 * cb0, sv[0], lane_addr + TM_DS + 16 * cb0, dv[0],
+                        lane_addr + TM_S + 16 * cb0 + 16, sv[1], lane_addr + TM_DS + 16 * cb0 + 16, dv[1]);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) sv[u] = __fmaf_rn(gl, sv[u], dv[u]);
-        tc::tmem_st16(lane_addr + TM_S + 16 * cb, sv);
+        for (int k = 0; k < 2; ++k) {
+          const int cb = cb0 + k;
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          uint4 hi, lo;
-          tc::split8(sv + 8 * hlf, hi, lo);
-          st16(SHI + tc::kmajor_offset(i, 16 * cb + 8 * hlf, 128), hi);
-          st16(SLO + tc::kmajor_offset(i, 16 * cb + 8 * hlf, 128), lo);
+          for (int u = 0; u < 16; ++u) sv[k][u] = __fmaf_rn(gl, sv[k][u], dv[k][u]);
+          tc::tmem_st16(lane_addr + TM_S + 16 * cb, sv[k]);
+#pragma unroll
+          for (int hlf = 0; hlf < 2; ++hlf) {
+            uint4 hi, lo;
+            tc::split8(sv[k] + 8 * hlf, hi, lo);
+            st16(SHI + tc::kmajor_offset(i, 16 * cb + 8 * hlf, 128), hi);
+            st16(SLO + tc::kmajor_offset(i, 16 * cb + 8 * hlf, 128), lo);
+          }
         }
       }
       tc::tmem_st_wait();
