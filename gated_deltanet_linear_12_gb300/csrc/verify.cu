@@ -669,9 +669,11 @@ cudaError_t launch_verify_impl(const StepArgs& a, cudaStream_t stream) {
       case 2: return launch_kernel<A, false, 2>(a, smap, stream);
       case 3: return launch_kernel<A, false, 3>(a, smap, stream);
       case 4: return launch_kernel<A, false, 4>(a, smap, stream);
+      case 5: return launch_kernel<A, false, 5>(a, smap, stream);
       case 6: return launch_kernel<A, false, 6>(a, smap, stream);
       case 7: return launch_kernel<A, false, 7>(a, smap, stream);
-      default: return launch_kernel<A, false, 8>(a, smap, stream);
+      case 8: return launch_kernel<A, false, 8>(a, smap, stream);
+      default: return cudaErrorInvalidValue;               // T is 1..8 (checked by the API)
     }
   }
 }

@@ -28,11 +28,11 @@ def _oracle_qkv(orc, inp):
     return syn.to_act(y, inp["act"])
 
 
-def _run_prefill(G, inp, qkv, dev_err=None):
+def _run_prefill(G, inp, qkv, dev_err=None, q_scale=1.0, eps=1e-6):
     act = torch.bfloat16 if inp["act"] == "bf16" else torch.float32
     S = to_dev(inp["state"])
     out = torch.zeros(inp["n_tok"], inp["Hv"] * 128, dtype=act, device="cuda")
-    cfg = G.make_config(inp["Hk"], inp["Hv"], act, S.shape[0], dev_err=dev_err)
+    cfg = G.make_config(inp["Hk"], inp["Hv"], act, S.shape[0], dev_err=dev_err, q_scale=q_scale, eps=eps)
     G.gdn_delta_prefill(cfg, to_dev(qkv), to_dev(inp["alpha"]), to_dev(inp["beta"]),
                         to_dev(inp["z"]), to_dev(inp["norm_w"]), out, S, to_dev(inp["slot_idx"]),
                         to_dev(inp["cu_seqlens"]), to_dev(inp["has_init_state"]))
@@ -40,10 +40,10 @@ def _run_prefill(G, inp, qkv, dev_err=None):
     return out, S
 
 
-def _oracle_prefill(orc, inp, qkv):
+def _oracle_prefill(orc, inp, qkv, q_scale=1.0, eps=1e-6):
     return orc.prefill(qkv, inp["alpha"], inp["beta"], inp["z"], inp["norm_w"], inp["state"],
                        inp["slot_idx"], inp["cu_seqlens"], inp["has_init_state"], inp["Hk"],
-                       inp["Hv"])
+                       inp["Hv"], q_scale=q_scale, eps=eps)
 
 
 def test_prefill_tiny_f32(G, orc):
@@ -69,6 +69,22 @@ def test_prefill_varlen_bf16(G, orc, lens, init):
     unused = sorted(set(range(inp["state"].shape[0])) - set(int(s) for s in inp["slot_idx"]))
     for sl in unused:
         assert np.array_equal(bits(S)[sl], inp["state"][sl].view(np.int32))
+
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_prefill_q_scale_and_eps(G, orc, act):
+    """q_scale = d^-1/2 (an ABI parameter the definition does not have) with an eps
+    large enough that the output RMSNorm does not divide the scale away."""
+    inp = syn.prefill_inputs([70, 129], 2, 4, act, seed=530, init_mask=np.array([1, 0]))
+    qkv = _oracle_qkv(orc, inp)
+    qs, eps = 128 ** -0.5, 0.05
+    out, S = _run_prefill(G, inp, qkv, q_scale=qs, eps=eps)
+    ro, rs = _oracle_prefill(orc, inp, qkv, q_scale=qs, eps=eps)
+    if act == "bf16":
+        check_bf16(to_np(out), ro, what="prefill q_scale out")
+    else:
+        check_f32_out(to_np(out), ro, 1e-4, "prefill q_scale out")
+    check_states(to_np(S), rs, [int(s) for s in inp["slot_idx"]], 1e-4, "prefill q_scale state")
 
 
 def test_prefill_group_of_three(G, orc):

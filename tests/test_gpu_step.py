@@ -71,7 +71,7 @@ def _used_slots(inp):
     return [int(s) for s in inp["slot_idx"] if s >= 0]
 
 
-@pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("T", range(1, 9))                 # every compiled variant
 def test_verify_bf16(G, orc, T):
     inp = syn.verify_inputs(6, T, 2, 4, "bf16", seed=200 + T, pad_slots=1)
     L = Layer(inp)
@@ -86,14 +86,14 @@ def test_verify_bf16(G, orc, T):
     assert np.all(to_np(L.out)[5] == 0), "padding entry must not be written"
 
 
-@pytest.mark.parametrize("T", [1, 4, 8])
+@pytest.mark.parametrize("T", range(1, 9))                 # every compiled variant
 def test_verify_f32_arm(G, orc, T):
     inp = syn.verify_inputs(3, T, 1, 2, "f32", seed=210 + T)
     L = Layer(inp)
     L.verify(G)
     torch.cuda.synchronize()
     out, pc, _, _ = _oracle_verify(orc, inp)
-    check_f32_out(to_np(L.out), out, 1e-4, "verify f32 out")
+    check_f32_out(to_np(L.out), out, 1e-4, f"verify f32 out T={T}")
 
 
 @pytest.mark.parametrize("T", [1, 3, 8])
@@ -206,6 +206,28 @@ def test_verify_window_geometry_48_v_heads(G, orc, T):
     check_bf16(to_np(L.out), out2, what=f"decode Hv=48 T={T}")
     assert np.array_equal(to_np(L.cs), cs)
     check_states(to_np(L.S), st, _used_slots(inp), 1e-4, f"state Hv=48 T={T}")
+
+
+@pytest.mark.parametrize("T,act", [(3, "bf16"), (8, "bf16"), (5, "f32")])
+def test_verify_q_scale_and_eps(G, orc, T, act):
+    """q_scale = d^-1/2 with an eps large enough that the output RMSNorm does not
+    divide the scale away (eps also enters the q/k norms, on both sides)."""
+    inp = syn.verify_inputs(4, T, 2, 4, act, seed=460 + T)
+    L = Layer(inp)
+    qs, eps = 128 ** -0.5, 0.05
+    cfg = G.make_config(inp["Hk"], inp["Hv"], L.act, L.S.shape[0], q_scale=qs, eps=eps)
+    G.gdn_verify_step(cfg, L.x, L.conv_w, L.cs, L.S, L.alpha, L.beta, L.z, L.norm_w, L.out, L.slot,
+                      postconv_out=L.pc)
+    torch.cuda.synchronize()
+    out, pc, _, _ = orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"], inp["alpha"],
+                               inp["beta"], inp["z"], inp["norm_w"], inp["slot_idx"], inp["Hk"],
+                               inp["Hv"], q_scale=qs, eps=eps, round_act=act == "bf16",
+                               act32=True)
+    if act == "bf16":
+        check_bf16(to_np(L.out), out, what=f"verify q_scale T={T}")
+        assert np.array_equal(bits(L.pc), _act_bits(pc, act)), "post-conv bitwise"
+    else:
+        check_f32_out(to_np(L.out), out, 1e-4, f"verify q_scale f32 T={T}")
 
 
 def test_verify_postconv_matches_conv_fwd_bitwise(G):
