@@ -66,6 +66,36 @@ def state_bytes_per_layer(Hv, C, dv=D, dk=D, conv_rows=3, state_es=4, conv_es=4)
     return Hv * dv * dk * state_es + C * conv_rows * conv_es
 
 
+def prefill_roofline(kernel, flops, nbytes, ms, peaks, peak_src, traffic):
+    """Roofline entry of a prefill launch of `flops` algorithmic FLOPs and
+    `nbytes` algorithmic HBM bytes that took `ms`. The binding roofline is the one
+    with the longer floor: the bytes at the HBM peak, or the FLOPs at the peak of
+    the unit the products run on (tensor cores for bf16, the FP32 pipe for f32).
+    Both fractions are reported."""
+    s = ms * 1e-3
+    gbs, tflops = nbytes / s / 1e9, flops / s / 1e12
+    if kernel == "prefill_tc_kernel":
+        c_bound, c_peak = "tensor", peaks.get("bf16_tflops", 1920.0)
+        c_src = f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)"
+    else:
+        mhz = peaks.get("sm_max_mhz", 2070.0)
+        c_bound, c_peak = "alu", round(fp32_alu_peak_tflops(mhz), 1)
+        c_src = f"derived: 152 SMs x 128 FP32 lanes x 2 FLOP x {mhz:.0f} MHz"
+    floor_hbm_us = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    floor_c_us = flops / (c_peak * 1e12) * 1e6
+    common = {"algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
+              "floor_us": {"hbm": round(floor_hbm_us, 2), c_bound: round(floor_c_us, 2)},
+              "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+              f"{c_bound}_tflops": round(tflops, 3), f"{c_bound}_frac": round(tflops / c_peak, 4)}
+    if floor_hbm_us >= floor_c_us:
+        return {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)", **common}
+    return {"kernel": kernel, "bound": c_bound, "achieved": round(tflops, 3), "peak": c_peak,
+            "unit": "TFLOP/s", "frac": round(tflops / c_peak, 4),
+            "traffic": traffic if c_bound == "tensor" else None, "peak_source": c_src, **common}
+
+
 def max_over_ranks(value, device, world):
     """The largest value over the ranks (every rank gets it): with independent
     replicas the job is done when the slowest one is."""
@@ -525,29 +555,13 @@ def main():
                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
             value = whole_job_rate(W.tokens * W.LAYERS, world, ms_max)
         else:
-            alu_peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
             pf_tflops = W.flops["prefill"] / (b_avg * 1e-3) / 1e12
             pf_gbs = W.bytes["prefill"] / (b_avg * 1e-3) / 1e9
             conv_gbs = W.bytes["conv"] / (a_avg * 1e-3) / 1e9
             pf_name = "prefill_tc_kernel" if W.inp["act"] == "bf16" else "prefill_ffma_kernel"
-            if b_avg >= a_avg and pf_name == "prefill_tc_kernel":
-                peak = peaks.get("bf16_tflops", 1920.0)
-                roof = {"kernel": pf_name, "bound": "tensor", "achieved": round(pf_tflops, 3),
-                        "peak": peak, "unit": "TFLOP/s", "frac": round(pf_tflops / peak, 4),
-                        "traffic": ncu_traffic(pf_name, W.name),
-                        "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)",
-                        "algorithmic_flops_per_launch": W.flops["prefill"],
-                        "algorithmic_bytes_per_launch": W.bytes["prefill"],
-                        "hbm_gbs": round(pf_gbs, 1),
-                        "hbm_frac": round(pf_gbs / peaks["hbm_gbs"], 4)}
-            elif b_avg >= a_avg:
-                roof = {"kernel": pf_name, "bound": "alu",
-                        "achieved": round(pf_tflops, 3), "peak": round(alu_peak, 1),
-                        "unit": "TFLOP/s", "frac": round(pf_tflops / alu_peak, 4), "traffic": None,
-                        "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x "
-                                       f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz",
-                        "algorithmic_flops_per_launch": W.flops["prefill"],
-                        "hbm_gbs": round(pf_gbs, 1)}
+            if b_avg >= a_avg:
+                roof = prefill_roofline(pf_name, W.flops["prefill"], W.bytes["prefill"], b_avg, peaks,
+                                        peak_src, ncu_traffic(pf_name, W.name))
             else:
                 roof = {"kernel": "conv_fwd_kernel", "bound": "hbm", "achieved": round(conv_gbs, 1),
                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
