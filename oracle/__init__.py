@@ -156,6 +156,19 @@ def round_bf16(v, prec="f64"):
     return vw
 
 
+# --------------------------------------------------------------------- gates
+def gates(a, b, prec="f64"):
+    """The gate step from raw projections: (alpha, beta) = (exp(-softplus(a)),
+    sigmoid(b)) elementwise, in the oracle precision."""
+    aw, bw = widen(a, prec), widen(b, prec)
+    assert aw.shape == bw.shape
+    al, be = np.zeros(aw.shape, _np_t(prec)), np.zeros(bw.shape, _np_t(prec))
+    f = _fn("oracle_gates", prec)
+    f.restype = None
+    f(_p(aw), _p(bw), ctypes.c_int64(aw.size), _p(al), _p(be))
+    return al, be
+
+
 # --------------------------------------------------------------------- recurrence
 def prefill(qkv, alpha, beta, z, norm_w, state, slot_idx, cu_seqlens, has_init, Hk, Hv, *,
             q_scale=1.0, eps=1e-6, chunk=0, prec="f64", want_raw=False):

@@ -36,6 +36,10 @@
 //   - o_t uses the updated state; q_scale multiplies o (1.0 reproduces DEF).
 //   - a negative slot index marks a padding sequence: nothing is read or
 //     written for it.
+//   - the gate step (named by [P3] "Root Cause & RED / GREEN Verification",
+//     which tests a fused gate kernel against its multi-token form, with no
+//     formula) is the workload's own form of the gates: alpha = e^-softplus(a),
+//     beta = sigmoid(b), from raw per-(token, v head) projections a, b.
 //
 // Parity pins (tests/test_oracle_pins.py) fix every function here against
 // brute force, closed forms and invariants; see the test file for the list.
@@ -317,6 +321,19 @@ void chunked_seq(const Geo& g, const T* qkv, const T* alpha, const T* beta, cons
   }
 }
 
+// The gate step: alpha = exp(-softplus(a)), softplus(a) = log(1 + e^a), and
+// beta = 1 / (1 + e^-b), for n elements. softplus is taken as a + log(1 + e^-a)
+// for a > 0 so that e^a is never formed for large a (the same value in exact
+// arithmetic); log1p keeps the small-argument digits.
+template <class T> void gates(const T* a, const T* b, int64_t n, T* alpha, T* beta) {
+  for (int64_t i = 0; i < n; ++i) {
+    const T x = a[i];
+    const T sp = x > T(0) ? x + std::log1p(std::exp(-x)) : std::log1p(std::exp(x));
+    alpha[i] = std::exp(-sp);
+    beta[i] = T(1) / (T(1) + std::exp(-b[i]));
+  }
+}
+
 }  // namespace
 
 // ============================================================== C entry points
@@ -497,6 +514,9 @@ void commit(const T* x, const T* alpha, const T* beta, const T* w, T* conv_state
       T* out, T* postconv, T* o_raw) {                                                          \
     verify<T>(x, w, conv_state, state, alpha, beta, z, norm_w, slot_idx, B, Tn, Hk, Hv,         \
               q_scale, eps, round_act, act32, commit_all, out, postconv, o_raw);                \
+  }                                                                                             \
+  ORACLE_EXPORT void oracle_gates_##SUF(const T* a, const T* b, int64_t n, T* alpha, T* beta) { \
+    gates<T>(a, b, n, alpha, beta);                                                             \
   }                                                                                             \
   ORACLE_EXPORT void oracle_commit_##SUF(const T* x, const T* alpha, const T* beta,            \
       const T* w, T* conv_state, T* state, const int32_t* slot_idx, const int32_t* n_keep,      \

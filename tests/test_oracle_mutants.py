@@ -42,6 +42,10 @@ MUTANTS = {
     "chunk_decay_flipped": ("A[(size_t)t * chunk + s] = beta[(c0 + t) * g.Hv + h] * std::exp(G[t] - G[s])",
                             "A[(size_t)t * chunk + s] = beta[(c0 + t) * g.Hv + h] * std::exp(G[s] - G[t])"),
     "chunk_state_no_decay": ("const T gl = std::exp(G[m - 1]);", "const T gl = T(1);"),
+    "gate_softplus_sign": ("alpha[i] = std::exp(-sp);", "alpha[i] = std::exp(sp);"),
+    "gate_log1p_dropped": ("const T sp = x > T(0) ? x + std::log1p(std::exp(-x)) : std::log1p(std::exp(x));",
+                           "const T sp = x > T(0) ? x : std::exp(x);"),
+    "gate_beta_sign": ("beta[i] = T(1) / (T(1) + std::exp(-b[i]));", "beta[i] = T(1) / (T(1) + std::exp(b[i]));"),
     "commit_keeps_one_more": ("if (slot < 0 || n <= 0 || n > Tn) continue;",
                               "if (slot < 0 || n <= 0 || n > Tn) continue;\n    n = n < Tn ? n + 1 : n;"),
 }

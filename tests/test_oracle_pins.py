@@ -20,6 +20,9 @@ operand, a changed reduction order) fails at least one of them:
   P10 float instantiation against double
   DEF the matrix form of the gated delta rule
   BF  bfloat16 rounding against torch's conversion
+  GT  the gate step: alpha = exp(-softplus(a)) equals the logistic function of -a
+      (scipy's expit), beta = expit(b), closed values at 0, saturation without
+      overflow, the float instantiation against double
 """
 import math
 from fractions import Fraction
@@ -491,3 +494,48 @@ def test_bf16_rounding_matches_torch(orc):
     assert np.array_equal(orc.round_bf16(v, prec="f32"), want)
     assert np.array_equal(orc.round_bf16(v.astype(np.float64)), want.astype(np.float64))
     assert np.array_equal(syn.bf16_bits_to_f32(syn.f32_to_bf16_bits(v)), want)
+
+
+# ------------------------------------------------------------------ GT
+def test_gt_gates_closed_values(orc):
+    """a = 0: softplus = ln 2, alpha = 1/2; b = 0: beta = 1/2 (exact)."""
+    al, be = orc.gates(np.zeros(3), np.zeros(3))
+    assert np.all(np.abs(al - 0.5) <= 2.0 ** -53) and np.all(be == 0.5)
+
+
+def test_gt_gates_are_logistic_functions(orc):
+    """exp(-log(1 + e^a)) = 1 / (1 + e^a) = expit(-a), and beta = expit(b): a sign
+    slip, a dropped log1p or swapped outputs all break one of these."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(31)
+    a = np.concatenate([np.linspace(-40.0, 40.0, 4001), 3.0 * rng.standard_normal(2000)])
+    b = rng.permutation(a)
+    al, be = orc.gates(a, b)
+    np.testing.assert_allclose(al, special.expit(-a), rtol=1e-13, atol=0)
+    np.testing.assert_allclose(be, special.expit(b), rtol=1e-13, atol=0)
+    al2, be2 = orc.gates(-a, -b)
+    np.testing.assert_allclose(al + al2, 1.0, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(be + be2, 1.0, rtol=0, atol=1e-15)
+
+
+def test_gt_gates_saturate_without_overflow(orc):
+    for prec in ("f64", "f32"):
+        a = np.array([-1000.0, -100.0, 100.0, 1000.0])
+        al, be = orc.gates(a, a, prec=prec)
+        assert np.all(np.isfinite(al)) and np.all(np.isfinite(be))
+        assert al[0] == 1.0 and al[3] == 0.0 and be[0] == 0.0 and be[3] == 1.0
+        assert 0.0 <= al[2] < 1e-40 and al[1] == 1.0
+
+
+def test_gt_gates_float_against_double(orc):
+    """The float instantiation (library expf / log1pf) within a few ulp of the
+    double one; alpha's relative error grows with softplus(a) ~ |a| (its
+    exponent's rounding)."""
+    rng = np.random.default_rng(32)
+    a = (3.0 * rng.standard_normal(20000)).astype(np.float32)
+    b = (3.0 * rng.standard_normal(20000)).astype(np.float32)
+    al32, be32 = orc.gates(a, b, prec="f32")
+    al64, be64 = orc.gates(a.astype(np.float64), b.astype(np.float64))
+    ulp = 2.0 ** -23
+    assert np.all(np.abs(al32 - al64) <= al64 * ulp * (3.0 + 2.0 * np.abs(a)))
+    assert np.all(np.abs(be32 - be64) <= be64 * ulp * 3.0)
