@@ -96,6 +96,11 @@ def prefill_roofline(kernel, flops, nbytes, ms, peaks, peak_src, traffic):
             "traffic": traffic if c_bound == "tensor" else None, "peak_source": c_src, **common}
 
 
+def gates_note(gates):
+    return ("raw projections; the gate step runs inside the kernels" if gates == "raw"
+            else "activated alpha, beta inputs")
+
+
 def max_over_ranks(value, device, world):
     """The largest value over the ranks (every rank gets it): with independent
     replicas the job is done when the slowest one is."""
@@ -217,9 +222,10 @@ class ClockSampler:
 class PrefillWorkload:
     """One layer's varlen prefill; inputs resident on the device."""
 
-    def __init__(self, name, torch, G, device):
+    def __init__(self, name, torch, G, device, gates="activated"):
         self.name, self.torch, self.G, self.dev = name, torch, G, device
-        inp = syn.workload_prefill(name)
+        self.gates = gates
+        inp = syn.workload_prefill(name, gate_form="raw" if gates == "raw" else None)
         self.inp = inp
         self.act = torch.bfloat16 if inp["act"] == "bf16" else torch.float32
         t = lambda a: self._dev(a)
@@ -235,7 +241,8 @@ class PrefillWorkload:
         self.slot, self.cu = t(inp["slot_idx"]), t(inp["cu_seqlens"])
         self.hic, self.his = t(inp["has_init_conv"]), t(inp["has_init_state"])
         self.out = torch.empty(inp["n_tok"], inp["Hv"] * D, dtype=self.act, device=device)
-        self.cfg = G.make_config(inp["Hk"], inp["Hv"], self.act, self.S.shape[0])
+        self.cfg = G.make_config(inp["Hk"], inp["Hv"], self.act, self.S.shape[0],
+                                 gates=G.GDN_GATES_RAW if gates == "raw" else G.GDN_GATES_ACTIVATED)
         self.tokens = int(inp["n_tok"])
         es = 2 if inp["act"] == "bf16" else 4
         n_init_c = int(inp["has_init_conv"].sum())
@@ -289,6 +296,7 @@ class PrefillWorkload:
                 "lens": [int(v) for v in inp["lens"]], "qk_heads": int(inp["Hk"]),
                 "v_heads": int(inp["Hv"]), "head_dim": D, "conv_width": 4, "channels": int(inp["C"]),
                 "chunk": 64, "state_dtype": "f32", "act_dtype": inp["act"],
+                "gates": gates_note(self.gates),
                 "l2": "flush 256 MiB between timed steps"}
 
 
@@ -301,8 +309,10 @@ class StepWorkload:
 
     LAYERS = 36
 
-    def __init__(self, name, torch, G, device, T=None):
+    def __init__(self, name, torch, G, device, T=None, gates="activated"):
         self.name, self.torch, self.G, self.dev = name, torch, G, device
+        self.gates = gates
+        raw = gates == "raw"
         decode = name == "decode-bf16"
         self.decode = decode
         h48 = name == "spec-verify-bf16-h48"
@@ -321,14 +331,16 @@ class StepWorkload:
         for _ in range(L):
             lay = dict(x=rn(B, T, C, dt=bf), conv_w=(rn(C, 4) * 0.5).to(bf),
                        conv_state=rn(B, 3, C, dt=bf), state=rn(B, Hv, D, D),
-                       alpha=torch.exp(-torch.nn.functional.softplus(rn(B, T, Hv))),
-                       beta=torch.sigmoid(rn(B, T, Hv)), z=rn(B, T, Hv * D, dt=bf))
+                       alpha=rn(B, T, Hv) if raw else torch.exp(-torch.nn.functional.softplus(rn(B, T, Hv))),
+                       beta=rn(B, T, Hv) if raw else torch.sigmoid(rn(B, T, Hv)),
+                       z=rn(B, T, Hv * D, dt=bf))
             self.layers.append(lay)
         self.norm_w = (1 + 0.1 * rn(D)).contiguous()
         self.slot = torch.randperm(B, generator=g, device=device).to(torch.int32)
         self.n_keep = torch.randint(0, T + 1, (B,), generator=g, device=device, dtype=torch.int32)
         self.out = torch.empty(B, T, Hv * D, dtype=bf, device=device)
-        self.cfg = G.make_config(self.Hk, self.Hv, bf, self.n_slots)
+        self.cfg = G.make_config(self.Hk, self.Hv, bf, self.n_slots,
+                                 gates=G.GDN_GATES_RAW if raw else G.GDN_GATES_ACTIVATED)
         self.views = G.make_layer_views([{k: l[k] for k in ("x", "alpha", "beta", "conv_w",
                                                              "conv_state", "state")}
                                          for l in self.layers], device)
@@ -410,16 +422,19 @@ class StepWorkload:
                 "layers": self.LAYERS, "qk_heads": self.Hk, "v_heads": self.Hv, "head_dim": D,
                 "channels": self.C, "state_dtype": "f32", "act_dtype": "bf16",
                 "n_keep": "uniform in [0, T]" if not self.decode else "all",
+                "gates": gates_note(self.gates),
                 "launch": "CUDA graphs of the window's public calls (value); direct calls (e2e)",
                 "l2": "state pools of all layers exceed L2; flush 256 MiB between timed steps"}
 
 
 # ----------------------------------------------------------------------------- CPU baseline
-def cpu_baseline(name, max_tokens=4096):
+def cpu_baseline(name, max_tokens=4096, gates="activated"):
     """The oracle as it stands (single thread) on a bounded sample of the
-    workload: the first max_tokens tokens of its sequences, conv + recurrence."""
+    workload: the first max_tokens tokens of its sequences, conv (+ the gate
+    step for raw gates) + recurrence."""
     import oracle as orc
-    inp = syn.workload_prefill(name)
+    raw = gates == "raw"
+    inp = syn.workload_prefill(name, gate_form="raw" if raw else None)
     lens, cu = inp["lens"], inp["cu_seqlens"]
     keep, tot = [], 0
     for s in range(inp["n_seq"]):
@@ -436,13 +451,42 @@ def cpu_baseline(name, max_tokens=4096):
                         inp["has_init_conv"][ss], inp["Hk"], inp["Hv"])
     if inp["act"] == "bf16":
         y = orc.round_bf16(y)
-    orc.prefill(y, inp["alpha"][rows], inp["beta"][rows], inp["z"][rows], inp["norm_w"],
+    al, be = inp["alpha"][rows], inp["beta"][rows]
+    if raw:
+        al, be = orc.gates(al, be)
+    orc.prefill(y, al, be, inp["z"][rows], inp["norm_w"],
                 inp["state"], inp["slot_idx"][ss], cu2, inp["has_init_state"][ss], inp["Hk"],
                 inp["Hv"])
     dt = time.perf_counter() - t0
     return {"value": tot / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"first {tot} tokens of {len(keep)} sequence(s) of the {name} workload, "
-                      f"conv + token-by-token recurrence in f64, {dt:.1f} s"}
+                      f"conv + {'gate step + ' if raw else ''}token-by-token recurrence in f64, "
+                      f"{dt:.1f} s"}
+
+
+def cpu_baseline_window(name, T, n_seq=4, gates="activated"):
+    """The oracle on a bounded sample of a verify / decode window: n_seq
+    sequences of one layer (verify, then the commit of the accepted prefix; for
+    decode the commit-all verify), reported as tokens per second per layer."""
+    import oracle as orc
+    decode = name == "decode-bf16"
+    Hv = 48 if name == "spec-verify-bf16-h48" else 32
+    T = 1 if decode else T
+    raw = gates == "raw"
+    inp = syn.verify_inputs(n_seq, T, 16, Hv, "bf16", seed=syn.seed_of(name) + T,
+                            gate_form="raw" if raw else "softplus")
+    t0 = time.perf_counter()
+    al, be = (orc.gates(inp["alpha"], inp["beta"]) if raw else (inp["alpha"], inp["beta"]))
+    orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"], al, be, inp["z"],
+               inp["norm_w"], inp["slot_idx"], 16, Hv, commit_all=decode, act32=True)
+    if not decode:
+        orc.commit(inp["x"], al, be, inp["conv_w"], inp["conv_state"], inp["state"],
+                   inp["slot_idx"], inp["n_keep"], 16, Hv, act32=True)
+    dt = time.perf_counter() - t0
+    return {"value": n_seq * T / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_seq} sequences x {T} tokens of one layer of the {name} window, "
+                      f"{'gate step + ' if raw else ''}verify{'' if decode else ' + commit'} in f64, "
+                      f"{dt:.2f} s"}
 
 
 # ----------------------------------------------------------------------------- main
@@ -455,6 +499,9 @@ def main():
     ap.add_argument("--workload", default="varlen-prefill-bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--T", type=int, default=8, help="draft tokens of spec-verify-bf16")
+    ap.add_argument("--gates", default="activated", choices=["activated", "raw"],
+                    help="raw: alpha / beta inputs are raw projections and the kernels apply "
+                         "the gate step as they read them")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -480,9 +527,9 @@ def main():
         torch.cuda.synchronize()
 
     if args.workload in ("spec-verify-bf16", "spec-verify-bf16-h48", "decode-bf16"):
-        W = StepWorkload(args.workload, torch, G, dev, T=args.T)
+        W = StepWorkload(args.workload, torch, G, dev, T=args.T, gates=args.gates)
     else:
-        W = PrefillWorkload(args.workload, torch, G, dev)
+        W = PrefillWorkload(args.workload, torch, G, dev, gates=args.gates)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -590,7 +637,9 @@ def main():
             "wall_s_timed_region": round(t_wall, 3),
         }
         if world == 1 and not args.no_cpu_baseline and isinstance(W, PrefillWorkload):
-            line["cpu_baseline"] = cpu_baseline(args.workload)
+            line["cpu_baseline"] = cpu_baseline(args.workload, gates=args.gates)
+        elif world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline_window(args.workload, W.T, gates=args.gates)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -606,19 +655,22 @@ def reference_arm(args, rank, world):
     orc.build()
     for _ in range(args.warmup):
         pass                                      # the oracle has no warm-up state
+    window = args.workload in ("spec-verify-bf16", "spec-verify-bf16-h48", "decode-bf16")
     times, toks = [], 0
     line0 = None
     for _ in range(args.steps):
-        cb = cpu_baseline(args.workload, max_tokens=512)
+        cb = (cpu_baseline_window(args.workload, args.T, gates=args.gates) if window
+              else cpu_baseline(args.workload, max_tokens=512, gates=args.gates))
         times.append(1.0 / cb["value"])
         line0 = cb
     tps = 1.0 / statistics.mean(times)
+    per_step = (4 * (1 if args.workload == "decode-bf16" else args.T)) if window else 512
     line = {"impl": "reference", "metric": METRIC, "value": round(tps, 2), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(512 / tps * 1e3, 2), "higher_is_better": True,
+            "ms_per_step": round(per_step / tps * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload,
-                       "sample": "first 512 tokens of the workload per step"},
+            "config": {"workload": args.workload, "gates": gates_note(args.gates),
+                       "sample": line0["sample"] if line0 else ""},
             "cpu_baseline": {"value": round(tps, 2), "unit": "tokens/s", "cores": 1,
                              "kind": "oracle", "sample": line0["sample"] if line0 else ""},
             "e2e": {"value": round(tps, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
-SOURCES = ["conv.cu", "step.cu", "verify.cu", "verify_noalloc.cu", "prefill.cu", "prefill_tc.cu", "gdn_api.cu", "tc_selftest.cu"]
+SOURCES = ["conv.cu", "step.cu", "verify.cu", "verify_noalloc.cu", "prefill.cu", "prefill_tc.cu", "gdn_api.cu", "tc_selftest.cu", "gates.cu"]
 HEADERS = ["common.cuh", "launch.h", "tc.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

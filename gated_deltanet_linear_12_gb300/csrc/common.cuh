@@ -180,6 +180,24 @@ __device__ __forceinline__ float silu_gate(float z) {
   return __fdividef(z, 1.0f + __expf(-z));
 }
 
+// The gate step from raw projections ("Strata PR #3226" names a fused gate
+// kernel; the form is the one of the synthetic workloads' gates):
+//   alpha = exp(-softplus(a)), softplus(a) = log(1 + e^a), taken as
+//           a + log(1 + e^-a) for a > 0 so that e^a is never formed there;
+//   beta  = 1 / (1 + e^-b), taken as e^b / (1 + e^b) for b < 0 (the same value
+//           in exact arithmetic) so that e^-b never overflows there.
+// CUDA's accurate expf / log1pf and correctly rounded adds, multiplies and
+// divide: every kernel that applies the step gets the same bits as gdn_gates.
+__device__ __forceinline__ float gate_alpha(float a) {
+  const float sp = a > 0.0f ? __fadd_rn(a, log1pf(expf(-a))) : log1pf(expf(a));
+  return expf(-sp);
+}
+__device__ __forceinline__ float gate_beta(float b) {
+  const float e = expf(-fabsf(b));                      // in [0, 1]
+  const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, e));  // sigmoid(|b|)
+  return b >= 0.0f ? s : __fmul_rn(e, s);
+}
+
 // Sum of squares of a 128-channel head held as 8 contiguous channels by each
 // of 16 consecutive lanes (lane & 15 = channel group). In-lane: strides 4, 2, 1;
 // across lanes: xor 8, 4, 2, 1, which gives every lane the same bits because

@@ -24,6 +24,7 @@ gdn_status check_cfg(const gdn_config* cfg) {
   if (cfg->n_slots < 1) return GDN_ERR_INVALID;
   if (!(cfg->eps >= 0.f)) return GDN_ERR_INVALID;
   if (cfg->dev_err && (reinterpret_cast<uintptr_t>(cfg->dev_err) & 3u)) return GDN_ERR_INVALID;
+  if (cfg->gates != GDN_GATES_ACTIVATED && cfg->gates != GDN_GATES_RAW) return GDN_ERR_INVALID;
   return GDN_OK;
 }
 
@@ -117,7 +118,7 @@ gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const float
   if (n_seq > 65535) return GDN_ERR_UNSUPPORTED;
   gdn::PrefillArgs a{qkv, alpha, beta, z, norm_w, out, state, slot_idx, cu_seqlens, has_init,
                      n_seq, cfg->n_qk_heads, cfg->n_v_heads, cfg->n_slots, n_tok, cfg->eps,
-                     cfg->q_scale, cfg->dev_err};
+                     cfg->q_scale, cfg->dev_err, cfg->gates == GDN_GATES_RAW};
   return from_cuda(gdn::launch_prefill(a, cfg->act, static_cast<cudaStream_t>(stream)));
 }
 
@@ -153,7 +154,7 @@ gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* con
   if (workspace_bytes < 0 || (!workspace && workspace_bytes != 0)) return GDN_ERR_INVALID;
   gdn::StepArgs a{x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, postconv_out,
                   slot_idx, nullptr, nullptr, B, T, cfg->n_qk_heads, cfg->n_v_heads,
-                  cfg->n_slots, cfg->eps, cfg->q_scale, cfg->dev_err};
+                  cfg->n_slots, cfg->eps, cfg->q_scale, cfg->dev_err, cfg->gates == GDN_GATES_RAW};
   return from_cuda(gdn::launch_verify(a, (flags & GDN_VERIFY_COMMIT_ALL) != 0, cfg->act,
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -170,8 +171,25 @@ gdn_status gdn_commit_layers(const gdn_config* cfg, const gdn_layer_view* layers
     return GDN_ERR_INVALID;
   gdn::StepArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                   nullptr, nullptr, slot_idx, n_keep, layers, B, T, cfg->n_qk_heads,
-                  cfg->n_v_heads, cfg->n_slots, cfg->eps, 1.0f, cfg->dev_err};
+                  cfg->n_v_heads, cfg->n_slots, cfg->eps, 1.0f, cfg->dev_err,
+                  cfg->gates == GDN_GATES_RAW};
   return from_cuda(gdn::launch_commit(a, L, cfg->act, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_gates(const gdn_config* cfg, const float* a, const float* b, float* alpha,
+                     float* beta, int64_t n_tok, void* stream) {
+  if (!cfg) return GDN_ERR_INVALID;
+  if (cfg->n_v_heads < 1 || n_tok < 0) return GDN_ERR_INVALID;
+  if (n_tok == 0) return GDN_OK;
+  if (!a || !b || !alpha || !beta) return GDN_ERR_INVALID;
+  const int64_t n = n_tok * cfg->n_v_heads;
+  if (n / cfg->n_v_heads != n_tok) return GDN_ERR_INVALID;
+  const size_t nb = (size_t)n * sizeof(float);
+  // in place is allowed (alpha = a, beta = b); any other overlap is not
+  if ((alpha != a && overlap(alpha, nb, a, nb)) || (beta != b && overlap(beta, nb, b, nb)) ||
+      overlap(alpha, nb, beta, nb) || overlap(alpha, nb, b, nb) || overlap(beta, nb, a, nb))
+    return GDN_ERR_INVALID;
+  return from_cuda(gdn::launch_gates(a, b, alpha, beta, n, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -68,6 +68,7 @@ struct StepArgs {
   int B, T, Hk, Hv, n_slots;
   float eps, q_scale;
   uint32_t* dev_err;
+  int raw_gates;            // alpha / beta hold raw projections: apply the gate step
 };
 
 struct PrefillArgs {
@@ -85,6 +86,7 @@ struct PrefillArgs {
   int64_t n_tok;
   float eps, q_scale;
   uint32_t* dev_err;
+  int raw_gates;            // alpha / beta hold raw projections: apply the gate step
 };
 
 // Encodes a 2-D row-major bf16 tensor map (rows x cols, row pitch in elements)
@@ -108,5 +110,7 @@ cudaError_t launch_verify_readonly(const StepArgs& a, int act, cudaStream_t stre
 cudaError_t launch_commit(const StepArgs& a, int L, int act, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, int act, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_gates(const float* a, const float* b, float* alpha, float* beta, int64_t n,
+                         cudaStream_t stream);
 
 }  // namespace gdn

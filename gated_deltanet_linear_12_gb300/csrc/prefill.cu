@@ -166,8 +166,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_ffma_kernel(PrefillArgs
     }
     if (warp == 0) {                       // chunk-local log-decay scan (2 tokens per lane)
       const int t0 = 2 * lane;
-      const float la0 = t0 < m ? logf(p.alpha[(c0 + t0) * Hv + h]) : 0.f;
-      const float la1 = t0 + 1 < m ? logf(p.alpha[(c0 + t0 + 1) * Hv + h]) : 0.f;
+      // raw projections: the gate step on the values read
+      auto alpha_of = [&](int64_t gi) { const float v = p.alpha[gi]; return p.raw_gates ? gate_alpha(v) : v; };
+      auto beta_of = [&](int64_t gi) { const float v = p.beta[gi]; return p.raw_gates ? gate_beta(v) : v; };
+      const float la0 = t0 < m ? logf(alpha_of((c0 + t0) * Hv + h)) : 0.f;
+      const float la1 = t0 + 1 < m ? logf(alpha_of((c0 + t0 + 1) * Hv + h)) : 0.f;
       const float pair = la0 + la1;
       float inc = pair;
 #pragma unroll
@@ -178,8 +181,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_ffma_kernel(PrefillArgs
       const float g0 = inc - pair + la0, g1 = inc;
       gl_s[t0] = g0;
       gl_s[t0 + 1] = g1;
-      b_s[t0] = t0 < m ? p.beta[(c0 + t0) * Hv + h] : 0.f;
-      b_s[t0 + 1] = t0 + 1 < m ? p.beta[(c0 + t0 + 1) * Hv + h] : 0.f;
+      b_s[t0] = t0 < m ? beta_of((c0 + t0) * Hv + h) : 0.f;
+      b_s[t0 + 1] = t0 + 1 < m ? beta_of((c0 + t0 + 1) * Hv + h) : 0.f;
       const float glast = __shfl_sync(FULL, g1, 31);
       G_s[t0] = expf(g0);
       G_s[t0 + 1] = expf(g1);

@@ -333,7 +333,14 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
         *reinterpret_cast<uint16_t*>(KT + tc::kmajor_offset(8 * w8 + u, t, 128)) =
             (uint16_t)(wv[u >> 1] >> (16 * (u & 1)));
     }
-    if (tid < C64) la_s[tid] = tid < m ? log2f(al_raw[tid]) : 0.f;
+    if (tid < C64) {
+      float al = al_raw[tid];
+      if (p.raw_gates) {                                 // raw projections: the gate step
+        al = gate_alpha(al);                             // (tokens past the end keep beta = 0)
+        if (tid < m) b_s[tid] = gate_beta(b_s[tid]);
+      }
+      la_s[tid] = tid < m ? log2f(al) : 0.f;
+    }
     tc::fence_async_smem();
     __syncthreads();
 

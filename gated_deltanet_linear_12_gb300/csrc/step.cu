@@ -198,8 +198,9 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
   for (int e = tid; e < nh * n; e += STEP_THREADS) {
     const int g = e / n, t = e % n;
     const int64_t gi = ((int64_t)b * T + t) * Hv + h0 + g;
-    al_s[g * MAXT + t] = alpha[gi];
-    be_s[g * MAXT + t] = beta[gi];
+    const float ga = alpha[gi], gb = beta[gi];
+    al_s[g * MAXT + t] = p.raw_gates ? gate_alpha(ga) : ga;      // raw projections: the gate step
+    be_s[g * MAXT + t] = p.raw_gates ? gate_beta(gb) : gb;
   }
 
   // ---- phase 1: post-conv activations of the block's channels, tokens < n

@@ -392,9 +392,9 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
       gb = p.beta[gi];
     }
     conv_heads();
-    if (tid < T) {
-      al_s[tid] = ga;
-      be_s[tid] = gb;
+    if (tid < T) {                                       // raw projections: the gate step
+      al_s[tid] = p.raw_gates ? gate_alpha(ga) : ga;
+      be_s[tid] = p.raw_gates ? gate_beta(gb) : gb;
     }
   }
 

@@ -19,12 +19,13 @@ from . import build as _build
 GDN_OK, GDN_ERR_INVALID, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
 GDN_F32, GDN_BF16 = 0, 1
 GDN_VERIFY_COMMIT_ALL = 1
+GDN_GATES_ACTIVATED, GDN_GATES_RAW = 0, 1
 GDN_DEVERR_SLOT, GDN_DEVERR_NKEEP, GDN_DEVERR_SEQLENS, GDN_DEVERR_TIMEOUT = 1, 2, 4, 8
 HEAD_DIM, CONV_WIDTH, CHUNK, MAX_DRAFT = 128, 4, 64, 8
 
 EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_workspace_bytes",
            "gdn_verify_step", "gdn_verify_step_noalloc",
-           "gdn_commit_layers", "gdn_selftest_tc_gemm", "gdn_selftest_tc_gemm_tf32", "gdn_status_string"]
+           "gdn_commit_layers", "gdn_gates", "gdn_selftest_tc_gemm", "gdn_selftest_tc_gemm_tf32", "gdn_status_string"]
 
 
 class GdnError(RuntimeError):
@@ -37,7 +38,7 @@ class GdnConfig(ctypes.Structure):
     _fields_ = [("n_qk_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("conv_width", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("eps", ctypes.c_float), ("q_scale", ctypes.c_float),
-                ("n_slots", ctypes.c_int32), ("dev_err", ctypes.c_void_p)]
+                ("n_slots", ctypes.c_int32), ("dev_err", ctypes.c_void_p), ("gates", ctypes.c_int32)]
 
 
 class GdnLayerView(ctypes.Structure):
@@ -75,6 +76,7 @@ def load() -> ctypes.CDLL:
             L.gdn_verify_step_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                                   i32, vp, vp]
             L.gdn_commit_layers.argtypes = [cfgp, vp, i32, vp, vp, i32, i32, vp]
+            L.gdn_gates.argtypes = [cfgp, vp, vp, vp, vp, i64, vp]
             L.gdn_selftest_tc_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
             L.gdn_selftest_tc_gemm_tf32.argtypes = [vp, vp, vp, i32, i32, vp, vp]
             for f in EXPORTS[:-1]:
@@ -103,12 +105,14 @@ def act_of(dtype: torch.dtype) -> int:
     raise ValueError(f"unsupported activation dtype {dtype}")
 
 
-def make_config(n_qk_heads, n_v_heads, act, n_slots, *, eps=1e-6, q_scale=1.0, dev_err=None):
-    """gdn_config; act is GDN_F32/GDN_BF16 or a torch dtype; dev_err a CUDA int32 tensor."""
+def make_config(n_qk_heads, n_v_heads, act, n_slots, *, eps=1e-6, q_scale=1.0, dev_err=None,
+                gates=GDN_GATES_ACTIVATED):
+    """gdn_config; act is GDN_F32/GDN_BF16 or a torch dtype; dev_err a CUDA int32 tensor;
+    gates GDN_GATES_RAW makes alpha / beta arguments raw projections."""
     if isinstance(act, torch.dtype):
         act = act_of(act)
     return GdnConfig(n_qk_heads, n_v_heads, HEAD_DIM, CONV_WIDTH, act, eps, q_scale, n_slots,
-                     dev_err.data_ptr() if dev_err is not None else None)
+                     dev_err.data_ptr() if dev_err is not None else None, gates)
 
 
 def _ptr(t):
@@ -226,6 +230,18 @@ def gdn_commit_layers(cfg, views, n_layers, slot_idx, n_keep, T, *, stream=None)
     _check("gdn_commit_layers", load().gdn_commit_layers(
         ctypes.byref(cfg), _ptr(views), n_layers, _ptr(slot_idx), _ptr(n_keep), slot_idx.numel(),
         T, _stream(slot_idx, stream)))
+
+
+def gdn_gates(cfg, a, b, alpha, beta, *, stream=None):
+    """alpha = exp(-softplus(a)), beta = sigmoid(b) for f32 tensors of the same
+    shape whose last dimension is Hv ([n_tok][Hv] or [B][T][Hv])."""
+    _dense(a, b, alpha, beta)
+    if not (a.shape == b.shape == alpha.shape == beta.shape) or a.shape[-1] != cfg.n_v_heads:
+        raise ValueError("a, b, alpha, beta must share one shape [..., Hv]")
+    if any(t.dtype != torch.float32 for t in (a, b, alpha, beta)):
+        raise ValueError("gates are float32")
+    _check("gdn_gates", load().gdn_gates(ctypes.byref(cfg), _ptr(a), _ptr(b), _ptr(alpha), _ptr(beta),
+                                         a.numel() // cfg.n_v_heads, _stream(a, stream)))
 
 
 def gdn_selftest_tc_gemm(A, B, D, *, starve_wait=False, dev_err=None, stream=None):

@@ -3,8 +3,11 @@
 This module is shared by the tests, the benchmark and the CPU oracle's
 callers. It draws random numbers and packs them into the layouts the path
 uses; it performs none of the path's arithmetic (no convolution, activation,
-normalisation or recurrence). Gate values alpha and beta are drawn directly in
-their activated form, because the gate projection lies before the path.
+normalisation or recurrence). Gate values alpha and beta are drawn in their
+activated form (the workloads' distribution, alpha = exp(-softplus(N)) and
+beta = sigmoid(N), written here with numpy as an input recipe), or, with
+gate_form "raw", as the raw projections a, b ~ N(0, 1) that the library's gate
+step (and the oracle's, independently) turns into that same distribution.
 
 Layouts (row-major, head_dim d = 128, conv width 4):
   qkv / x       [n_tok][C], C = (2*Hk + Hv) * d, channels packed [q | k | v]
@@ -83,6 +86,9 @@ def _gates(rng, shape, form: str):
     if form == "uniform":          # alpha ~ U(0.9, 1), beta ~ U(0, 1)
         a = rng.uniform(0.9, 1.0, size=shape).astype(np.float32)
         b = rng.uniform(0.0, 1.0, size=shape).astype(np.float32)
+    elif form == "raw":            # raw projections a, b ~ N(0, 1) for the gate step
+        a = rng.standard_normal(shape).astype(np.float32)
+        b = rng.standard_normal(shape).astype(np.float32)
     elif form == "softplus":       # alpha = exp(-softplus(N)), beta = sigmoid(N)
         na = rng.standard_normal(shape)
         nb = rng.standard_normal(shape)
@@ -139,20 +145,22 @@ def prefill_inputs(lens, Hk, Hv, act, *, seed, init_mask=None, gate_form="softpl
     )
 
 
-def workload_prefill(name: str, *, seed=None):
+def workload_prefill(name: str, *, seed=None, gate_form=None):
+    """gate_form None: the workload's own; "raw": raw projections for the gate step."""
     seed = seed_of(name) if seed is None else seed
+    gf = gate_form or "softplus"
     if name == "tiny-f32":
         # one sequence of 64 tokens; random conv_state read, zero initial S
         return prefill_inputs([64], 2, 4, "f32", seed=seed, init_conv=[1], init_state=[0],
-                              gate_form="uniform")
+                              gate_form=gate_form or "uniform")
     if name == "varlen-prefill-bf16":
         rng = np.random.default_rng(seed ^ 0x5EED)
         lens = rng.integers(1, 2049, size=8)
         mask = np.array([i % 2 for i in range(8)], np.uint8)   # odd sequences carry state
-        return prefill_inputs(lens, 16, 32, "bf16", seed=seed, init_mask=mask)
+        return prefill_inputs(lens, 16, 32, "bf16", seed=seed, init_mask=mask, gate_form=gf)
     if name == "long-prefill-bf16":
         return prefill_inputs([16384] * 4, 16, 32, "bf16", seed=seed,
-                              init_mask=np.zeros(4, np.uint8))
+                              init_mask=np.zeros(4, np.uint8), gate_form=gf)
     raise ValueError(name)
 
 

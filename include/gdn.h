@@ -62,6 +62,11 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 #define GDN_MAX_DRAFT 8
 #define GDN_CHUNK 64
 
+/* gdn_config.gates: what the alpha / beta arguments hold */
+#define GDN_GATES_ACTIVATED 0     /* the gates alpha_t, beta_t themselves */
+#define GDN_GATES_RAW 1           /* raw projections a_t, b_t: each kernel applies the
+                                     gate step (see gdn_gates) to the values it reads */
+
 /* verify flags */
 #define GDN_VERIFY_COMMIT_ALL 1u  /* accept every draft token: advance conv_state
                                      and state in place (decode) */
@@ -83,10 +88,14 @@ typedef struct gdn_config {
   float q_scale;        /* multiplies o_t; 1.0 gives o_t = S_t q_t */
   int32_t n_slots;      /* slots in the conv_state and state pools */
   uint32_t* dev_err;    /* nullable device word receiving GDN_DEVERR_* bits */
+  int32_t gates;        /* GDN_GATES_ACTIVATED (0) or GDN_GATES_RAW: applies to the
+                           alpha / beta arguments of gdn_delta_prefill and
+                           gdn_verify_step and to the layer views of gdn_commit_layers */
 } gdn_config;
 
 /* One layer's device views for gdn_commit_layers (the array itself lives in
- * device memory). x, alpha, beta are that layer's verify inputs. */
+ * device memory). x, alpha, beta are that layer's verify inputs (raw
+ * projections a, b when the config's gates is GDN_GATES_RAW). */
 typedef struct gdn_layer_view {
   const void* x;         /* [B][T][C] act */
   const float* alpha;    /* [B][T][Hv] */
@@ -140,7 +149,8 @@ gdn_status gdn_postconv_norm(const gdn_config* cfg, int32_t in_t, const void* y_
  * o_t = S_t q_t, and "Strata PR #3226" (output norm after the recurrence).
  *   qkv     [n_tok][C] act: post-conv rows (q, k L2-normalised), e.g. from
  *           gdn_conv_fwd(fuse_norm=1)
- *   alpha, beta [n_tok][Hv] f32 (already activated gates)
+ *   alpha, beta [n_tok][Hv] f32: the gates, or the raw a, b when cfg->gates is
+ *               GDN_GATES_RAW
  *   z, out  [n_tok][Hv*128] act; out = RMSNorm(o) * norm_w * silu(z)
  *   norm_w  [128] f32
  *   state   pool: read at slot_idx[s] when has_init[s] (else zero), always
@@ -168,7 +178,8 @@ int64_t gdn_verify_workspace_bytes(const gdn_config* cfg, int32_t B, int32_t T);
  * state, and the gated RMSNorm, for every draft token.
  * Source: "Strata PR #3226" ("Summary": verify forward launched once per layer).
  *   x       [B][T][C] act (raw, pre-conv rows of the draft tokens)
- *   alpha, beta [B][T][Hv] f32; z, out [B][T][Hv*128] act; norm_w [128] f32
+ *   alpha, beta [B][T][Hv] f32 (raw a, b when cfg->gates is GDN_GATES_RAW);
+ *   z, out [B][T][Hv*128] act; norm_w [128] f32
  *   slot_idx [B] int32 into both pools
  *   flags   0: conv_state and state are only read;
  *           GDN_VERIFY_COMMIT_ALL: both advance in place by all T tokens,
@@ -225,6 +236,29 @@ gdn_status gdn_verify_step_noalloc(const gdn_config* cfg, const void* x, const v
 gdn_status gdn_commit_layers(const gdn_config* cfg, const gdn_layer_view* layers, int32_t L,
                              const int32_t* slot_idx, const int32_t* n_keep, int32_t B,
                              int32_t T, void* stream);
+
+/*
+ * gdn_gates — the gate step: alpha = exp(-softplus(a)), beta = sigmoid(b),
+ * softplus(a) = log(1 + e^a), elementwise over n_tok rows of Hv values.
+ * Source: "Strata PR #3226", "Root Cause & RED / GREEN Verification" — a fused
+ * gate kernel and its multi-token form, tested bitwise against each other; the
+ * pages print no formula, and the form here is the one that defines the gates
+ * of the synthetic workloads. In GDN_GATES_RAW mode the prefill, verify and
+ * commit kernels apply the same device function to the raw values they read,
+ * so their results are bitwise those of gdn_gates followed by the same call in
+ * GDN_GATES_ACTIVATED mode.
+ *
+ *   a, b          [n_tok][Hv] f32 raw projections (device)
+ *   alpha, beta   [n_tok][Hv] f32 results (device, caller-owned); alpha may be a
+ *                 and beta may be b (in place), other overlaps are invalid
+ *   cfg->gates is not read (the call always applies the gate step).
+ * Accuracy: CUDA's expf / log1pf and a correctly rounded divide, within a few
+ * ulp of the exact gates (alpha's relative error grows with softplus(a)).
+ * Errors: GDN_ERR_INVALID for null pointers (n_tok > 0), n_tok < 0 or bad
+ * overlaps; GDN_ERR_CUDA if the launch fails. n_tok == 0 enqueues nothing.
+ */
+gdn_status gdn_gates(const gdn_config* cfg, const float* a, const float* b, float* alpha,
+                     float* beta, int64_t n_tok, void* stream);
 
 /* Static description of a status code. */
 const char* gdn_status_string(gdn_status s);

@@ -119,3 +119,25 @@ def test_binding_refuses_cpu_tensors():
     t = torch.zeros(4, 384)
     with pytest.raises(ValueError):
         gdn.gdn_postconv_norm(cfg, t, t)
+
+
+def test_gates_mode_and_gdn_gates_host_validation(lib):
+    """An unknown gates mode is rejected by every entry that reads the config;
+    gdn_gates rejects null pointers, negative sizes and overlaps other than in
+    place, and enqueues nothing for n_tok = 0."""
+    assert _conv(lib, _cfg(gates=2)) == 1
+    assert _conv(lib, _cfg(gates=-1)) == 1
+    c = _cfg()
+    c_raw = _cfg(gates=1)
+    n = 10
+    nb = n * 4 * 4                                          # n_tok x Hv f32
+    assert lib.gdn_gates(None, P[0], P[1], P[2], P[3], n, None) == 1
+    assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[2], P[3], -1, None) == 1
+    assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[2], P[3], 0, None) == 0
+    assert lib.gdn_gates(ctypes.byref(c_raw), 0, 0, 0, 0, 0, None) == 0
+    assert lib.gdn_gates(ctypes.byref(c), 0, P[1], P[2], P[3], n, None) == 1
+    assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[2], 0, n, None) == 1
+    assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[2], P[2] + nb - 4, n, None) == 1   # alpha/beta
+    assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[1], P[3], n, None) == 1            # alpha = b
+    assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[0] + 4, P[3], n, None) == 1        # shifted a
+    assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[2], P[0], n, None) == 1            # beta = a
