@@ -131,6 +131,8 @@ KERNEL_SOURCES = {
                         "gated_deltanet_linear_12_gb300/csrc/common.cuh"],
     "step_kernel": ["gated_deltanet_linear_12_gb300/csrc/step.cu",
                     "gated_deltanet_linear_12_gb300/csrc/common.cuh"],
+    "lazy_kernel": ["gated_deltanet_linear_12_gb300/csrc/step.cu",
+                    "gated_deltanet_linear_12_gb300/csrc/common.cuh"],
     "verify_kernel": ["gated_deltanet_linear_12_gb300/csrc/verify.cu",
                       "gated_deltanet_linear_12_gb300/csrc/tc.cuh",
                       "gated_deltanet_linear_12_gb300/csrc/common.cuh"],
@@ -309,10 +311,12 @@ class StepWorkload:
 
     LAYERS = 36
 
-    def __init__(self, name, torch, G, device, T=None, gates="activated"):
+    def __init__(self, name, torch, G, device, T=None, gates="activated", lazy=False):
         self.name, self.torch, self.G, self.dev = name, torch, G, device
         self.gates = gates
         raw = gates == "raw"
+        # lazy: each verify launch first commits the previous window's accepted prefix
+        self.lazy = lazy and name != "decode-bf16"
         decode = name == "decode-bf16"
         self.decode = decode
         h48 = name == "spec-verify-bf16-h48"
@@ -334,6 +338,10 @@ class StepWorkload:
                        alpha=rn(B, T, Hv) if raw else torch.exp(-torch.nn.functional.softplus(rn(B, T, Hv))),
                        beta=rn(B, T, Hv) if raw else torch.sigmoid(rn(B, T, Hv)),
                        z=rn(B, T, Hv * D, dt=bf))
+            if self.lazy:                                   # the previous window's drafts
+                lay.update(px=rn(B, T, C, dt=bf),
+                           palpha=rn(B, T, Hv) if raw else torch.exp(-torch.nn.functional.softplus(rn(B, T, Hv))),
+                           pbeta=rn(B, T, Hv) if raw else torch.sigmoid(rn(B, T, Hv)))
             self.layers.append(lay)
         self.norm_w = (1 + 0.1 * rn(D)).contiguous()
         self.slot = torch.randperm(B, generator=g, device=device).to(torch.int32)
@@ -346,7 +354,7 @@ class StepWorkload:
                                          for l in self.layers], device)
         self.tokens = B * T                                 # per layer per step
         # read-only verify: one cooperative launch per layer, then one commit launch
-        self.launches_per_step = L if decode else L + 1
+        self.launches_per_step = L if (decode or self.lazy) else L + 1
         self.ws = None if decode else G.verify_workspace(self.cfg, B, T, device)
         nk = self.n_keep.cpu().numpy()
         S_head = D * D * 4
@@ -359,19 +367,33 @@ class StepWorkload:
                 sum(2 * per_seq_state + 2 * 3 * C * 2 + n * (C * 2 + 2 * Hv * 4) + C * 4 * 2
                     for n in nk if n > 0)),
         }
+        if self.lazy:                    # one pass: S read once, written where n_keep > 0
+            self.bytes = {
+                "verify": L * int(B * per_seq_state + B * 3 * C * 2
+                                  + sum(per_seq_state + 3 * C * 2 + n * (C * 2 + 2 * Hv * 4)
+                                        for n in nk if n > 0)
+                                  + B * T * (C * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + C * 4 * 2),
+                "commit": 0}
 
     def reset(self):
         pass                                                # state evolution does not change work
 
     def verify_layers(self):
         G = self.G
+        if self.lazy:
+            for lay in self.layers:
+                G.gdn_verify_step_lazy(self.cfg, lay["px"], lay["palpha"], lay["pbeta"], self.n_keep,
+                                       lay["x"], lay["conv_w"], lay["conv_state"], lay["state"],
+                                       lay["alpha"], lay["beta"], lay["z"], self.norm_w, self.out,
+                                       self.slot)
+            return
         for lay in self.layers:
             G.gdn_verify_step(self.cfg, lay["x"], lay["conv_w"], lay["conv_state"], lay["state"],
                               lay["alpha"], lay["beta"], lay["z"], self.norm_w, self.out, self.slot,
                               commit_all=self.decode, workspace=self.ws)
 
     def commit(self):
-        if not self.decode:
+        if not self.decode and not self.lazy:
             self.G.gdn_commit_layers(self.cfg, self.views, self.LAYERS, self.slot, self.n_keep, self.T)
 
     def capture(self):
@@ -386,8 +408,9 @@ class StepWorkload:
         with torch.cuda.stream(s):
             with torch.cuda.graph(self.g_verify, stream=s):
                 self.verify_layers()
-            with torch.cuda.graph(self.g_commit, stream=s):
-                self.commit()
+            if not self.lazy:                           # lazy: the commit rides on the verify
+                with torch.cuda.graph(self.g_commit, stream=s):
+                    self.commit()
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
 
@@ -398,7 +421,8 @@ class StepWorkload:
         self.g_verify.replay() if graphs else self.verify_layers()
         if ev:
             ev[1].record()
-        self.g_commit.replay() if graphs else self.commit()
+        if not self.lazy:
+            self.g_commit.replay() if graphs else self.commit()
         if ev:
             ev[2].record()
 
@@ -422,6 +446,8 @@ class StepWorkload:
                 "layers": self.LAYERS, "qk_heads": self.Hk, "v_heads": self.Hv, "head_dim": D,
                 "channels": self.C, "state_dtype": "f32", "act_dtype": "bf16",
                 "n_keep": "uniform in [0, T]" if not self.decode else "all",
+                "window": ("lazy: each verify launch commits the previous window's accepted prefix"
+                           if self.lazy else "verify launches, then one batched commit"),
                 "gates": gates_note(self.gates),
                 "launch": "CUDA graphs of the window's public calls (value); direct calls (e2e)",
                 "l2": "state pools of all layers exceed L2; flush 256 MiB between timed steps"}
@@ -499,6 +525,8 @@ def main():
     ap.add_argument("--workload", default="varlen-prefill-bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--T", type=int, default=8, help="draft tokens of spec-verify-bf16")
+    ap.add_argument("--lazy", action="store_true",
+                    help="verify windows: fold each window's commit into the next window's verify")
     ap.add_argument("--gates", default="activated", choices=["activated", "raw"],
                     help="raw: alpha / beta inputs are raw projections and the kernels apply "
                          "the gate step as they read them")
@@ -527,7 +555,7 @@ def main():
         torch.cuda.synchronize()
 
     if args.workload in ("spec-verify-bf16", "spec-verify-bf16-h48", "decode-bf16"):
-        W = StepWorkload(args.workload, torch, G, dev, T=args.T, gates=args.gates)
+        W = StepWorkload(args.workload, torch, G, dev, T=args.T, gates=args.gates, lazy=args.lazy)
     else:
         W = PrefillWorkload(args.workload, torch, G, dev, gates=args.gates)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -585,13 +613,14 @@ def main():
         peaks, peak_src = load_peaks()
         a_avg, b_avg = statistics.mean(conv_ms), statistics.mean(pf_ms)
         if isinstance(W, StepWorkload):
-            vk = "step_kernel" if W.decode else "verify_kernel"
-            names = (f"{vk} ({'decode' if W.decode else 'verify'})", "step_kernel (commit)")
+            vk = "step_kernel" if W.decode else "lazy_kernel" if W.lazy else "verify_kernel"
+            names = (f"{vk} ({'decode' if W.decode else 'commit + verify' if W.lazy else 'verify'})",
+                     "step_kernel (commit)")
             ka = {"ms": round(a_avg, 4), "bytes": W.bytes["verify"],
                   "GB/s": round(W.bytes["verify"] / (a_avg * 1e-3) / 1e9, 1)}
             ka["frac_hbm"] = round(ka["GB/s"] / peaks["hbm_gbs"], 4)
             kernels = {names[0]: ka}
-            if not W.decode:
+            if not W.decode and not W.lazy:
                 kb = {"ms": round(b_avg, 4), "bytes": W.bytes["commit"],
                       "GB/s": round(W.bytes["commit"] / max(b_avg, 1e-9) / 1e6, 1)}
                 kb["frac_hbm"] = round(kb["GB/s"] / peaks["hbm_gbs"], 4)

@@ -159,6 +159,38 @@ gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* con
                                       static_cast<cudaStream_t>(stream)));
 }
 
+gdn_status gdn_verify_step_lazy(const gdn_config* cfg, const void* prev_x, const float* prev_alpha,
+                                const float* prev_beta, const int32_t* prev_n_keep, int32_t prev_T,
+                                const void* x, const void* conv_w, void* conv_state, float* state,
+                                const float* alpha, const float* beta, const void* z,
+                                const float* norm_w, void* out, const int32_t* slot_idx, int32_t B,
+                                int32_t T, void* postconv_out, void* stream) {
+  gdn_status st = check_cfg(cfg);
+  if (st != GDN_OK) return st;
+  if (B < 0 || T < 1 || T > GDN_MAX_DRAFT || prev_T < 1 || prev_T > GDN_MAX_DRAFT)
+    return GDN_ERR_INVALID;
+  if (B == 0) return GDN_OK;
+  if (B > 65535) return GDN_ERR_UNSUPPORTED;
+  if (!prev_x || !prev_alpha || !prev_beta || !prev_n_keep || !x || !conv_w || !conv_state ||
+      !state || !alpha || !beta || !z || !norm_w || !out || !slot_idx)
+    return GDN_ERR_INVALID;
+  if (!aligned16(prev_x) || !aligned16(x) || !aligned16(conv_w) || !aligned16(conv_state) ||
+      !aligned16(state) || !aligned16(z) || !aligned16(out) || !aligned16(norm_w) ||
+      (postconv_out && !aligned16(postconv_out)))
+    return GDN_ERR_INVALID;
+  const size_t es = esize(cfg->act);
+  const size_t HvD = (size_t)cfg->n_v_heads * GDN_HEAD_DIM, C = (size_t)channels(cfg);
+  const size_t nt = (size_t)B * T, np = (size_t)B * prev_T;
+  if (overlap(out, nt * HvD * es, x, nt * C * es) || overlap(out, nt * HvD * es, z, nt * HvD * es) ||
+      overlap(out, nt * HvD * es, prev_x, np * C * es))
+    return GDN_ERR_INVALID;
+  gdn::StepArgs a{x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, postconv_out,
+                  slot_idx, prev_n_keep, nullptr, B, T, cfg->n_qk_heads, cfg->n_v_heads,
+                  cfg->n_slots, cfg->eps, cfg->q_scale, cfg->dev_err, cfg->gates == GDN_GATES_RAW,
+                  prev_x, prev_alpha, prev_beta, prev_T};
+  return from_cuda(gdn::launch_verify_lazy(a, cfg->act, static_cast<cudaStream_t>(stream)));
+}
+
 gdn_status gdn_commit_layers(const gdn_config* cfg, const gdn_layer_view* layers, int32_t L,
                              const int32_t* slot_idx, const int32_t* n_keep, int32_t B,
                              int32_t T, void* stream) {

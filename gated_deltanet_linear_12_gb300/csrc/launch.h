@@ -69,6 +69,11 @@ struct StepArgs {
   float eps, q_scale;
   uint32_t* dev_err;
   int raw_gates;            // alpha / beta hold raw projections: apply the gate step
+  // verify with the previous window's commit folded in (n_keep: its accepted prefixes)
+  const void* prev_x;       // [B][prev_T][C]
+  const float* prev_alpha;  // [B][prev_T][Hv]
+  const float* prev_beta;
+  int prev_T;
 };
 
 struct PrefillArgs {
@@ -108,6 +113,7 @@ cudaError_t launch_postconv_norm(const gdn_config& cfg, int in_t, const void* yi
 cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, cudaStream_t stream);
 cudaError_t launch_verify_readonly(const StepArgs& a, int act, cudaStream_t stream);
 cudaError_t launch_commit(const StepArgs& a, int L, int act, cudaStream_t stream);
+cudaError_t launch_verify_lazy(const StepArgs& a, int act, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, int act, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_gates(const float* a, const float* b, float* alpha, float* beta, int64_t n,

@@ -33,7 +33,7 @@
 
 namespace gdn {
 
-enum StepMode { VERIFY_COMMIT_ALL = 1, COMMIT = 2 };
+enum StepMode { VERIFY_COMMIT_ALL = 1, COMMIT = 2, VERIFY_ONLY = 3 };
 
 constexpr int STEP_THREADS = 256;
 constexpr int MAX_HEADS = 16;                    // v heads per block (Hv / Hk limit)
@@ -115,42 +115,47 @@ __device__ __forceinline__ void rows_dot(const float4 (&S)[2][8], const float* v
   r1 = a1;
 }
 
-template <int A, int MODE>
-__global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
-  extern __shared__ __align__(16) float smem[];
+// One pass of the step over the draft tokens of sequence b = blockIdx.y of one
+// layer, by MODE:
+//   COMMIT             the first n_keep[b] tokens enter conv_state and state (no outputs)
+//   VERIFY_COMMIT_ALL  outputs of the T tokens, conv_state and state advanced by all
+//   VERIFY_ONLY        outputs of the T tokens, nothing written back
+// The pass reads x, alpha, beta (T tokens per sequence) and the pools given, or
+// with VIEWS those of layer blockIdx.z of the view table. Returns false when the
+// sequence is skipped (padding, or a bad slot or n_keep, reported).
+template <int A, int MODE, bool VIEWS>
+__device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, const float* alpha,
+                                          const float* beta, const int T, float* smem) {
   constexpr bool OUTPUTS = MODE != COMMIT;
+  constexpr bool WRITES = MODE != VERIFY_ONLY;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.y;
-  const int T = p.T, Hk = p.Hk, Hv = p.Hv, G = Hv / Hk;
+  const int Hk = p.Hk, Hv = p.Hv, G = Hv / Hk;
   const int C = (2 * Hk + Hv) * D;
 
-  // Per-layer views (the committing call walks the layers in blockIdx.z).
-  const void* x = p.x;
   const void* conv_w = p.conv_w;
   void* conv_state = p.conv_state;
   float* state = p.state;
-  const float* alpha = p.alpha;
-  const float* beta = p.beta;
-  if constexpr (MODE == COMMIT) {
+  if constexpr (VIEWS) {                                  // the committing call walks the layers
     const gdn_layer_view lv = p.layers[blockIdx.z];
     x = lv.x; conv_w = lv.conv_w; conv_state = lv.conv_state; state = lv.state;
     alpha = lv.alpha; beta = lv.beta;
   }
 
   const int slot = p.slot_idx[b];
-  if (slot < 0) return;                                   // padding entry
+  if (slot < 0) return false;                             // padding entry
   if (slot >= p.n_slots) {
     if (tid == 0 && blockIdx.x == 0) report(p.dev_err, GDN_DEVERR_SLOT);
-    return;
+    return false;
   }
   int n = T;                                              // tokens that enter the state
   if constexpr (MODE == COMMIT) {
     n = p.n_keep[b];
     if (n < 0 || n > T) {
       if (tid == 0 && blockIdx.x == 0) report(p.dev_err, GDN_DEVERR_NKEEP);
-      return;
+      return false;
     }
-    if (n == 0) return;
+    if (n == 0) return true;
   }
 
   // Heads of this block: a whole q/k head group.
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
   __syncthreads();
 
   // ---- conv_state commit: last 3 rows of (old rows ++ draft rows 0..n-1)
-  {
+  if constexpr (WRITES) {
     constexpr int MAXI = 4;                               // (2 + G) * 48 <= 4 * 256
     const int groups = (2 + nh) * 16;
     const int items = KS * groups;
@@ -353,7 +358,7 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
     }
 
     // state commit: S_n = g_{n-1} S0 + sum_s r(n-1,s) d_s k_s^T, in place
-    {
+    if constexpr (WRITES) {
       const float gl = g_s[n - 1];
       float e0[MAXT], e1[MAXT];
 #pragma unroll
@@ -410,6 +415,27 @@ __global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
       }
     }
   }
+  return true;
+}
+
+template <int A, int MODE>
+__global__ void __launch_bounds__(STEP_THREADS, 2) step_kernel(StepArgs p) {
+  extern __shared__ __align__(16) float smem[];
+  step_pass<A, MODE, MODE == COMMIT>(p, p.x, p.alpha, p.beta, p.T, smem);
+}
+
+// Verify with the previous window's commit folded in: first the accepted
+// prefix (n_keep[b] of its prev_T tokens) of the previous window enters
+// conv_state and state, by the same instructions as the batched commit, then
+// the T new draft tokens are verified from the committed state, which this
+// block has just written (its state rows come back from L2; each thread reads
+// the rows it wrote). Nothing of the new drafts is written back.
+template <int A>
+__global__ void __launch_bounds__(STEP_THREADS, 2) lazy_kernel(StepArgs p) {
+  extern __shared__ __align__(16) float smem[];
+  if (!step_pass<A, COMMIT, false>(p, p.prev_x, p.prev_alpha, p.prev_beta, p.prev_T, smem)) return;
+  __syncthreads();                                        // conv_state rows and tables settled
+  step_pass<A, VERIFY_ONLY, false>(p, p.x, p.alpha, p.beta, p.T, smem);
 }
 
 size_t step_smem_bytes(int nh) {
@@ -437,6 +463,22 @@ cudaError_t launch_verify(const StepArgs& a, bool commit_all, int act, cudaStrea
   const int nh = a.Hv / a.Hk;
   return act == GDN_BF16 ? launch_mode<BF16, VERIFY_COMMIT_ALL>(a, grid, nh, stream)
                          : launch_mode<F32, VERIFY_COMMIT_ALL>(a, grid, nh, stream);
+}
+
+template <int A>
+static cudaError_t launch_lazy_t(const StepArgs& a, cudaStream_t stream) {
+  const int nh = a.Hv / a.Hk;
+  const size_t smem = step_smem_bytes(nh);
+  if (smem > 48 * 1024) {
+    cudaError_t e = set_smem_once<lazy_kernel<A>>((int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  lazy_kernel<A><<<dim3(a.Hk, a.B, 1), STEP_THREADS, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_lazy(const StepArgs& a, int act, cudaStream_t stream) {
+  return act == GDN_BF16 ? launch_lazy_t<BF16>(a, stream) : launch_lazy_t<F32>(a, stream);
 }
 
 cudaError_t launch_commit(const StepArgs& a, int L, int act, cudaStream_t stream) {

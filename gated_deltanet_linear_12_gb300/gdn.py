@@ -25,7 +25,7 @@ HEAD_DIM, CONV_WIDTH, CHUNK, MAX_DRAFT = 128, 4, 64, 8
 
 EXPORTS = ["gdn_conv_fwd", "gdn_postconv_norm", "gdn_delta_prefill", "gdn_verify_workspace_bytes",
            "gdn_verify_step", "gdn_verify_step_noalloc",
-           "gdn_commit_layers", "gdn_gates", "gdn_selftest_tc_gemm", "gdn_selftest_tc_gemm_tf32", "gdn_status_string"]
+           "gdn_commit_layers", "gdn_gates", "gdn_verify_step_lazy", "gdn_selftest_tc_gemm", "gdn_selftest_tc_gemm_tf32", "gdn_status_string"]
 
 
 class GdnError(RuntimeError):
@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
                                                   i32, vp, vp]
             L.gdn_commit_layers.argtypes = [cfgp, vp, i32, vp, vp, i32, i32, vp]
             L.gdn_gates.argtypes = [cfgp, vp, vp, vp, vp, i64, vp]
+            L.gdn_verify_step_lazy.argtypes = [cfgp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp,
+                                               vp, vp, vp, i32, i32, vp, vp]
             L.gdn_selftest_tc_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
             L.gdn_selftest_tc_gemm_tf32.argtypes = [vp, vp, vp, i32, i32, vp, vp]
             for f in EXPORTS[:-1]:
@@ -230,6 +232,23 @@ def gdn_commit_layers(cfg, views, n_layers, slot_idx, n_keep, T, *, stream=None)
     _check("gdn_commit_layers", load().gdn_commit_layers(
         ctypes.byref(cfg), _ptr(views), n_layers, _ptr(slot_idx), _ptr(n_keep), slot_idx.numel(),
         T, _stream(slot_idx, stream)))
+
+
+def gdn_verify_step_lazy(cfg, prev_x, prev_alpha, prev_beta, prev_n_keep, x, conv_w, conv_state,
+                         state, alpha, beta, z, norm_w, out, slot_idx, *, postconv_out=None,
+                         stream=None):
+    """Verify of x's T drafts with the previous window's accepted prefixes
+    (prev_x [B][prev_T][C], prev_n_keep [B]) committed first, in one launch."""
+    _dense(prev_x, prev_alpha, prev_beta, prev_n_keep, x, conv_w, conv_state, state, alpha, beta,
+           z, norm_w, out, slot_idx, postconv_out)
+    B, T = x.shape[0], x.shape[1]
+    if prev_x.shape[0] != B:
+        raise ValueError("prev_x and x must have the same batch")
+    _check("gdn_verify_step_lazy", load().gdn_verify_step_lazy(
+        ctypes.byref(cfg), _ptr(prev_x), _ptr(prev_alpha), _ptr(prev_beta), _ptr(prev_n_keep),
+        prev_x.shape[1], _ptr(x), _ptr(conv_w), _ptr(conv_state), _ptr(state), _ptr(alpha),
+        _ptr(beta), _ptr(z), _ptr(norm_w), _ptr(out), _ptr(slot_idx), B, T, _ptr(postconv_out),
+        _stream(x, stream)))
 
 
 def gdn_gates(cfg, a, b, alpha, beta, *, stream=None):

@@ -238,6 +238,43 @@ gdn_status gdn_commit_layers(const gdn_config* cfg, const gdn_layer_view* layers
                              int32_t T, void* stream);
 
 /*
+ * gdn_verify_step_lazy — the verify of T new draft tokens with the commit of the
+ * previous window's accepted prefix folded in, for one layer.
+ * Source: "Strata PR #3226" — "Summary": the verify forward launched once per
+ * layer and the batched commit of the accepted prefix of conv_state and state;
+ * "Problem and result": a forward variant that commits inside the forward
+ * (commit_state = true), tested bitwise against the forward without it followed
+ * by the separate commit. Here the commit of one window rides on the next
+ * window's forward.
+ *
+ * Equivalent to gdn_commit_layers over this one layer with (prev_x, prev_alpha,
+ * prev_beta, prev_n_keep, prev_T), followed by gdn_verify_step (read-only) of
+ * (x, alpha, beta, T): conv_state and state leave the call bitwise equal to that
+ * commit (same instructions), and nothing of the new drafts is written back, so
+ * the next window passes this window's inputs and accepted prefixes as prev_*.
+ * The state is read from HBM once per call, not twice (verify, then commit).
+ * The outputs come from the step kernel's CUDA-core products on the committed
+ * state (bitwise equal to decode's arithmetic, within the bf16 / f32
+ * tolerances of gdn_verify_step's).
+ *
+ *   prev_x        [B][prev_T][C] act: the previous window's draft rows of this layer
+ *   prev_alpha, prev_beta  [B][prev_T][Hv] f32 (raw a, b in GDN_GATES_RAW mode)
+ *   prev_n_keep   [B] int32 in [0, prev_T]: accepted tokens of the previous window
+ *                 (0: nothing to commit for that sequence)
+ *   the other arguments as gdn_verify_step's (without flags and workspace); row b
+ *   is the same sequence (slot_idx[b]) in both windows.
+ * Errors: GDN_ERR_INVALID for null pointers, T or prev_T outside 1..GDN_MAX_DRAFT,
+ * misalignment, out overlapping x, z or prev_x. A prev_n_keep outside
+ * [0, prev_T] sets GDN_DEVERR_NKEEP and skips that sequence (nothing written).
+ */
+gdn_status gdn_verify_step_lazy(const gdn_config* cfg, const void* prev_x, const float* prev_alpha,
+                                const float* prev_beta, const int32_t* prev_n_keep, int32_t prev_T,
+                                const void* x, const void* conv_w, void* conv_state, float* state,
+                                const float* alpha, const float* beta, const void* z,
+                                const float* norm_w, void* out, const int32_t* slot_idx, int32_t B,
+                                int32_t T, void* postconv_out, void* stream);
+
+/*
  * gdn_gates — the gate step: alpha = exp(-softplus(a)), beta = sigmoid(b),
  * softplus(a) = log(1 + e^a), elementwise over n_tok rows of Hv values.
  * Source: "Strata PR #3226", "Root Cause & RED / GREEN Verification" — a fused

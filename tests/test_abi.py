@@ -141,3 +141,25 @@ def test_gates_mode_and_gdn_gates_host_validation(lib):
     assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[1], P[3], n, None) == 1            # alpha = b
     assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[0] + 4, P[3], n, None) == 1        # shifted a
     assert lib.gdn_gates(ctypes.byref(c), P[0], P[1], P[2], P[0], n, None) == 1            # beta = a
+
+
+def test_verify_lazy_host_validation(lib):
+    c = _cfg()
+    prev = [P[11], P[12], P[13], P[14]]                     # prev_x, prev_alpha, prev_beta, n_keep
+    v = [P[i] for i in range(10)]
+
+    def call(prev_args, prev_T, B, T, vv=v, post=None, cfg=c):
+        return lib.gdn_verify_step_lazy(ctypes.byref(cfg), *prev_args, prev_T, *vv, B, T, post, None)
+
+    assert call(prev, 4, 0, 2) == 0                          # B = 0 enqueues nothing
+    assert call(prev, 4, 4, 9) == 1                          # T > 8
+    assert call(prev, 0, 4, 2) == 1                          # prev_T < 1
+    assert call(prev, 9, 4, 2) == 1                          # prev_T > 8
+    assert call([0] + prev[1:], 4, 4, 2) == 1                # null prev_x
+    assert call(prev[:3] + [0], 4, 4, 2) == 1                # null prev_n_keep
+    assert call([P[11] + 8] + prev[1:], 4, 4, 2) == 1        # misaligned prev_x
+    bad = list(v)
+    bad[8] = P[11]                                           # out = prev_x
+    assert call(prev, 4, 4, 2, vv=bad) == 1
+    assert call(prev, 4, 4, 2, post=P[15] + 4) == 1          # misaligned post-conv output
+    assert call(prev, 4, 4, 2, cfg=_cfg(gates=3)) == 1
