@@ -303,23 +303,26 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   load8<F32>(p.norm_w, el16 * 8, nwr);
 
   // ---- post-conv activations. Item (part, head, l16) = thread: 8 channels of
-  // head `head` (0 q, 1 k, 2 v) for tokens 4 part .. 4 part + 3 (at most 96
-  // items). 16-lane groups share (part, head).
+  // head `head` (0 q, 1 k, 2 v) for the IT tokens IT part .. IT part + IT - 1
+  // (at most 96 items). 16-lane groups share (part, head).
   auto conv_heads = [&]() {
-    const int n_items = (T + 3) / 4 * 3 * 16;
+    // tokens per item: 2 for the CUDA-core variants at T = 3, 4 (96 items in
+    // place of 48, half the serial work each), else 4
+    constexpr int IT = (!TC && (NT == 3 || NT == 4)) ? 2 : 4;
+    const int n_items = (T + IT - 1) / IT * 3 * 16;
     const int64_t xb = (int64_t)b * T * C;
     const int64_t cs = (int64_t)slot * KS * C;
     const bool write_qk = p.postconv && (h % G) == 0;     // one v head of the group writes q, k
     const bool grp = tid < n_items;                       // uniform per 16 lanes
     const int l16 = tid & 15, head = (tid >> 4) % 3, part = (tid >> 4) / 3;
-    const int t0 = 4 * part;
+    const int t0 = IT * part;
     const int c = (head == 0 ? hq * D : head == 1 ? (Hk + hq) * D : (2 * Hk + h) * D) + l16 * 8;
-    Raw8<A> wr[4], rw[7];
+    Raw8<A> wr[4], rw[IT + 3];
     if (grp) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) raw_load<A>(p.conv_w, (int64_t)c * KW + 8 * q, wr[q]);
 #pragma unroll
-      for (int j = 0; j < 7; ++j) {
+      for (int j = 0; j < IT + 3; ++j) {
         const int idx = t0 + j;
         if (idx < KS) raw_load<A>(p.conv_state, cs + (int64_t)idx * C + c, rw[j]);
         else if (idx - KS < T) raw_load<A>(p.x, xb + (int64_t)(idx - KS) * C + c, rw[j]);
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
 #pragma unroll
       for (int q = 0; q < 4; ++q) raw_zero<A>(wr[q]);
 #pragma unroll
-      for (int j = 0; j < 7; ++j) raw_zero<A>(rw[j]);
+      for (int j = 0; j < IT + 3; ++j) raw_zero<A>(rw[j]);
     }
     float2 w[4][4];
 #pragma unroll
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
       for (int j = 0; j < 4; ++j) w[q][j] = make_float2(t8[j], t8[4 + j]);
     }
 #pragma unroll
-    for (int uu = 0; uu < 4; ++uu) {
+    for (int uu = 0; uu < IT; ++uu) {
       const int t = t0 + uu;
       const bool live = grp && t < T;
       float v[8];
