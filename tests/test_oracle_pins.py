@@ -423,6 +423,31 @@ def test_p8_commit_equals_prefill_of_accepted_prefix(orc, n_keep):
     assert np.array_equal(st_c, st_p)
 
 
+@pytest.mark.parametrize("k", [0, 2, 6])
+def test_p8_commit_then_next_verify_equals_longer_prefill(orc, k):
+    """Two verify windows of one sequence: the first window's k accepted drafts
+    committed, then the second window's drafts verified, equal one prefill over
+    the history, the accepted drafts and the new drafts (the rejected drafts of
+    the first window leave no trace). This is the meaning of folding a window's
+    commit into the next window's verify."""
+    n, Tp, T = 9, 6, 4
+    inp = _one_seq(n + Tp + T, 95 + k)
+    x, a, b, z = inp["x"], inp["alpha"], inp["beta"], inp["z"]
+    Hk, Hv = inp["Hk"], inp["Hv"]
+    _, cs1, st1 = _conv_then_prefill(orc, inp, x[:n], a[:n], b[:n], z[:n],
+                                     inp["conv_state"], inp["state"], 1, True)
+    w1 = slice(n, n + Tp)                                   # first window's drafts
+    w2 = slice(n + Tp, n + Tp + T)                          # second window's drafts
+    cs2, st2 = orc.commit(x[None, w1], a[None, w1], b[None, w1], inp["conv_w"], cs1, st1, [0], [k],
+                          Hk, Hv)
+    out, _, _, _ = orc.verify(x[None, w2], inp["conv_w"], cs2, st2, a[None, w2], b[None, w2],
+                              z[None, w2], inp["norm_w"], [0], Hk, Hv)
+    keep = np.r_[0:n + k, n + Tp:n + Tp + T]                # history ++ accepted ++ new drafts
+    o_full, _, _ = _conv_then_prefill(orc, inp, x[keep], a[keep], b[keep], z[keep],
+                                      inp["conv_state"], inp["state"], 1, True)
+    assert np.array_equal(out[0], o_full[n + k:])
+
+
 def test_p8_commit_rejects_out_of_range_n_keep(orc):
     inp = syn.verify_inputs(3, 4, 1, 1, "f32", seed=90)
     cs, st = orc.commit(inp["x"], inp["alpha"], inp["beta"], inp["conv_w"], inp["conv_state"],
