@@ -24,6 +24,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -180,7 +181,9 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the raw samples (a CSV); GDN_CLOCK_LOG_DIR keeps them somewhere of the user's choice
+        log_dir = os.environ.get("GDN_CLOCK_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(log_dir, f"gdn_bench_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def start(self):
         try:
