@@ -62,6 +62,27 @@ def prefill_delta_flops(n_tok, Hv):
     return n_tok * Hv * (5 * 64 * 128 * 2 + 3 * 128 * 128 * 2)
 
 
+def window_bytes(B, T, Hv, C, L, n_keep, decode=False, lazy=False):
+    """Algorithmic HBM bytes of one window over L layers (bf16 activations, f32
+    state and gates): "verify" for the verify launches (decode: the commit-all
+    verify, which also writes S and conv_state; lazy: the verify that first
+    commits the previous window's n_keep[b] tokens) and "commit" for the batched
+    commit of the accepted prefixes n_keep[b]."""
+    per_seq_state = Hv * D * D * 4
+    conv_rows = 3 * C * 2
+    drafts = B * T * (C * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + C * 4 * 2   # x, z, out, gates, conv_w
+    accepted = [int(n) for n in n_keep if n > 0]
+    if lazy:
+        verify = B * per_seq_state + B * conv_rows + drafts + sum(
+            per_seq_state + conv_rows + n * (C * 2 + 2 * Hv * 4) for n in accepted)
+        return {"verify": L * verify, "commit": 0}
+    rw = 2 if decode else 1
+    verify = B * per_seq_state * rw + B * conv_rows * rw + drafts
+    commit = 0 if decode else sum(2 * per_seq_state + 2 * conv_rows + n * (C * 2 + 2 * Hv * 4)
+                                  + C * 4 * 2 for n in accepted)
+    return {"verify": L * verify, "commit": L * commit}
+
+
 def state_bytes_per_layer(Hv, C, dv=D, dk=D, conv_rows=3, state_es=4, conv_es=4):
     """Bytes of one layer's recurrent state plus conv_state for one sequence."""
     return Hv * dv * dk * state_es + C * conv_rows * conv_es
@@ -359,24 +380,8 @@ class StepWorkload:
         # read-only verify: one cooperative launch per layer, then one commit launch
         self.launches_per_step = L if (decode or self.lazy) else L + 1
         self.ws = None if decode else G.verify_workspace(self.cfg, B, T, device)
-        nk = self.n_keep.cpu().numpy()
-        S_head = D * D * 4
-        per_seq_state = Hv * S_head
-        self.bytes = {
-            "verify": L * (B * per_seq_state * (2 if decode else 1)
-                           + B * 3 * C * 2 * (2 if decode else 1)
-                           + B * T * (C * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + C * 4 * 2),
-            "commit": 0 if decode else L * int(
-                sum(2 * per_seq_state + 2 * 3 * C * 2 + n * (C * 2 + 2 * Hv * 4) + C * 4 * 2
-                    for n in nk if n > 0)),
-        }
-        if self.lazy:                    # one pass: S read once, written where n_keep > 0
-            self.bytes = {
-                "verify": L * int(B * per_seq_state + B * 3 * C * 2
-                                  + sum(per_seq_state + 3 * C * 2 + n * (C * 2 + 2 * Hv * 4)
-                                        for n in nk if n > 0)
-                                  + B * T * (C * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + C * 4 * 2),
-                "commit": 0}
+        self.bytes = window_bytes(B, T, Hv, C, L, self.n_keep.cpu().numpy(), decode=decode,
+                                  lazy=self.lazy)
 
     def reset(self):
         pass                                                # state evolution does not change work
