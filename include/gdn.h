@@ -15,7 +15,14 @@
  *     initial/final conv_state rows of exact chunks ("Merged ...", "New issue #305");
  *     exact causal-conv chunk descriptors ("Before starting").
  *   "Strata PR #3226" — speculative verify over T draft tokens, the output norm,
- *     and the one-call commit of conv_state and state for all layers ("Summary").
+ *     and the one-call commit of conv_state and state for all layers ("Summary");
+ *     the fused gate kernel ("Root Cause & RED / GREEN Verification") and the
+ *     forward that commits inside itself ("Problem and result").
+ *
+ * Entry points: gdn_conv_fwd, gdn_postconv_norm, gdn_delta_prefill,
+ * gdn_verify_step (and gdn_verify_step_noalloc), gdn_commit_layers,
+ * gdn_verify_step_lazy, gdn_gates; gdn_verify_workspace_bytes and
+ * gdn_status_string are helpers.
  *
  * Conventions shared by every entry point
  *   - head_dim d = 128 and conv width 4 are the only supported values.
