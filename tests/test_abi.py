@@ -163,3 +163,13 @@ def test_verify_lazy_host_validation(lib):
     assert call(prev, 4, 4, 2, vv=bad) == 1
     assert call(prev, 4, 4, 2, post=P[15] + 4) == 1          # misaligned post-conv output
     assert call(prev, 4, 4, 2, cfg=_cfg(gates=3)) == 1
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No fallback: with libgdn.so absent the binding raises instead of computing
+    anything another way."""
+    from gated_deltanet_linear_12_gb300 import build, gdn
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "libgdn.so"))
+    monkeypatch.setattr(gdn, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        gdn.load()
