@@ -173,3 +173,12 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gdn, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         gdn.load()
+
+
+def test_build_compiles_every_cuda_source():
+    """Every translation unit under csrc/ is in the build, and every header it lists exists."""
+    from gated_deltanet_linear_12_gb300 import build
+    cu = sorted(f for f in os.listdir(build.CSRC) if f.endswith(".cu"))
+    assert sorted(build.SOURCES) == cu
+    for h in build.HEADERS:
+        assert os.path.exists(os.path.join(build.CSRC, h))
