@@ -304,7 +304,9 @@ gdn_status gdn_verify_step_lazy(const gdn_config* cfg, const void* prev_x, const
 gdn_status gdn_gates(const gdn_config* cfg, const float* a, const float* b, float* alpha,
                      float* beta, int64_t n_tok, void* stream);
 
-/* Static description of a status code. */
+/* Static description of a status code (never NULL; "unknown status" for a value
+ * outside gdn_status; the string is owned by the library). The pages have no
+ * counterpart: it exists for callers' error messages. */
 const char* gdn_status_string(gdn_status s);
 
 #ifdef __cplusplus
