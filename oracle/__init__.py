@@ -6,7 +6,7 @@ C++, compiled with g++ -O2 -ffp-contract=off) through ctypes. It shares no code
 with the GPU library and never calls it.
 
 Every routine takes ``prec`` = "f64" (the precision reference) or "f32" (the
-float instantiation, which follows the documented float orders bit for bit).
+same plain definitions evaluated in single precision).
 Activation inputs may be float32 arrays or bfloat16 bit patterns (uint16);
 they are widened exactly before the call. Results are returned unrounded
 unless stated.
@@ -139,7 +139,7 @@ def gated_rmsnorm(o, z, w, *, eps=1e-6, prec="f64"):
 
 
 def silu(v, prec="f64"):
-    """SiLU y / (1 + exp(-y)) elementwise (f32: the documented exp scheme)."""
+    """SiLU y / (1 + exp(-y)) elementwise, with the library exp of the precision."""
     vw = widen(v, prec).copy()
     f = _fn("oracle_silu", prec)
     f.restype = None
@@ -193,12 +193,13 @@ def prefill(qkv, alpha, beta, z, norm_w, state, slot_idx, cu_seqlens, has_init, 
 
 
 def verify(x, conv_w, conv_state, state, alpha, beta, z, norm_w, slot_idx, Hk, Hv, *,
-           q_scale=1.0, eps=1e-6, round_act=True, commit_all=False, prec="f64",
-           want_raw=False, act32=False):
+           q_scale=1.0, eps=1e-6, round_act=False, commit_all=False, prec="f64",
+           want_raw=False):
     """Speculative verify of T draft tokens (x [B][T][C]).
 
-    act32: compute the post-conv activations with the float instantiation
-    (the float order the GPU follows) whatever prec is.
+    round_act: round the post-conv activations to bfloat16 before the
+    recurrence (activations that went through memory). The fused verify,
+    commit and decode kernels keep them on chip unrounded, hence the default.
 
     Returns (out [B][T][Hv*D], postconv [B][T][C], conv_state', state'[, o_raw]);
     the states are unchanged copies unless commit_all.
@@ -216,14 +217,15 @@ def verify(x, conv_w, conv_state, state, alpha, beta, z, norm_w, slot_idx, Hk, H
     f(_p(xw), _p(widen(conv_w, prec)), _p(cs), _p(st), _p(widen(alpha, prec)),
       _p(widen(beta, prec)), _p(widen(z, prec)), _p(widen(norm_w, prec)), _p(_i32(slot_idx)),
       ctypes.c_int(B), ctypes.c_int(Tn), ctypes.c_int(Hk), ctypes.c_int(Hv),
-      _c_t(prec)(q_scale), _c_t(prec)(eps), ctypes.c_int(int(round_act)), ctypes.c_int(int(act32)),
+      _c_t(prec)(q_scale), _c_t(prec)(eps), ctypes.c_int(int(round_act)),
       ctypes.c_int(int(commit_all)), _p(out), _p(pc), _p(raw))
     return (out, pc, cs, st, raw) if want_raw else (out, pc, cs, st)
 
 
 def commit(x, alpha, beta, conv_w, conv_state, state, slot_idx, n_keep, Hk, Hv, *,
-           eps=1e-6, round_act=True, prec="f64", act32=False):
-    """Commit the accepted prefix n_keep[b] of one layer. Returns (conv_state', state')."""
+           eps=1e-6, round_act=False, prec="f64"):
+    """Commit the accepted prefix n_keep[b] of one layer (round_act as for
+    verify). Returns (conv_state', state')."""
     xw = widen(x, prec)
     B, Tn, C = xw.shape
     cs = widen(conv_state, prec).copy()
@@ -232,6 +234,5 @@ def commit(x, alpha, beta, conv_w, conv_state, state, slot_idx, n_keep, Hk, Hv, 
     f.restype = None
     f(_p(xw), _p(widen(alpha, prec)), _p(widen(beta, prec)), _p(widen(conv_w, prec)), _p(cs),
       _p(st), _p(_i32(slot_idx)), _p(_i32(n_keep)), ctypes.c_int(B), ctypes.c_int(Tn),
-      ctypes.c_int(Hk), ctypes.c_int(Hv), _c_t(prec)(eps), ctypes.c_int(int(round_act)),
-      ctypes.c_int(int(act32)))
+      ctypes.c_int(Hk), ctypes.c_int(Hv), _c_t(prec)(eps), ctypes.c_int(int(round_act)))
     return cs, st

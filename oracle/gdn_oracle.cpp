@@ -4,8 +4,10 @@
 // by the tests and by the benchmark's CPU-baseline leg to check and time the
 // GPU library. It shares no code with the GPU library and is never on the
 // product path. One template body serves float and double; the double
-// instantiation is the precision reference, the float one follows the
-// documented float orders exactly where the GPU is required to be bitwise.
+// instantiation is the precision reference, the float one evaluates the same
+// plain definitions in single precision (each product and each sum rounded
+// separately, the library exp) so that its own error can be bounded against
+// the double one.
 //
 // Build: g++ -std=c++17 -O2 -ffp-contract=off -fPIC -shared (no fast-math, no
 // FMA contraction: every product and every sum below is rounded separately).
@@ -46,7 +48,6 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <type_traits>
 #include <vector>
 
 namespace {
@@ -69,63 +70,8 @@ template <class T> T round_bf16(T v) {
   return std::ldexp(r, e - 8);
 }
 
-// SiLU of the float instantiation, by published schemes whose every step is a
-// correctly rounded IEEE operation (or an exact integer operation on the bits),
-// so that any IEEE machine following the same steps gets the same bits (this
-// fixes how post-conv activations round to bf16 on every implementation):
-//   t = e^-|y| : Cody & Waite's reduction -|y| = n ln2 + r (n the nearest
-//                integer to -|y| log2 e; ln 2 split in a 16-bit high part, so
-//                n * high is exact, and a low part; the argument clamped at
-//                -86 so that 2^n p stays normal), then a degree-5 polynomial
-//                of e^r in Horner form (coefficients: the near-minimax
-//                relative fit on |r| <= ln2/2 rounded to float, relative error
-//                1.1e-7), scaled by 2^n by adding n to the exponent field;
-//   s = 1/(1 + t) on [1, 2] : Newton-Raphson from the quadratic start
-//                2.1212120 - 1.4545449 d + 0.32323205 d^2 (its near-minimax
-//                relative fit, error <= 0.0102), two iterations
-//                x <- x + x (1 - d x);
-//   sigmoid(y) = s for y >= 0, t s for y < 0;   silu(y) = y sigmoid(y).
-// The whole scheme is within 6 ulp of silu over [-86, 90]. The double
-// instantiation is the plain y / (1 + exp(-y)). Both are pinned against the
-// library exp.
-inline float exp_neg_cw(float a) {          // e^a for a <= 0
-  a = std::fmax(a, -86.0f);
-  // n = nearbyint(a log2 e) of the exact product: one fused multiply-add with
-  // 1.5 * 2^23 rounds it to an integer, the subtraction is exact
-  const float n = std::fma(a, 1.44269504088896341f, 12582912.0f) - 12582912.0f;
-  float r = std::fma(-n, 0.693145751953125f, a);                   // ln2 high part
-  r = std::fma(-n, 1.42860682030941723212e-6f, r);                 // ln2 low part
-  float p = 0.008297654800117016f;
-  p = std::fma(p, r, 0.04191538318991661f);
-  p = std::fma(p, r, 0.16667574644088745f);
-  p = std::fma(p, r, 0.49998894333839417f);
-  p = std::fma(p, r, 0.9999997019767761f);
-  p = std::fma(p, r, 1.0000001192092896f);
-  uint32_t bits;                                                   // p * 2^n, exact
-  std::memcpy(&bits, &p, 4);
-  bits += static_cast<uint32_t>(static_cast<int32_t>(n)) << 23;
-  std::memcpy(&p, &bits, 4);
-  return p;
-}
-
-inline float recip_12(float d) {            // 1/d for d in [1, 2]
-  float x = std::fma(std::fma(0.3232320547103882f, d, -1.4545449018478394f), d, 2.1212120056152344f);
-  for (int i = 0; i < 2; ++i) {
-    const float e = std::fma(-d, x, 1.0f);
-    x = std::fma(x, e, x);
-  }
-  return x;
-}
-
-inline float silu_f32(float y) {
-  const float t = exp_neg_cw(-std::fabs(y));
-  const float s = recip_12(1.0f + t);
-  const float sig = y >= 0.0f ? s : t * s;
-  return y * sig;
-}
-
+// SiLU, y / (1 + e^-y), with the library exponential, in the oracle's type.
 template <class T> T silu(T y) { return y / (T(1) + std::exp(-y)); }
-template <> inline float silu<float>(float y) { return silu_f32(y); }
 
 // The canonical sum-of-squares tree over 128 values: 16 groups of 8
 // contiguous channels; inside a group the strides 4, 2, 1 are folded, then the
@@ -168,13 +114,11 @@ struct Geo {
 };
 
 // Causal depthwise conv of one channel's padded column xp (3 state rows then
-// the tokens): y[t] = sum_j w[j] * xp[t + j], accumulated in tap order with
-// fused multiply-adds (one rounding per tap).
+// the tokens): y[t] = sum_j w[j] * xp[t + j], summed from zero in tap order,
+// each product and each sum rounded on its own (no fused multiply-add).
 template <class T> T conv_tap(const T* w, const T* xp_t) {
-  T acc = w[0] * xp_t[0];
-  acc = std::fma(w[1], xp_t[1], acc);
-  acc = std::fma(w[2], xp_t[2], acc);
-  acc = std::fma(w[3], xp_t[3], acc);
+  T acc = T(0);
+  for (int j = 0; j < KW; ++j) acc = acc + w[j] * xp_t[j];
   return acc;
 }
 
@@ -398,21 +342,14 @@ void prefill(const T* qkv, const T* alpha, const T* beta, const T* z, const T* n
 }
 
 // Post-conv activations of T draft tokens of batch entry b from its
-// conv_state, rounded to the activation type when round_act (they are stored
-// activations in every phase).
-// act32: compute the activations with the float instantiation (the order the
-// GPU follows bit for bit) and widen them, whatever T is.
+// conv_state; rounded to the activation type when round_act (the reading of
+// the verify / commit phases is that the fused kernels feed the recurrence
+// unrounded values, so the tests pass round_act = 0; 1 models activations
+// that went through memory, as the prefill's do).
 template <class T>
 void draft_activations(const Geo& g, const T* xb, int Tn, const T* w, const T* st, T eps,
-                       int round_act, int act32, T* qkv) {
+                       int round_act, T* qkv) {
   const int64_t n = (int64_t)Tn * g.C;
-  if (act32 && !std::is_same<T, float>::value) {
-    std::vector<float> xf(xb, xb + n), wf(w, w + (int64_t)g.C * KW), sf(st, st + (int64_t)KS * g.C);
-    std::vector<float> yf(n);
-    conv_block<float>(g, xf.data(), Tn, wf.data(), sf.data(), 1, 1, (float)eps, yf.data());
-    for (int64_t i = 0; i < n; ++i) qkv[i] = (T)(round_act ? round_bf16(yf[i]) : yf[i]);
-    return;
-  }
   conv_block(g, xb, Tn, w, st, 1, 1, eps, qkv);
   if (round_act)
     for (int64_t i = 0; i < n; ++i) qkv[i] = round_bf16(qkv[i]);
@@ -424,8 +361,7 @@ void draft_activations(const Geo& g, const T* xb, int Tn, const T* w, const T* s
 template <class T>
 void verify(const T* x, const T* w, T* conv_state, T* state, const T* alpha, const T* beta,
             const T* z, const T* norm_w, const int32_t* slot_idx, int B, int Tn, int Hk, int Hv,
-            T q_scale, T eps, int round_act, int act32, int commit_all, T* out, T* postconv,
-            T* o_raw) {
+            T q_scale, T eps, int round_act, int commit_all, T* out, T* postconv, T* o_raw) {
   Geo g(Hk, Hv);
   const int64_t HvD = (int64_t)Hv * D, SS = (int64_t)Hv * D * D;
   std::vector<T> qkv((size_t)Tn * g.C), S(SS), tail((size_t)KS * g.C);
@@ -434,7 +370,7 @@ void verify(const T* x, const T* w, T* conv_state, T* state, const T* alpha, con
     if (slot < 0) continue;
     const T* xb = x + (int64_t)b * Tn * g.C;
     T* st = conv_state + (int64_t)slot * KS * g.C;
-    draft_activations(g, xb, Tn, w, st, eps, round_act, act32, qkv.data());
+    draft_activations(g, xb, Tn, w, st, eps, round_act, qkv.data());
     if (postconv) std::memcpy(postconv + (int64_t)b * Tn * g.C, qkv.data(), sizeof(T) * qkv.size());
     std::memcpy(S.data(), state + slot * SS, sizeof(T) * SS);
     recurrence_seq(g, qkv.data(), alpha + (int64_t)b * Tn * Hv, beta + (int64_t)b * Tn * Hv,
@@ -456,7 +392,7 @@ void verify(const T* x, const T* w, T* conv_state, T* state, const T* alpha, con
 template <class T>
 void commit(const T* x, const T* alpha, const T* beta, const T* w, T* conv_state, T* state,
             const int32_t* slot_idx, const int32_t* n_keep, int B, int Tn, int Hk, int Hv,
-            T eps, int round_act, int act32) {
+            T eps, int round_act) {
   Geo g(Hk, Hv);
   const int64_t SS = (int64_t)Hv * D * D;
   std::vector<T> qkv((size_t)Tn * g.C), S(SS), tail((size_t)KS * g.C);
@@ -466,7 +402,7 @@ void commit(const T* x, const T* alpha, const T* beta, const T* w, T* conv_state
     if (slot < 0 || n <= 0 || n > Tn) continue;
     const T* xb = x + (int64_t)b * Tn * g.C;
     T* st = conv_state + (int64_t)slot * KS * g.C;
-    draft_activations(g, xb, n, w, st, eps, round_act, act32, qkv.data());
+    draft_activations(g, xb, n, w, st, eps, round_act, qkv.data());
     std::memcpy(S.data(), state + slot * SS, sizeof(T) * SS);
     recurrence_seq<T>(g, qkv.data(), alpha + (int64_t)b * Tn * Hv, beta + (int64_t)b * Tn * Hv,
                       nullptr, nullptr, S.data(), n, T(1), eps, nullptr, nullptr);
@@ -510,19 +446,19 @@ void commit(const T* x, const T* alpha, const T* beta, const T* w, T* conv_state
   }                                                                                             \
   ORACLE_EXPORT void oracle_verify_##SUF(const T* x, const T* w, T* conv_state, T* state,      \
       const T* alpha, const T* beta, const T* z, const T* norm_w, const int32_t* slot_idx,      \
-      int B, int Tn, int Hk, int Hv, T q_scale, T eps, int round_act, int act32, int commit_all, \
-      T* out, T* postconv, T* o_raw) {                                                          \
+      int B, int Tn, int Hk, int Hv, T q_scale, T eps, int round_act, int commit_all, T* out,   \
+      T* postconv, T* o_raw) {                                                                  \
     verify<T>(x, w, conv_state, state, alpha, beta, z, norm_w, slot_idx, B, Tn, Hk, Hv,         \
-              q_scale, eps, round_act, act32, commit_all, out, postconv, o_raw);                \
+              q_scale, eps, round_act, commit_all, out, postconv, o_raw);                       \
   }                                                                                             \
   ORACLE_EXPORT void oracle_gates_##SUF(const T* a, const T* b, int64_t n, T* alpha, T* beta) { \
     gates<T>(a, b, n, alpha, beta);                                                             \
   }                                                                                             \
   ORACLE_EXPORT void oracle_commit_##SUF(const T* x, const T* alpha, const T* beta,            \
       const T* w, T* conv_state, T* state, const int32_t* slot_idx, const int32_t* n_keep,      \
-      int B, int Tn, int Hk, int Hv, T eps, int round_act, int act32) {                         \
+      int B, int Tn, int Hk, int Hv, T eps, int round_act) {                                    \
     commit<T>(x, alpha, beta, w, conv_state, state, slot_idx, n_keep, B, Tn, Hk, Hv, eps,       \
-              round_act, act32);                                                                \
+              round_act);                                                                       \
   }
 
 ORACLE_INSTANTIATE(float, f32)

@@ -22,14 +22,12 @@ MUTANTS = {
                          "for (int j = 0; j < D; ++j) u = u + S[(int64_t)j * D + i] * k[j];"),
     "output_uses_k": ("for (int j = 0; j < D; ++j) acc = acc + row[j] * q[j];",
                       "for (int j = 0; j < D; ++j) acc = acc + row[j] * k[j];"),
-    "taps_reversed": ("T acc = w[0] * xp_t[0];\n  acc = std::fma(w[1], xp_t[1], acc);\n"
-                      "  acc = std::fma(w[2], xp_t[2], acc);\n  acc = std::fma(w[3], xp_t[3], acc);",
-                      "T acc = w[3] * xp_t[0];\n  acc = std::fma(w[2], xp_t[1], acc);\n"
-                      "  acc = std::fma(w[1], xp_t[2], acc);\n  acc = std::fma(w[0], xp_t[3], acc);"),
-    "exp_poly_term_dropped": ("  p = std::fma(p, r, 0.16667574644088745f);\n", "  p = std::fma(p, r, 0.0f);\n"),
-    "exp_ln2_low_dropped": ("  r = std::fma(-n, 1.42860682030941723212e-6f, r);", "  r = r;"),
-    "recip_one_iteration": ("  for (int i = 0; i < 2; ++i) {", "  for (int i = 0; i < 1; ++i) {"),
-    "sigmoid_branch_swapped": ("const float sig = y >= 0.0f ? s : t * s;", "const float sig = y >= 0.0f ? t * s : s;"),
+    "taps_reversed": ("for (int j = 0; j < KW; ++j) acc = acc + w[j] * xp_t[j];",
+                      "for (int j = 0; j < KW; ++j) acc = acc + w[KW - 1 - j] * xp_t[j];"),
+    "conv_drops_current_tap": ("for (int j = 0; j < KW; ++j) acc = acc + w[j] * xp_t[j];",
+                               "for (int j = 0; j < KW - 1; ++j) acc = acc + w[j] * xp_t[j];"),
+    "silu_without_input": ("template <class T> T silu(T y) { return y / (T(1) + std::exp(-y)); }",
+                           "template <class T> T silu(T y) { return T(1) / (T(1) + std::exp(-y)); }"),
     "tail_off_by_one": ("int64_t idx = n + r;", "int64_t idx = n + r - 1;"),
     "tree_adjacent_pairs": ("T p0 = e[0] + e[4], p1 = e[1] + e[5], p2 = e[2] + e[6], p3 = e[3] + e[7];",
                             "T p0 = e[0] + e[1], p1 = e[4] + e[5], p2 = e[2] + e[3], p3 = e[6] + e[7];"),

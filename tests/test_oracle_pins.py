@@ -4,9 +4,9 @@ Each test fixes one part of the oracle to something other than itself, so
 that a plausible slip (a dropped term, a wrong sign or index, a transposed
 operand, a changed reduction order) fails at least one of them:
 
-  P1  conv = exact 4-term sums (rational arithmetic) within 4 roundings;
-      has_init=0 = zero-padded np.convolve; SiLU = y / (1 + e^-y), the f32 exp
-      scheme within 2 ulp of the library exp
+  P1  conv = exact 4-term sums (rational arithmetic) within 7 roundings;
+      has_init=0 = zero-padded np.convolve; SiLU = y / (1 + e^-y), the float
+      instantiation within 4 ulp of the double one
   P2  delta conv weights: pass-through of the current token and a 3-row shift
       that reads the conv_state (pins tap orientation and state row order)
   P3  L2 norm: unit norm, tree sum within the pairwise bound of the exact sum,
@@ -56,8 +56,8 @@ def test_p1_conv_explicit_sums(orc):
             for t in range(n):
                 terms = [Fraction(float(w[c, j])) * Fraction(float(col[t + j])) for j in range(4)]
                 exact = sum(terms)
-                # one rounded product and three fused multiply-adds: 4 roundings
-                bound = 4 * 2.0 ** -53 * float(sum(abs(v) for v in terms))
+                # four rounded products and three rounded sums: 7 roundings
+                bound = 7 * 2.0 ** -53 * float(sum(abs(v) for v in terms))
                 assert abs(Fraction(float(y[t0 + t, c])) - exact) <= Fraction(bound)
             # committed state = last three rows of the padded column
             assert [st[slot, r, c] for r in range(3)] == col[n:n + 3]
@@ -86,22 +86,16 @@ def test_p1_silu_applied_after_conv(orc):
     np.testing.assert_allclose(post, want, rtol=1e-15, atol=0)
 
 
-def test_p1_f32_silu_scheme_within_six_ulp(orc):
-    """The float instantiation's SiLU (exp by Cody-Waite + a degree-5 polynomial,
-    reciprocal by Newton-Raphson) against y / (1 + math.exp(-y)) in double."""
-    ys = np.concatenate([np.linspace(-90.0, 90.0, 400001, dtype=np.float32),
+def test_p1_f32_silu_within_four_ulp(orc):
+    """The float instantiation's SiLU (library expf, a rounded add and divide)
+    against y / (1 + math.exp(-y)) in double."""
+    ys = np.concatenate([np.linspace(-87.0, 88.0, 400001, dtype=np.float32),
                          np.float32([0.0, -0.0, 1e-8, -1e-8, 0.34657359, -0.34657359, 1e-30])])
     got = orc.silu(ys, prec="f32").astype(np.float64)
-    worst = 0.0
     for y, g in zip(ys[::37].astype(np.float64), got[::37]):
         want = y / (1.0 + math.exp(-y))
-        if y < -86.0:                          # exp argument clamped: saturated, negligible
-            assert abs(g) < 3e-35 and abs(want) < 3e-35
-            continue
         ulp = float(np.spacing(np.float32(abs(want))))
-        worst = max(worst, abs(g - want) / ulp)
-        assert abs(g - want) <= 6 * ulp, (y, g, want)
-    assert worst > 0.0                         # it is not an exact copy of the library
+        assert abs(g - want) <= 4 * ulp, (y, g, want)
 
 
 # ------------------------------------------------------------------ P2
@@ -376,55 +370,59 @@ def test_p8_split_prefill_equals_one_prefill(orc):
     assert np.array_equal(st2, st_full)
 
 
-@pytest.mark.parametrize("T", [1, 3, 8])
-def test_p8_prefill_then_verify_equals_longer_prefill(orc, T):
+@pytest.mark.parametrize("T,ra", [(1, False), (3, False), (8, False), (3, True), (8, True)])
+def test_p8_prefill_then_verify_equals_longer_prefill(orc, T, ra):
+    """ra: the activations are rounded to bfloat16 on every side (stored rows)
+    or on none (kept on chip); the identity holds bitwise either way."""
     n = 13
     inp = _one_seq(n + T, 72 + T)
     x, a, b, z = inp["x"], inp["alpha"], inp["beta"], inp["z"]
     Hk, Hv = inp["Hk"], inp["Hv"]
     o_full, cs_full, st_full = _conv_then_prefill(orc, inp, x, a, b, z, inp["conv_state"],
-                                                  inp["state"], 1, True)
+                                                  inp["state"], 1, ra)
     _, cs1, st1 = _conv_then_prefill(orc, inp, x[:n], a[:n], b[:n], z[:n],
-                                     inp["conv_state"], inp["state"], 1, True)
+                                     inp["conv_state"], inp["state"], 1, ra)
     out, _, cs_v, st_v = orc.verify(x[None, n:], inp["conv_w"], cs1, st1, a[None, n:],
-                                    b[None, n:], z[None, n:], inp["norm_w"], [0], Hk, Hv)
+                                    b[None, n:], z[None, n:], inp["norm_w"], [0], Hk, Hv,
+                                    round_act=ra)
     assert np.array_equal(out[0], o_full[n:])
     assert np.array_equal(cs_v, cs1) and np.array_equal(st_v, st1)     # verify is read-only
     # commit of every draft token lands on the longer prefill's states
     for kind in ("commit", "commit_all"):
         if kind == "commit":
             cs_c, st_c = orc.commit(x[None, n:], a[None, n:], b[None, n:], inp["conv_w"], cs1, st1,
-                                    [0], [T], Hk, Hv)
+                                    [0], [T], Hk, Hv, round_act=ra)
         else:
             _, _, cs_c, st_c = orc.verify(x[None, n:], inp["conv_w"], cs1, st1, a[None, n:],
                                           b[None, n:], z[None, n:], inp["norm_w"], [0], Hk, Hv,
-                                          commit_all=True)
+                                          commit_all=True, round_act=ra)
         assert np.array_equal(cs_c, cs_full)
         assert np.array_equal(st_c, st_full)
 
 
-@pytest.mark.parametrize("n_keep", [0, 1, 2, 3, 5, 8])
-def test_p8_commit_equals_prefill_of_accepted_prefix(orc, n_keep):
+@pytest.mark.parametrize("n_keep,ra", [(0, False), (1, False), (2, False), (3, False),
+                                        (5, False), (8, False), (2, True), (8, True)])
+def test_p8_commit_equals_prefill_of_accepted_prefix(orc, n_keep, ra):
     T, n = 8, 9
     inp = _one_seq(n + T, 80 + n_keep)
     x, a, b, z = inp["x"], inp["alpha"], inp["beta"], inp["z"]
     Hk, Hv = inp["Hk"], inp["Hv"]
     _, cs1, st1 = _conv_then_prefill(orc, inp, x[:n], a[:n], b[:n], z[:n],
-                                     inp["conv_state"], inp["state"], 1, True)
+                                     inp["conv_state"], inp["state"], 1, ra)
     cs_c, st_c = orc.commit(x[None, n:], a[None, n:], b[None, n:], inp["conv_w"], cs1, st1, [0],
-                            [n_keep], Hk, Hv)
+                            [n_keep], Hk, Hv, round_act=ra)
     if n_keep == 0:
         assert np.array_equal(cs_c, cs1) and np.array_equal(st_c, st1)
         return
     m = n + n_keep
     _, cs_p, st_p = _conv_then_prefill(orc, inp, x[:m], a[:m], b[:m], z[:m],
-                                       inp["conv_state"], inp["state"], 1, True)
+                                       inp["conv_state"], inp["state"], 1, ra)
     assert np.array_equal(cs_c, cs_p)
     assert np.array_equal(st_c, st_p)
 
 
-@pytest.mark.parametrize("k", [0, 2, 6])
-def test_p8_commit_then_next_verify_equals_longer_prefill(orc, k):
+@pytest.mark.parametrize("k,ra", [(0, False), (2, False), (6, False), (2, True)])
+def test_p8_commit_then_next_verify_equals_longer_prefill(orc, k, ra):
     """Two verify windows of one sequence: the first window's k accepted drafts
     committed, then the second window's drafts verified, equal one prefill over
     the history, the accepted drafts and the new drafts (the rejected drafts of
@@ -435,16 +433,16 @@ def test_p8_commit_then_next_verify_equals_longer_prefill(orc, k):
     x, a, b, z = inp["x"], inp["alpha"], inp["beta"], inp["z"]
     Hk, Hv = inp["Hk"], inp["Hv"]
     _, cs1, st1 = _conv_then_prefill(orc, inp, x[:n], a[:n], b[:n], z[:n],
-                                     inp["conv_state"], inp["state"], 1, True)
+                                     inp["conv_state"], inp["state"], 1, ra)
     w1 = slice(n, n + Tp)                                   # first window's drafts
     w2 = slice(n + Tp, n + Tp + T)                          # second window's drafts
     cs2, st2 = orc.commit(x[None, w1], a[None, w1], b[None, w1], inp["conv_w"], cs1, st1, [0], [k],
-                          Hk, Hv)
+                          Hk, Hv, round_act=ra)
     out, _, _, _ = orc.verify(x[None, w2], inp["conv_w"], cs2, st2, a[None, w2], b[None, w2],
-                              z[None, w2], inp["norm_w"], [0], Hk, Hv)
+                              z[None, w2], inp["norm_w"], [0], Hk, Hv, round_act=ra)
     keep = np.r_[0:n + k, n + Tp:n + Tp + T]                # history ++ accepted ++ new drafts
     o_full, _, _ = _conv_then_prefill(orc, inp, x[keep], a[keep], b[keep], z[keep],
-                                      inp["conv_state"], inp["state"], 1, True)
+                                      inp["conv_state"], inp["state"], 1, ra)
     assert np.array_equal(out[0], o_full[n + k:])
 
 
@@ -486,7 +484,7 @@ def test_p10_float_against_double(orc):
             inp["has_init_conv"], inp["Hk"], inp["Hv"])
     y64, _ = orc.conv_fwd(*args, prec="f64")
     y32, _ = orc.conv_fwd(*args, prec="f32")
-    # pre-activations: error of the f32 order against the conditioning of the
+    # pre-activations: error of the f32 sum against the conditioning of the
     # 4-term sum (sum of |w_j x_j|), 10x under the 1e-5 bound
     pre64, _ = orc.conv_fwd(*args, silu=False, l2norm=False, prec="f64")
     pre32, _ = orc.conv_fwd(*args, silu=False, l2norm=False, prec="f32")
