@@ -1,17 +1,19 @@
 """Benchmark of the GDN token-mixing path on GB300.
 
-Default workload (N=1): varlen prefill bf16 — 8 sequences with lengths drawn
-uniformly from [1, 2048], q/k 16 heads and v 32 heads of 128 (C = 8192),
-conv width 4, half the sequences carrying an initial conv_state and state,
-exact 64-token chunks. One step = one layer's pass of the whole prefill path:
-gdn_conv_fwd (conv + SiLU + q/k L2 norm) then gdn_delta_prefill (chunked
-delta rule + z-gated RMSNorm), through the C ABI.
+Headline workload (N=1, no --workload): high-batch decode bf16 — 256 sequences,
+one token each, 36 layers with q/k 16 heads and v 32 heads of 128 (C = 8192),
+conv width 4, every token accepted: one step = one decode window, 36
+gdn_verify_step calls with GDN_VERIFY_COMMIT_ALL (conv + SiLU + L2 norm, the
+delta rule on the 18 GiB f32 state pool, z-gated RMSNorm, state and conv_state
+advanced in place), through the C ABI. The same run then measures every other
+workload as a further entry ("workloads"): tiny-f32, varlen-prefill-bf16
+(gdn_conv_fwd + gdn_delta_prefill), spec-verify-bf16 at T = 1, 4, 8 (36 verify
+launches + 1 batched commit per window) and long-prefill-bf16. Each entry has
+its own roofline, kernel table, end-to-end number, clocks and CPU baseline.
 
 metric: GDN tokens/s per layer (whole job: tokens of all ranks / max time).
-Other workloads (--workload): tiny-f32, long-prefill-bf16, spec-verify-bf16
-(36 verify launches + 1 batched commit per window), spec-verify-bf16-h48 (the same
-window for one sequence with Hk = 16, Hv = 48), decode-bf16 (36 layers,
-T = 1, every token accepted).
+--workload NAME times one workload only (also spec-verify-bf16-h48: the verify
+window of one sequence with Hk = 16, Hv = 48).
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference];
 for N > 1 under torch.distributed.run, one rank per GPU, replicas of the same
@@ -462,17 +464,35 @@ class StepWorkload:
 
 
 # ----------------------------------------------------------------------------- CPU baseline
-def cpu_baseline(name, max_tokens=4096, gates="activated"):
-    """The oracle as it stands (single thread) on a bounded sample of the
-    workload: the first max_tokens tokens of its sequences, conv (+ the gate
-    step for raw gates) + recurrence."""
+def host_info():
+    """The host the CPU baseline ran on: logical CPUs and the CPU model."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+def cpu_baseline(name, max_tokens=None, gates="activated"):
+    """The oracle as it stands (single thread) on the prefill workload: its
+    sequences in full, or the first max_tokens tokens of them; conv (+ the gate
+    step for raw gates) + token-by-token recurrence in f64."""
     import oracle as orc
     raw = gates == "raw"
     inp = syn.workload_prefill(name, gate_form="raw" if raw else None)
     lens, cu = inp["lens"], inp["cu_seqlens"]
+    cap = int(inp["n_tok"]) if max_tokens is None else max_tokens
     keep, tot = [], 0
     for s in range(inp["n_seq"]):
-        n = int(min(lens[s], max_tokens - tot))
+        n = int(min(lens[s], cap - tot))
         if n <= 0:
             break
         keep.append((s, n))
@@ -492,45 +512,186 @@ def cpu_baseline(name, max_tokens=4096, gates="activated"):
                 inp["state"], inp["slot_idx"][ss], cu2, inp["has_init_state"][ss], inp["Hk"],
                 inp["Hv"])
     dt = time.perf_counter() - t0
+    full = tot == int(inp["n_tok"])
+    what = (f"the whole {name} workload ({tot} tokens, {len(keep)} sequences)" if full else
+            f"first {tot} tokens of {len(keep)} sequence(s) of the {name} workload")
     return {"value": tot / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {tot} tokens of {len(keep)} sequence(s) of the {name} workload, "
-                      f"conv + {'gate step + ' if raw else ''}token-by-token recurrence in f64, "
-                      f"{dt:.1f} s"}
+            "sample": f"{what}, conv + {'gate step + ' if raw else ''}token-by-token recurrence "
+                      f"in f64, {dt:.1f} s", "host": host_info()}
 
 
-def cpu_baseline_window(name, T, n_seq=4, gates="activated"):
-    """The oracle on a bounded sample of a verify / decode window: n_seq
-    sequences of one layer (verify, then the commit of the accepted prefix; for
-    decode the commit-all verify), reported as tokens per second per layer."""
+def cpu_baseline_window(name, T, n_seq=None, gates="activated"):
+    """The oracle on one layer of a verify / decode window: n_seq sequences
+    (default: the workload's whole batch) verified, then the accepted prefix
+    committed (decode: the commit-all verify), as tokens per second per layer."""
     import oracle as orc
     decode = name == "decode-bf16"
-    Hv = 48 if name == "spec-verify-bf16-h48" else 32
+    h48 = name == "spec-verify-bf16-h48"
+    Hv = 48 if h48 else 32
     T = 1 if decode else T
+    if n_seq is None:
+        n_seq = 256 if decode else 1 if h48 else 32
     raw = gates == "raw"
     inp = syn.verify_inputs(n_seq, T, 16, Hv, "bf16", seed=syn.seed_of(name) + T,
                             gate_form="raw" if raw else "softplus")
     t0 = time.perf_counter()
     al, be = (orc.gates(inp["alpha"], inp["beta"]) if raw else (inp["alpha"], inp["beta"]))
     orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"], al, be, inp["z"],
-               inp["norm_w"], inp["slot_idx"], 16, Hv, commit_all=decode, act32=True)
+               inp["norm_w"], inp["slot_idx"], 16, Hv, commit_all=decode)
     if not decode:
         orc.commit(inp["x"], al, be, inp["conv_w"], inp["conv_state"], inp["state"],
-                   inp["slot_idx"], inp["n_keep"], 16, Hv, act32=True)
+                   inp["slot_idx"], inp["n_keep"], 16, Hv)
     dt = time.perf_counter() - t0
     return {"value": n_seq * T / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n_seq} sequences x {T} tokens of one layer of the {name} window, "
+            "sample": f"one layer of the {name} window in full ({n_seq} sequences x {T} tokens), "
                       f"{'gate step + ' if raw else ''}verify{'' if decode else ' + commit'} in f64, "
-                      f"{dt:.2f} s"}
+                      f"{dt:.2f} s", "host": host_info()}
 
 
 # ----------------------------------------------------------------------------- main
+WINDOWS = ("spec-verify-bf16", "spec-verify-bf16-h48", "decode-bf16")
+# The default run: the largest single-GPU workload as the headline, then every
+# other workload of the benchmark as a further entry of the same line.
+HEADLINE = "decode-bf16"
+EXTRAS = [("tiny-f32", None), ("varlen-prefill-bf16", None), ("spec-verify-bf16", 1),
+          ("spec-verify-bf16", 4), ("spec-verify-bf16", 8), ("long-prefill-bf16", None)]
+# CPU-baseline sample per prefill workload (None: the whole workload)
+CPU_PREFILL_TOKENS = {"tiny-f32": None, "varlen-prefill-bf16": None, "long-prefill-bf16": 4096}
+
+
+def run_workload(name, T, args, torch, G, dev, world, barrier, flush, lazy=False, steps=None,
+                 cpu=True):
+    """Times one workload (value: device time of the step, CUDA events on the
+    launching stream; e2e: the same calls with host copies). Returns the fields
+    of its JSON entry; every rank returns, rank 0's is printed."""
+    steps = steps or args.steps
+    if name in WINDOWS:
+        W = StepWorkload(name, torch, G, dev, T=T, gates=args.gates, lazy=lazy)
+    else:
+        W = PrefillWorkload(name, torch, G, dev, gates=args.gates)
+    for _ in range(max(args.warmup, 3)):
+        W.reset()
+        W.step()
+    torch.cuda.synchronize()
+    if isinstance(W, StepWorkload):
+        W.capture()
+        for _ in range(2):
+            W.step()
+        torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t_wall = time.perf_counter()
+    for k in range(steps):
+        W.reset()
+        flush.fill_(float(k))
+        W.step(evs[k])
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    conv_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(steps)]
+    pf_ms = [evs[k][1].elapsed_time(evs[k][2]) for k in range(steps)]
+    step_ms = [c + p for c, p in zip(conv_ms, pf_ms)]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, dev, world)
+
+    # end-to-end through the public API with host buffers
+    W.setup_e2e()
+    for _ in range(3):
+        W.reset()
+        W.step_e2e()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for k in range(steps):
+        W.reset()
+        flush.fill_(float(k))
+        e0.record()
+        W.step_e2e()
+        e1.record()
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_max = max_over_ranks(statistics.mean(e2e_ms), dev, world)
+
+    peaks, peak_src = load_peaks()
+    a_avg, b_avg = statistics.mean(conv_ms), statistics.mean(pf_ms)
+    if isinstance(W, StepWorkload):
+        vk = "step_kernel" if W.decode else "lazy_kernel" if W.lazy else "verify_kernel"
+        names = (f"{vk} ({'decode' if W.decode else 'commit + verify' if W.lazy else 'verify'})",
+                 "step_kernel (commit)")
+        ka = {"ms": round(a_avg, 4), "bytes": W.bytes["verify"],
+              "GB/s": round(W.bytes["verify"] / (a_avg * 1e-3) / 1e9, 1)}
+        ka["frac_hbm"] = round(ka["GB/s"] / peaks["hbm_gbs"], 4)
+        kernels = {names[0]: ka}
+        if not W.decode and not W.lazy:
+            kb = {"ms": round(b_avg, 4), "bytes": W.bytes["commit"],
+                  "GB/s": round(W.bytes["commit"] / max(b_avg, 1e-9) / 1e6, 1)}
+            kb["frac_hbm"] = round(kb["GB/s"] / peaks["hbm_gbs"], 4)
+            kernels[names[1]] = kb
+        roof = {"kernel": names[0] + f", {W.LAYERS} launches", "bound": "hbm",
+                "achieved": ka["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ka["frac_hbm"], "traffic": ncu_traffic(vk, W.name + f"/T{W.T}"),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes": W.bytes["verify"], "per": "window of all layers"}
+        value = whole_job_rate(W.tokens * W.LAYERS, world, ms_max)
+    else:
+        pf_tflops = W.flops["prefill"] / (b_avg * 1e-3) / 1e12
+        pf_gbs = W.bytes["prefill"] / (b_avg * 1e-3) / 1e9
+        conv_gbs = W.bytes["conv"] / (a_avg * 1e-3) / 1e9
+        pf_name = "prefill_tc_kernel" if W.inp["act"] == "bf16" else "prefill_ffma_kernel"
+        if b_avg >= a_avg:
+            roof = prefill_roofline(pf_name, W.flops["prefill"], W.bytes["prefill"], b_avg, peaks,
+                                    peak_src, ncu_traffic(pf_name, W.name))
+        else:
+            roof = {"kernel": "conv_fwd_kernel", "bound": "hbm", "achieved": round(conv_gbs, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(conv_gbs / peaks["hbm_gbs"], 4),
+                    "traffic": ncu_traffic("conv_fwd_kernel", W.name),
+                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+        kernels = {
+            "conv_fwd_kernel": {"ms": round(a_avg, 4), "bytes": W.bytes["conv"],
+                                "GB/s": round(conv_gbs, 1),
+                                "frac_hbm": round(conv_gbs / peaks["hbm_gbs"], 4)},
+            pf_name: {"ms": round(b_avg, 4), "bytes": W.bytes["prefill"],
+                      "GB/s": round(pf_gbs, 1), "frac_hbm": round(pf_gbs / peaks["hbm_gbs"], 4),
+                      "TFLOP/s": round(pf_tflops, 3)},
+        }
+        value = whole_job_rate(W.tokens, world, ms_max)
+    e2e_val = value * ms_max / e2e_max
+    entry = {
+        "value": round(value, 1), "unit": "tokens/s", "steps": steps,
+        "ms_per_step": round(ms_max, 4), "ms_min": round(min(step_ms), 4),
+        "ms_max": round(max(step_ms), 4), "dtype": "f32" if name == "tiny-f32" else "bf16",
+        "config": W.config(), "roofline": roof, "kernels": kernels,
+        "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s", "h2d_bytes_per_step": W.h2d,
+                "d2h_bytes_per_step": W.d2h},
+        "gpu_launches": W.launches_per_step * steps,
+        "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    del W
+    torch.cuda.empty_cache()
+    if world == 1 and cpu and not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        if name in WINDOWS:
+            entry["cpu_baseline"] = cpu_baseline_window(name, T or 8, gates=args.gates)
+        else:
+            entry["cpu_baseline"] = cpu_baseline(name, max_tokens=CPU_PREFILL_TOKENS.get(name, 4096),
+                                                 gates=args.gates)
+    return entry
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="varlen-prefill-bf16")
+    ap.add_argument("--workload", default=None,
+                    help=f"one workload only (default: {HEADLINE} as the headline, then the others)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--T", type=int, default=8, help="draft tokens of spec-verify-bf16")
     ap.add_argument("--lazy", action="store_true",
@@ -562,121 +723,23 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    if args.workload in ("spec-verify-bf16", "spec-verify-bf16-h48", "decode-bf16"):
-        W = StepWorkload(args.workload, torch, G, dev, T=args.T, gates=args.gates, lazy=args.lazy)
-    else:
-        W = PrefillWorkload(args.workload, torch, G, dev, gates=args.gates)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    for _ in range(max(args.warmup, 3)):
-        W.reset()
-        W.step()
-    torch.cuda.synchronize()
-    if isinstance(W, StepWorkload):
-        W.capture()
-        for _ in range(2):
-            W.step()
-        torch.cuda.synchronize()
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    barrier()
-    t_wall = time.perf_counter()
-    for k in range(args.steps):
-        W.reset()
-        flush.fill_(float(k))
-        W.step(evs[k])
-    barrier()
-    t_wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
-    conv_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
-    pf_ms = [evs[k][1].elapsed_time(evs[k][2]) for k in range(args.steps)]
-    step_ms = [c + p for c, p in zip(conv_ms, pf_ms)]
-    ms = statistics.mean(step_ms)
-    ms_max = max_over_ranks(ms, dev, world)
-
-    # end-to-end through the public API with host buffers
-    W.setup_e2e()
-    for _ in range(3):
-        W.reset()
-        W.step_e2e()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e2e_ms = []
-    for k in range(args.steps):
-        W.reset()
-        flush.fill_(float(k))
-        e0.record()
-        W.step_e2e()
-        e1.record()
-        e1.synchronize()
-        e2e_ms.append(e0.elapsed_time(e1))
-    e2e_max = max_over_ranks(statistics.mean(e2e_ms), dev, world)
-
+    name = args.workload or HEADLINE
+    head = run_workload(name, args.T, args, torch, G, dev, world, barrier, flush, lazy=args.lazy)
+    extras = {}
+    if args.workload is None:
+        for wname, T in EXTRAS:
+            key = wname if T is None else f"{wname}/T{T}"
+            extras[key] = run_workload(wname, T, args, torch, G, dev, world, barrier, flush,
+                                       steps=min(args.steps, 20))
     if rank == 0:
-        peaks, peak_src = load_peaks()
-        a_avg, b_avg = statistics.mean(conv_ms), statistics.mean(pf_ms)
-        if isinstance(W, StepWorkload):
-            vk = "step_kernel" if W.decode else "lazy_kernel" if W.lazy else "verify_kernel"
-            names = (f"{vk} ({'decode' if W.decode else 'commit + verify' if W.lazy else 'verify'})",
-                     "step_kernel (commit)")
-            ka = {"ms": round(a_avg, 4), "bytes": W.bytes["verify"],
-                  "GB/s": round(W.bytes["verify"] / (a_avg * 1e-3) / 1e9, 1)}
-            ka["frac_hbm"] = round(ka["GB/s"] / peaks["hbm_gbs"], 4)
-            kernels = {names[0]: ka}
-            if not W.decode and not W.lazy:
-                kb = {"ms": round(b_avg, 4), "bytes": W.bytes["commit"],
-                      "GB/s": round(W.bytes["commit"] / max(b_avg, 1e-9) / 1e6, 1)}
-                kb["frac_hbm"] = round(kb["GB/s"] / peaks["hbm_gbs"], 4)
-                kernels[names[1]] = kb
-            roof = {"kernel": names[0] + ", 36 launches", "bound": "hbm", "achieved": ka["GB/s"],
-                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ka["frac_hbm"],
-                    "traffic": ncu_traffic(vk, W.name + f"/T{W.T}"),
-                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
-            value = whole_job_rate(W.tokens * W.LAYERS, world, ms_max)
-        else:
-            pf_tflops = W.flops["prefill"] / (b_avg * 1e-3) / 1e12
-            pf_gbs = W.bytes["prefill"] / (b_avg * 1e-3) / 1e9
-            conv_gbs = W.bytes["conv"] / (a_avg * 1e-3) / 1e9
-            pf_name = "prefill_tc_kernel" if W.inp["act"] == "bf16" else "prefill_ffma_kernel"
-            if b_avg >= a_avg:
-                roof = prefill_roofline(pf_name, W.flops["prefill"], W.bytes["prefill"], b_avg, peaks,
-                                        peak_src, ncu_traffic(pf_name, W.name))
-            else:
-                roof = {"kernel": "conv_fwd_kernel", "bound": "hbm", "achieved": round(conv_gbs, 1),
-                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(conv_gbs / peaks["hbm_gbs"], 4),
-                        "traffic": ncu_traffic("conv_fwd_kernel", W.name),
-                        "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
-            kernels = {
-                "conv_fwd_kernel": {"ms": round(a_avg, 4), "bytes": W.bytes["conv"],
-                                    "GB/s": round(conv_gbs, 1),
-                                    "frac_hbm": round(conv_gbs / peaks["hbm_gbs"], 4)},
-                pf_name: {"ms": round(b_avg, 4), "bytes": W.bytes["prefill"],
-                          "GB/s": round(pf_gbs, 1), "TFLOP/s": round(pf_tflops, 3)},
-            }
-            value = whole_job_rate(W.tokens, world, ms_max)
-        e2e_val = value * ms_max / e2e_max
-        line = {
-            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
-            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
-            "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": W.config(), "roofline": roof, "kernels": kernels,
-            "e2e": {"value": round(e2e_val, 1),
-                    "unit": "tokens/s", "h2d_bytes_per_step": W.h2d, "d2h_bytes_per_step": W.d2h},
-            "gpu_launches": W.launches_per_step * args.steps,
-            "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
-            "wall_s_timed_region": round(t_wall, 3),
-        }
-        if world == 1 and not args.no_cpu_baseline and isinstance(W, PrefillWorkload):
-            line["cpu_baseline"] = cpu_baseline(args.workload, gates=args.gates)
-        elif world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline_window(args.workload, W.T, gates=args.gates)
+        line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": max(args.warmup, 3),
+                "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic"}
+        line.update({k: v for k, v in head.items() if k not in line and k != "steps"})
+        if extras:
+            line["workloads"] = extras
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -692,24 +755,27 @@ def reference_arm(args, rank, world):
     orc.build()
     for _ in range(args.warmup):
         pass                                      # the oracle has no warm-up state
-    window = args.workload in ("spec-verify-bf16", "spec-verify-bf16-h48", "decode-bf16")
+    name = args.workload or HEADLINE
+    window = name in WINDOWS
+    n_seq = 16                                   # sequences of one layer per step
     times, toks = [], 0
     line0 = None
     for _ in range(args.steps):
-        cb = (cpu_baseline_window(args.workload, args.T, gates=args.gates) if window
-              else cpu_baseline(args.workload, max_tokens=512, gates=args.gates))
+        cb = (cpu_baseline_window(name, args.T, n_seq=n_seq, gates=args.gates) if window
+              else cpu_baseline(name, max_tokens=512, gates=args.gates))
         times.append(1.0 / cb["value"])
         line0 = cb
     tps = 1.0 / statistics.mean(times)
-    per_step = (4 * (1 if args.workload == "decode-bf16" else args.T)) if window else 512
+    per_step = (n_seq * (1 if name == "decode-bf16" else args.T)) if window else 512
     line = {"impl": "reference", "metric": METRIC, "value": round(tps, 2), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(per_step / tps * 1e3, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "gates": gates_note(args.gates),
+            "config": {"workload": name, "gates": gates_note(args.gates),
                        "sample": line0["sample"] if line0 else ""},
             "cpu_baseline": {"value": round(tps, 2), "unit": "tokens/s", "cores": 1,
-                             "kind": "oracle", "sample": line0["sample"] if line0 else ""},
+                             "kind": "oracle", "sample": line0["sample"] if line0 else "",
+                             "host": host_info()},
             "e2e": {"value": round(tps, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

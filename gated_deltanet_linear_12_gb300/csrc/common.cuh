@@ -95,90 +95,63 @@ template <int A> __device__ __forceinline__ void raw_unpack(const Raw8<A>& r, fl
   }
 }
 
+// Output rows: the activation dtype A, or f32 when out_f32.
+template <int A> __device__ __forceinline__ void store_out8(void* base, int64_t i, const float v[8], int out_f32) {
+  if (out_f32) store8<F32>(base, i, v);
+  else store8<A>(base, i, v);
+}
+
+// One gate value (alpha, beta or a raw projection) widened to f32.
+__device__ __forceinline__ float load_gate(const void* p, int64_t i, int bf16) {
+  return bf16 ? bf2f(static_cast<const uint16_t*>(p)[i]) : static_cast<const float*>(p)[i];
+}
+
 __device__ __forceinline__ void report(uint32_t* dev_err, uint32_t bit) {
   if (dev_err) atomicOr(dev_err, bit);
 }
 
-// Causal conv of one channel: taps in order, a rounded product then three
-// fused multiply-adds, tap 3 on the current token.
+// Causal conv of one channel: the tap products summed from zero in tap order,
+// tap 3 on the current token, each product and each sum rounded on its own.
+// Scalar __fmul_rn / __fadd_rn are never merged into fused multiply-adds.
 __device__ __forceinline__ float conv4(const float w[4], float x0, float x1, float x2, float x3) {
   float acc = __fmul_rn(w[0], x0);
-  acc = __fmaf_rn(w[1], x1, acc);
-  acc = __fmaf_rn(w[2], x2, acc);
-  acc = __fmaf_rn(w[3], x3, acc);
+  acc = __fadd_rn(acc, __fmul_rn(w[1], x1));
+  acc = __fadd_rn(acc, __fmul_rn(w[2], x2));
+  acc = __fadd_rn(acc, __fmul_rn(w[3], x3));
   return acc;
 }
 
-// The same for two channels at once (w0..w3 hold the taps of both).
+// The same for two channels at once (w0..w3 hold the taps of both). With bf16
+// operands every product is exact in f32 (8 x 8 significant bits), so a fused
+// multiply-add rounds exactly like a rounded product followed by a rounded
+// sum: the paired fused form gives the bits of conv4. f32 operands take conv4.
+template <int A>
 __device__ __forceinline__ float2 conv4x2(float2 w0, float2 w1, float2 w2, float2 w3, float2 x0,
                                           float2 x1, float2 x2, float2 x3) {
-  float2 acc = __fmul2_rn(w0, x0);
-  acc = __ffma2_rn(w1, x1, acc);
-  acc = __ffma2_rn(w2, x2, acc);
-  acc = __ffma2_rn(w3, x3, acc);
-  return acc;
-}
-
-// SiLU, two values at a time with Blackwell's paired f32 instructions, by
-// published schemes made only of correctly rounded IEEE operations and exact
-// integer operations on the bits, so the result is reproducible bit for bit by
-// any IEEE implementation of the same steps (the post-conv activations then
-// round to the same bf16 values everywhere):
-//   t = e^-|y|: Cody & Waite's reduction -|y| = n ln2 + r (ln 2 split in a
-//     16-bit high part, so n * high is exact, and a low part; the argument
-//     clamped at -86 keeps 2^n p normal), a degree-5 polynomial of e^r in Horner
-//     form (the near-minimax relative fit on |r| <= ln2/2 with float
-//     coefficients), scaled by 2^n by adding n to the exponent field. n, the
-//     nearest integer to the exact a log2 e, comes from one fused multiply-add
-//     with 1.5 * 2^23 (which rounds it to an integer) and an exact subtraction;
-//     n << 23 is read from the low bits of the sum;
-//   (Each multiply whose result feeds a single add is written as an explicit
-//   fused multiply-add, on both sides: the compiler is otherwise free to fuse
-//   paired f32 multiplies into the next add, which changes the rounding.)
-//   s = 1/(1 + t), d in [1, 2]: Newton-Raphson from the quadratic start
-//     2.1212120 - 1.4545449 d + 0.32323205 d^2 (relative error <= 0.0102), two
-//     steps x <- x + x (1 - d x);
-//   sigmoid = s (y >= 0) or t s (y < 0);  silu = y sigmoid.
-// Within 6 ulp of silu on [-86, 90].
-__device__ __forceinline__ float2 silu2(float2 y) {
-  constexpr float kMagic = 12582912.0f;                 // 1.5 * 2^23
-  constexpr float kLog2e = 1.44269504088896341f;
-  const float2 a = make_float2(fmaxf(-fabsf(y.x), -86.0f), fmaxf(-fabsf(y.y), -86.0f));
-  const float2 tt = __ffma2_rn(a, make_float2(kLog2e, kLog2e), make_float2(kMagic, kMagic));
-  const float2 n = __fadd2_rn(tt, make_float2(-kMagic, -kMagic));
-  const float2 mn = make_float2(-n.x, -n.y);
-  float2 r = __ffma2_rn(mn, make_float2(0.693145751953125f, 0.693145751953125f), a);
-  r = __ffma2_rn(mn, make_float2(1.42860682030941723212e-6f, 1.42860682030941723212e-6f), r);
-  float2 p = make_float2(0.008297654800117016f, 0.008297654800117016f);
-  p = __ffma2_rn(p, r, make_float2(0.04191538318991661f, 0.04191538318991661f));
-  p = __ffma2_rn(p, r, make_float2(0.16667574644088745f, 0.16667574644088745f));
-  p = __ffma2_rn(p, r, make_float2(0.49998894333839417f, 0.49998894333839417f));
-  p = __ffma2_rn(p, r, make_float2(0.9999997019767761f, 0.9999997019767761f));
-  p = __ffma2_rn(p, r, make_float2(1.0000001192092896f, 1.0000001192092896f));
-  const float2 t = make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(tt.x) << 23)),
-                               __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(tt.y) << 23)));  // e^-|y|
-  const float2 d = __fadd2_rn(make_float2(1.0f, 1.0f), t);
-  const float2 md = make_float2(-d.x, -d.y);
-  float2 x = __ffma2_rn(make_float2(0.3232320547103882f, 0.3232320547103882f), d,
-                        make_float2(-1.4545449018478394f, -1.4545449018478394f));
-  x = __ffma2_rn(x, d, make_float2(2.1212120056152344f, 2.1212120056152344f));
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float2 e = __ffma2_rn(md, x, make_float2(1.0f, 1.0f));
-    x = __ffma2_rn(x, e, x);
+  if constexpr (A == BF16) {
+    float2 acc = __fmul2_rn(w0, x0);
+    acc = __ffma2_rn(w1, x1, acc);
+    acc = __ffma2_rn(w2, x2, acc);
+    acc = __ffma2_rn(w3, x3, acc);
+    return acc;
+  } else {
+    const float wa[4] = {w0.x, w1.x, w2.x, w3.x}, wb[4] = {w0.y, w1.y, w2.y, w3.y};
+    return make_float2(conv4(wa, x0.x, x1.x, x2.x, x3.x), conv4(wb, x0.y, x1.y, x2.y, x3.y));
   }
-  const float2 ts = __fmul2_rn(t, x);
-  const float2 sig = make_float2(y.x >= 0.0f ? x.x : ts.x, y.y >= 0.0f ? x.y : ts.y);
-  return __fmul2_rn(y, sig);
 }
 
-__device__ __forceinline__ float silu(float y) { return silu2(make_float2(y, 0.f)).x; }
-
-// SiLU for the output gate z, where no bitwise agreement is asked for: the
-// fast exponential and divide intrinsics (relative error about 1e-6).
-__device__ __forceinline__ float silu_gate(float z) {
-  return __fdividef(z, 1.0f + __expf(-z));
+// SiLU y / (1 + e^-y) with the hardware exponential and reciprocal (__expf,
+// __fdividef). Relative error against the exact value: a few ulp plus
+// |y| 2^-24 from the rounding of the exponent's argument (below 2e-6 for
+// |y| <= 30); for y < -87 the exponential overflows and the result is -0,
+// against an exact value below 6e-37 in magnitude.
+__device__ __forceinline__ float silu(float y) {
+  return __fdividef(y, 1.0f + __expf(-y));
 }
+__device__ __forceinline__ float2 silu2(float2 y) { return make_float2(silu(y.x), silu(y.y)); }
+
+// SiLU of the output gate z: the same function.
+__device__ __forceinline__ float silu_gate(float z) { return silu(z); }
 
 // The gate step from raw projections ("Strata PR #3226" names a fused gate
 // kernel; the form is the one of the synthetic workloads' gates):

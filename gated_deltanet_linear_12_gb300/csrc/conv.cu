@@ -6,201 +6,329 @@
 // sum of squares then 1/sqrtf; "New issue #305": only the chunk-0 block reads
 // the initial conv_state while the last chunk wrote the final one — a race).
 //
-// Design (GB300). A block takes one 64-token chunk of one sequence and four
-// heads. Warp 0 bulk-copies (TMA) the chunk's rows of those heads, with the 3
-// rows before it (the initial conv_state rows for chunk 0), into shared memory
-// at once, all counted on one mbarrier, so a whole 67 KiB tile is in flight per
-// block. One thread then owns 8 contiguous channels of a quarter of the chunk
-// (16 tokens) and walks them with the 3 previous rows in registers. A warp holds
-// two heads x 16 lanes, which is exactly the lane layout of the fixed
-// sum-of-squares tree; tokens go in pairs so that even lanes take the 1/sqrt of
-// the first token and odd lanes of the second. The chunk-0 thread that reads a
-// channel's initial rows is the one that later writes that channel's final
-// rows: the final rows are taken from x (or from the initial rows when the
-// sequence is shorter than 3), so no other block ever touches conv_state.
+// Design (GB300). The work items are (64-token chunk of one sequence, group
+// of four heads). A persistent grid of one 512-thread block per SM walks them
+// round-robin; each block keeps three tile buffers in shared memory and has the
+// tiles of its next two items in flight (bulk copies, TMA) while it computes the
+// current one, so HBM streams while the SM computes. A tile is the chunk's rows
+// of its four heads with the 3 rows before it (x rows, or the initial conv_state
+// rows for chunk 0), kept as two halves of two heads each, [67 rows][256
+// channels]: the 64 chunk rows of a half arrive as one 2-D TMA box (256 x 64),
+// the 3 rows before it as three row copies. One thread owns 8 contiguous
+// channels of an eighth of the chunk (8 tokens) and walks them with the 3
+// previous rows in registers. A warp holds two heads x 16 lanes, which is
+// exactly the lane layout of the fixed sum-of-squares tree; tokens go in pairs
+// so that even lanes take the 1/sqrt of the first token and odd lanes of the
+// second. The chunk-0 thread that reads a channel's initial rows is the one that
+// later writes that channel's final rows: the final rows are taken from x (or
+// from the initial rows when the sequence is shorter than 3), so no other block
+// ever touches conv_state.
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
 
 namespace gdn {
 
-constexpr int CONV_HEADS_PER_BLOCK = 4;               // 4 heads x 16 lanes x 4 quarters
-constexpr int CONV_QUARTERS = 4;                      // token quarters of a chunk
-constexpr int CONV_THREADS = CONV_HEADS_PER_BLOCK * 16 * CONV_QUARTERS;
-constexpr int CONV_TOK = CHUNK / CONV_QUARTERS;       // 16 tokens per thread
+constexpr int CONV_HEADS_PER_BLOCK = 4;               // 4 heads x 16 lanes x 8 token groups
+constexpr int CONV_GROUPS = 8;                        // token groups of a chunk
+constexpr int CONV_THREADS = CONV_HEADS_PER_BLOCK * 16 * CONV_GROUPS;
+constexpr int CONV_TOK = CHUNK / CONV_GROUPS;         // 8 tokens per thread
 constexpr int CONV_ROWS = KS + CHUNK;                 // staged rows: 3 before the chunk + 64
 
-template <int A> constexpr int conv_tile_bytes() { return CONV_ROWS * CONV_HEADS_PER_BLOCK * D * (A == BF16 ? 2 : 4); }
+constexpr int CONV_HALF_COLS = 2 * D;                 // two heads per TMA box
+template <int A> __host__ __device__ constexpr int conv_half_bytes() { return CONV_ROWS * CONV_HALF_COLS * (A == BF16 ? 2 : 4); }
+template <int A> __host__ __device__ constexpr int conv_tile_bytes() { return 2 * conv_half_bytes<A>(); }
+// Tile buffers: three for bf16 (201 KiB), one for f32 (134 KiB; the f32 path is
+// the test arm, not a streaming workload).
+template <int A> __host__ __device__ constexpr int conv_stages() { return A == BF16 ? 3 : 1; }
 
-// Thread layout: warp w covers quarter w / 2 of the chunk and heads
-// 2 (w % 2), 2 (w % 2) + 1 of the block's 4 heads (16 lanes each, 8 contiguous
-// channels per lane). Quarter 0 of the chunk-0 block owns conv_state.
+// What a block knows about a staged item (written by the issuing thread before
+// its arrival on the stage's barrier, read after the wait).
+struct ConvItem {
+  int s, ci, head0, flags;                               // flags: CI_*
+  int slot, n_here;                                      // the sequence's slot, tokens in the chunk
+  int64_t t_chunk, seq0, len;                            // first token row, sequence start and length
+};
+constexpr int CI_VALID = 1, CI_HALO_X = 2, CI_HALO_STATE = 4, CI_BAD_SLOT = 8, CI_BAD_SEQ = 16;
+
+// 2-D TMA copy of a box of the x rows (x = column, y = row), counted on `bar`.
+__device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          tc::smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+// Thread layout: warp w covers token group w / 2 of the chunk (tokens 8 (w / 2)
+// .. + 7) and heads 2 (w % 2), 2 (w % 2) + 1 of the item's 4 heads (16 lanes
+// each, 8 contiguous channels per lane), which are tile half w % 2. Group 0 of
+// the chunk-0 item owns conv_state. xmap: x as [n_tok rows][C columns] in boxes
+// of 256 columns x 64 rows (rows past n_tok and columns past C read as zeros).
 template <int A, bool NORM>
-__global__ void __launch_bounds__(CONV_THREADS, 2)
+__global__ void __launch_bounds__(CONV_THREADS, 1)
 conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, int64_t ld_y,
                 const void* __restrict__ conv_w, void* __restrict__ conv_state,
                 const int32_t* __restrict__ slot_idx, const int32_t* __restrict__ cu,
                 const uint8_t* __restrict__ has_init, int n_seq, int64_t n_tok, int n_heads,
-                int n_qk, int n_slots, float eps, uint32_t* dev_err) {
-  extern __shared__ __align__(128) uint8_t tile[];      // [CONV_ROWS][4 heads x 128] act
-  __shared__ uint64_t bar;
-  int s, ci;
-  if (!find_chunk(cu, n_seq, blockIdx.x, CHUNK, s, ci)) return;
-  const int slot = slot_idx[s];
-  if (slot < 0) return;                                  // padding sequence
-  const int64_t seq0 = cu[s], seq1 = cu[s + 1];
-  if (seq1 < seq0 || seq0 < 0 || seq1 > n_tok) {
-    if (ci == 0 && threadIdx.x == 0 && blockIdx.y == 0) report(dev_err, GDN_DEVERR_SEQLENS);
-    return;
-  }
-  if (slot >= n_slots) {
-    if (ci == 0 && threadIdx.x == 0 && blockIdx.y == 0) report(dev_err, GDN_DEVERR_SLOT);
-    return;
-  }
+                int n_qk, int n_slots, float eps, uint32_t* dev_err, int64_t n_items, int n_hgroups,
+                const __grid_constant__ CUtensorMap xmap) {
+  constexpr int NS = conv_stages<A>();
+  constexpr int HALF = conv_half_bytes<A>();
+  constexpr int TILE = conv_tile_bytes<A>();
+  extern __shared__ __align__(128) uint8_t tiles[];      // NS x [CONV_ROWS][4 heads x 128] act
+  __shared__ uint64_t bar[NS];                           // stage filled (copies complete)
+  __shared__ uint64_t empty[NS];                         // stage read by all 16 warps
+  __shared__ ConvItem meta[NS];
+  __shared__ int abort_flag;
+  __shared__ int64_t n_produced;                         // items of this block whose copies started
   constexpr int asz = A == BF16 ? 2 : 4;
-  constexpr int ROW = CONV_HEADS_PER_BLOCK * D;           // tile row stride in elements
+  constexpr int ROW = CONV_HALF_COLS;                    // tile row stride in elements
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int head0 = blockIdx.y * CONV_HEADS_PER_BLOCK;
-  const int heads_here = min(CONV_HEADS_PER_BLOCK, n_heads - head0);
   const int C = n_heads * D;
-  const int64_t len = seq1 - seq0;
-  const int64_t t_chunk = seq0 + (int64_t)ci * CHUNK;
-  const int n_here = (int)(min(t_chunk + CHUNK, seq1) - t_chunk);   // 0 only for an empty sequence
-  const bool hi = has_init[s] != 0;
-  const int64_t st_base = (int64_t)slot * KS * C;
 
-  // ---- stage rows t_chunk - 3 .. t_chunk + n_here - 1 (tile row r = token t_chunk - 3 + r)
+  constexpr int WARPS = CONV_THREADS / 32;
   if (tid == 0) {
-    tc::mbar_init(&bar, 1);
+#pragma unroll
+    for (int st = 0; st < NS; ++st) {
+      tc::mbar_init(&bar[st], 1);
+      tc::mbar_init(&empty[st], WARPS);
+    }
+    abort_flag = 0;
+    n_produced = 0;
     tc::fence_mbar_init();
   }
-  __syncthreads();                                       // the barrier is initialised before any wait
-  const bool halo_x = ci > 0, halo_state = ci == 0 && hi;
-  if (warp == 0) {
-    const uint32_t row_bytes = (uint32_t)heads_here * D * asz;
-    if (lane == 0)
-      tc::mbar_arrive_expect_tx(&bar, (uint32_t)(n_here + ((halo_x || halo_state) ? KS : 0)) * row_bytes);
-    __syncwarp();
-    for (int r = lane; r < KS + n_here; r += 32) {
-      const char* src = nullptr;
-      if (r >= KS || halo_x)
-        src = static_cast<const char*>(x) + ((t_chunk - KS + r) * ld_x + (int64_t)head0 * D) * asz;
-      else if (halo_state)
-        src = static_cast<const char*>(conv_state) + (st_base + (int64_t)r * C + (int64_t)head0 * D) * asz;
-      if (src) tc::bulk_load(tile + (size_t)r * ROW * asz, src, row_bytes, &bar);
+  __syncthreads();                                       // the barriers are initialised before any use
+
+  // Warp 0: look up item `it` and start the copies of its tile into stage st.
+  // Every call arrives once on the stage's barrier (with the byte count of the
+  // copies, 0 for an item that stages nothing).
+  auto produce = [&](int64_t it, int st) {
+    ConvItem m{-1, 0, 0, 0, 0, 0, 0, 0, 0};
+    const int j = (int)(it / n_hgroups), g = (int)(it % n_hgroups);
+    int s = 0, ci = 0;
+    int64_t t_chunk = 0;
+    int n_here = 0, halves = 0;
+    if (find_chunk(cu, n_seq, j, CHUNK, s, ci)) {
+      m.s = s;
+      m.ci = ci;
+      m.head0 = g * CONV_HEADS_PER_BLOCK;
+      const int slot = slot_idx[s];
+      const int64_t seq0 = cu[s], seq1 = cu[s + 1];
+      if (slot >= 0) {
+        if (seq1 < seq0 || seq0 < 0 || seq1 > n_tok) m.flags = CI_BAD_SEQ;
+        else if (slot >= n_slots) m.flags = CI_BAD_SLOT;
+        else {
+          m.flags = CI_VALID;
+          t_chunk = seq0 + (int64_t)ci * CHUNK;
+          n_here = (int)(min(t_chunk + CHUNK, seq1) - t_chunk);   // 0 only for an empty sequence
+          m.slot = slot;
+          m.n_here = n_here;
+          m.t_chunk = t_chunk;
+          m.seq0 = seq0;
+          m.len = seq1 - seq0;
+          if (ci > 0) m.flags |= CI_HALO_X;
+          else if (has_init[s]) m.flags |= CI_HALO_STATE;
+          halves = min(CONV_HEADS_PER_BLOCK, n_heads - m.head0) > 2 ? 2 : 1;
+        }
+      }
     }
-  }
-  if (!halo_x && !halo_state) {                          // chunk 0 without initial rows: zeros
-    for (int e = tid; e < KS * ROW * asz / 16; e += CONV_THREADS)
-      reinterpret_cast<uint4*>(tile)[e] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  const int quarter = warp >> 1;
-  const int hb = (warp & 1) * 2 + (lane >> 4);           // head within the block
-  const int head = head0 + hb;
-  const bool active = hb < heads_here;                   // uniform per 16 lanes
-  const bool is_qk = head < 2 * n_qk;
-  const int c0 = head * D + (lane & 15) * 8;             // global channel
-  const int cb = hb * D + (lane & 15) * 8;               // channel within a tile row
-  const int u0 = quarter * CONV_TOK;                     // this thread's first token in the chunk
-  const int n_mine = max(0, min(CONV_TOK, n_here - u0)); // uniform per warp
-  const bool owner = ci == 0 && quarter == 0;            // reads and writes conv_state
-  Raw8<A> wr[4];                                          // the taps, in flight with the tile
-  if (active && n_mine > 0) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) raw_load<A>(conv_w, (int64_t)c0 * KW + 8 * q, wr[q]);
-  } else {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) raw_zero<A>(wr[q]);
-  }
-  const bool ok = tc::mbar_wait(&bar, 0, 1u << 24);
-  if (__syncthreads_or(!ok)) {                           // also orders the zero rows
-    if (tid == 0) report(dev_err, GDN_DEVERR_TIMEOUT);
-    tc::mbar_wait(&bar, 0, 1u << 24);                    // the copies, if still in flight
-    return;
+    const bool halo = (m.flags & (CI_HALO_X | CI_HALO_STATE)) != 0;
+    uint8_t* tile = tiles + (size_t)st * TILE;
+    // one box of 64 rows per half (the whole box is counted, rows past the
+    // chunk included), and 3 halo rows per half
+    const int heads_here = m.flags & CI_VALID ? min(CONV_HEADS_PER_BLOCK, n_heads - m.head0) : 0;
+    const uint32_t bytes = n_here > 0 ? (uint32_t)halves * CHUNK * ROW * asz : 0u;
+    const uint32_t halo_bytes = halo ? (uint32_t)(KS * heads_here * D * asz) : 0u;   // exact channels
+    if (lane == 0) {
+      meta[st] = m;
+      ++n_produced;
+      tc::fence_async_smem();                            // earlier reads of the stage come first
+      tc::mbar_arrive_expect_tx(&bar[st], bytes + halo_bytes);
+      for (int hf = 0; hf < halves && n_here > 0; ++hf)
+        tma_box(tile + (size_t)hf * HALF + (size_t)KS * ROW * asz, &xmap, (m.head0 + 2 * hf) * D,
+                (int)t_chunk, &bar[st]);
+    }
+    __syncwarp();                                        // the byte count is announced first
+    if (halo && lane < 2 * KS && (lane & 1) < halves) {
+      const int r = lane >> 1, hf = lane & 1;            // halo row r (0..2) of half hf
+      const char* src;
+      if (m.flags & CI_HALO_X)
+        src = static_cast<const char*>(x) + ((t_chunk - KS + r) * ld_x + (int64_t)(m.head0 + 2 * hf) * D) * asz;
+      else
+        src = static_cast<const char*>(conv_state) +
+              ((int64_t)slot_idx[s] * KS * C + (int64_t)r * C + (int64_t)(m.head0 + 2 * hf) * D) * asz;
+      const uint32_t nb = (uint32_t)(min(2, heads_here - 2 * hf) * D * asz);   // the half's heads only
+      tc::bulk_load(tile + (size_t)hf * HALF + (size_t)r * ROW * asz, src, nb, &bar[st]);
+    }
+    __syncwarp();
+  };
+
+  // Pipeline: item i of this block (it = blockIdx.x + i * gridDim.x) uses stage
+  // i % NS; its copies complete phase i / NS of bar[stage], and phase i / NS of
+  // empty[stage] completes when each of the 16 warps has finished reading it.
+  // Warp 0 issues item i + NS - 1 at the start of item i, once item i - 1 (the
+  // last user of that stage) has been released by every warp. No block-wide
+  // barrier: the warps drift apart by up to the pipeline depth.
+  const int64_t stride = gridDim.x;
+  const int64_t n_mine_items = blockIdx.x < n_items ? (n_items - 1 - blockIdx.x) / stride + 1 : 0;
+  if (warp == 0) {
+    for (int64_t i = 0; i < NS - 1 && i < n_mine_items; ++i) produce(blockIdx.x + i * stride, (int)i);
   }
 
-  if (n_mine > 0) {
-    float2 w[4][4];                                       // [channel pair][tap]
-    float2 p0[4], p1[4], p2[4];                           // the three previous rows
-    {
-      float r0[8], r1[8], r2[8];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {                      // channels 2q, 2q+1: 8 taps
-        float t8[8];
-        raw_unpack<A>(wr[q], t8);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w[q][j] = make_float2(t8[j], t8[4 + j]);
-      }
-      load8<A>(tile, (int64_t)u0 * ROW + cb, r0);        // tile rows u0 .. u0 + 2 = tokens u0 - 3 ..
-      load8<A>(tile, (int64_t)(u0 + 1) * ROW + cb, r1);
-      load8<A>(tile, (int64_t)(u0 + 2) * ROW + cb, r2);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        p0[q] = make_float2(r0[2 * q], r0[2 * q + 1]);
-        p1[q] = make_float2(r1[2 * q], r1[2 * q + 1]);
-        p2[q] = make_float2(r2[2 * q], r2[2 * q + 1]);
+  const int grp = warp >> 1;
+  const int hb = (warp & 1) * 2 + (lane >> 4);            // head within the item
+  const int u0 = grp * CONV_TOK;                          // this thread's first token in the chunk
+  bool failed = false;
+  for (int64_t k = 0; k < n_mine_items; ++k) {
+    if (warp == 0) {                                      // the item NS - 1 ahead goes in flight
+      const int64_t i = k + NS - 1;
+      if (i < n_mine_items) {
+        const int sti = (int)(i % NS);
+        bool ok = true;
+        if (i >= NS) ok = tc::mbar_wait(&empty[sti], (uint32_t)((i / NS - 1) & 1), 1u << 24);
+        if (__all_sync(FULL, ok)) produce(blockIdx.x + i * stride, sti);
+        else failed = true;
       }
     }
-    // 16 tokens in pairs, fully unrolled so the three-row window rotates through
-    // registers. A pair's second token may lie past the chunk's end: its tile
-    // row was not staged and its values are discarded.
+    const int st = (int)(k % NS);
+    if (!failed) failed = !tc::mbar_wait(&bar[st], (uint32_t)((k / NS) & 1), 1u << 24);
+    if (failed || *reinterpret_cast<volatile int*>(&abort_flag)) {   // a wait gave up: stop
+      if (lane == 0) {
+        abort_flag = 1;
+        report(dev_err, GDN_DEVERR_TIMEOUT);
+      }
+      break;
+    }
+    const ConvItem m = meta[st];
+    if (!(m.flags & CI_VALID)) {
+      if (m.ci == 0 && m.head0 == 0 && tid == 0 && m.flags)
+        report(dev_err, m.flags & CI_BAD_SLOT ? GDN_DEVERR_SLOT : GDN_DEVERR_SEQLENS);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[st]);          // this warp is done with the stage
+      continue;
+    }
+    const uint8_t* tile = tiles + (size_t)st * TILE + (size_t)(warp & 1) * HALF;   // this warp's half
+    const int slot = m.slot;
+    const int64_t seq0 = m.seq0, len = m.len, t_chunk = m.t_chunk;
+    const int n_here = m.n_here;
+    const int heads_here = min(CONV_HEADS_PER_BLOCK, n_heads - m.head0);
+    const int head = m.head0 + hb;
+    const bool active = hb < heads_here;                  // uniform per 16 lanes
+    const bool is_qk = head < 2 * n_qk;
+    const int c0 = head * D + (lane & 15) * 8;            // global channel
+    const int cb = (hb & 1) * D + (lane & 15) * 8;        // channel within a row of the half
+    const int n_mine = max(0, min(CONV_TOK, n_here - u0)); // uniform per warp
+    const bool zero_halo = u0 == 0 && !(m.flags & (CI_HALO_X | CI_HALO_STATE));
+
+    if (n_mine > 0) {
+      float2 w[4][4];                                     // [channel pair][tap]
+      float2 p0[4], p1[4], p2[4];                         // the three previous rows
+      {
+        Raw8<A> wr[4];
+        if (active) {
 #pragma unroll
-    for (int u = 0; u < CONV_TOK; u += 2) {
-      if (u >= n_mine) break;                             // uniform per warp
-      float v[2][8];
+          for (int q = 0; q < 4; ++q) raw_load<A>(conv_w, (int64_t)c0 * KW + 8 * q, wr[q]);
+        } else {
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        float xv[8];
-        load8<A>(tile, (int64_t)(u0 + u + k + KS) * ROW + cb, xv);
+          for (int q = 0; q < 4; ++q) raw_zero<A>(wr[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {                     // channels 2q, 2q+1: 8 taps
+          float t8[8];
+          raw_unpack<A>(wr[q], t8);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) w[q][jj] = make_float2(t8[jj], t8[4 + jj]);
+        }
+        float r0[8], r1[8], r2[8];
+        if (zero_halo) {                                  // chunk 0 without initial rows
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) { r0[jj] = 0.f; r1[jj] = 0.f; r2[jj] = 0.f; }
+        } else {
+          load8<A>(tile, (int64_t)u0 * ROW + cb, r0);    // tile rows u0 .. u0 + 2 = tokens u0 - 3 ..
+          load8<A>(tile, (int64_t)(u0 + 1) * ROW + cb, r1);
+          load8<A>(tile, (int64_t)(u0 + 2) * ROW + cb, r2);
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float2 cv = make_float2(xv[2 * q], xv[2 * q + 1]);
-          const float2 a = silu2(conv4x2(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cv));
-          v[k][2 * q] = a.x;
-          v[k][2 * q + 1] = a.y;
-          p0[q] = p1[q]; p1[q] = p2[q]; p2[q] = cv;
+          p0[q] = make_float2(r0[2 * q], r0[2 * q + 1]);
+          p1[q] = make_float2(r1[2 * q], r1[2 * q + 1]);
+          p2[q] = make_float2(r2[2 * q], r2[2 * q + 1]);
         }
       }
-      if constexpr (NORM) {
-        const float ss0 = head_sum_sq16(v[0]);            // all lanes take part
-        const float ss1 = head_sum_sq16(v[1]);
-        const float rm = inv_norm((lane & 1) ? ss1 : ss0, eps);   // even lanes token u, odd u + 1
-        const float r0 = __shfl_sync(FULL, rm, lane & ~1);
-        const float r1 = __shfl_sync(FULL, rm, lane | 1);
-        if (is_qk) {
+      // 8 tokens in pairs, fully unrolled so the three-row window rotates through
+      // registers. A pair's second token may lie past the chunk's end: its tile
+      // row was not staged and its values are discarded.
+#pragma unroll
+      for (int u = 0; u < CONV_TOK; u += 2) {
+        if (u >= n_mine) break;                           // uniform per warp
+        float v[2][8];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          float xv[8];
+          load8<A>(tile, (int64_t)(u0 + u + kk + KS) * ROW + cb, xv);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float2 o0 = __fmul2_rn(make_float2(v[0][2 * q], v[0][2 * q + 1]), make_float2(r0, r0));
-            const float2 o1 = __fmul2_rn(make_float2(v[1][2 * q], v[1][2 * q + 1]), make_float2(r1, r1));
-            v[0][2 * q] = o0.x; v[0][2 * q + 1] = o0.y;
-            v[1][2 * q] = o1.x; v[1][2 * q + 1] = o1.y;
+            const float2 cv = make_float2(xv[2 * q], xv[2 * q + 1]);
+            const float2 a = silu2(conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cv));
+            v[kk][2 * q] = a.x;
+            v[kk][2 * q + 1] = a.y;
+            p0[q] = p1[q]; p1[q] = p2[q]; p2[q] = cv;
           }
         }
-      }
-      if (active) {
-        store8<A>(y, (t_chunk + u0 + u) * ld_y + c0, v[0]);
-        if (u + 1 < n_mine) store8<A>(y, (t_chunk + u0 + u + 1) * ld_y + c0, v[1]);
+        if constexpr (NORM) {
+          const float ss0 = head_sum_sq16(v[0]);          // all lanes take part
+          const float ss1 = head_sum_sq16(v[1]);
+          const float rm = inv_norm((lane & 1) ? ss1 : ss0, eps);   // even lanes token u, odd u + 1
+          const float rn0 = __shfl_sync(FULL, rm, lane & ~1);
+          const float rn1 = __shfl_sync(FULL, rm, lane | 1);
+          if (is_qk) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float2 o0 = __fmul2_rn(make_float2(v[0][2 * q], v[0][2 * q + 1]), make_float2(rn0, rn0));
+              const float2 o1 = __fmul2_rn(make_float2(v[1][2 * q], v[1][2 * q + 1]), make_float2(rn1, rn1));
+              v[0][2 * q] = o0.x; v[0][2 * q + 1] = o0.y;
+              v[1][2 * q] = o1.x; v[1][2 * q + 1] = o1.y;
+            }
+          }
+        }
+        if (active) {
+          store8<A>(y, (t_chunk + u0 + u) * ld_y + c0, v[0]);
+          if (u + 1 < n_mine) store8<A>(y, (t_chunk + u0 + u + 1) * ld_y + c0, v[1]);
+        }
       }
     }
-  }
 
-  // Final conv_state: rows len, len+1, len+2 of (initial rows ++ x rows),
-  // written by the thread that read the initial rows, after its last read.
-  // When len < 3 new row r is old row len + r >= r; rows are rewritten in
-  // ascending order, so each old row is read before it is overwritten.
-  if (owner && active) {
+    // Final conv_state: rows len, len+1, len+2 of (initial rows ++ x rows),
+    // written by the thread that read the initial rows (through the tile), after
+    // its last read. When len < 3 new row r is old row len + r >= r; rows are
+    // rewritten in ascending order, so each old row is read before it is
+    // overwritten.
+    if (m.ci == 0 && grp == 0 && active) {
+      const bool hi = (m.flags & CI_HALO_STATE) != 0;
+      const int64_t st_base = (int64_t)slot * KS * C;
 #pragma unroll
-    for (int r = 0; r < 3; ++r) {
-      const int64_t idx = len + r;
-      float v[8];
-      if (idx >= 3) load8<A>(x, (seq0 + idx - 3) * ld_x + c0, v);
-      else if (hi) load8<A>(conv_state, st_base + idx * C + c0, v);
-      else {
+      for (int r = 0; r < 3; ++r) {
+        const int64_t idx = len + r;
+        float v[8];
+        if (idx >= 3) load8<A>(x, (seq0 + idx - 3) * ld_x + c0, v);
+        else if (hi) load8<A>(conv_state, st_base + idx * C + c0, v);
+        else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = 0.f;
+          for (int jj = 0; jj < 8; ++jj) v[jj] = 0.f;
+        }
+        store8<A>(conv_state, st_base + (int64_t)r * C + c0, v);
       }
-      store8<A>(conv_state, st_base + (int64_t)r * C + c0, v);
     }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&empty[st]);            // this warp is done with the stage
+  }
+  // Before the block exits no copy into its shared memory may still be in
+  // flight: after a failed wait, wait (bounded) for the last copy of each stage.
+  __syncthreads();
+  if (abort_flag && warp == 0) {
+    for (int64_t i = n_produced > NS ? n_produced - NS : 0; i < n_produced; ++i)
+      tc::mbar_wait(&bar[i % NS], (uint32_t)((i / NS) & 1), 1u << 24);
   }
 }
 
@@ -238,8 +366,8 @@ postconv_norm_kernel(const void* __restrict__ yin, void* __restrict__ yout, int6
 
 // ------------------------------------------------------------------ launchers
 template <int A, bool NORM, typename... Args>
-static cudaError_t launch_conv_variant(dim3 grid, cudaStream_t stream, Args... args) {
-  const int smem = conv_tile_bytes<A>();
+static cudaError_t launch_conv_variant(unsigned grid, cudaStream_t stream, Args... args) {
+  const int smem = conv_stages<A>() * conv_tile_bytes<A>();
   cudaError_t e = set_smem_once<conv_fwd_kernel<A, NORM>>(smem);
   if (e != cudaSuccess) return e;
   conv_fwd_kernel<A, NORM><<<grid, CONV_THREADS, smem, stream>>>(args...);
@@ -251,12 +379,34 @@ cudaError_t launch_conv_fwd(const gdn_config& cfg, const void* x, int64_t ld_x, 
                             const int32_t* slot_idx, const int32_t* cu, const uint8_t* has_init,
                             int n_seq, int64_t n_tok, int fuse_norm, cudaStream_t stream) {
   const int n_heads = 2 * cfg.n_qk_heads + cfg.n_v_heads;
+  const int n_hgroups = (n_heads + CONV_HEADS_PER_BLOCK - 1) / CONV_HEADS_PER_BLOCK;
+  // chunks of all sequences: at most ceil(n_tok / 64) + n_seq (every sequence,
+  // empty ones too, owns at least one); items past the last chunk are skipped
   const int64_t max_chunks = (n_tok + CHUNK - 1) / CHUNK + n_seq;
-  dim3 grid((unsigned)max_chunks, (n_heads + CONV_HEADS_PER_BLOCK - 1) / CONV_HEADS_PER_BLOCK);
+  const int64_t n_items = max_chunks * n_hgroups;
+  int n_sm = 0;
+  cudaError_t e = sm_count(&n_sm);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(n_items < n_sm ? n_items : n_sm);   // one block per SM
+  // x as a 2-D tensor [n_tok rows][C columns], row pitch ld_x, boxes of 256 x 64
+  CUtensorMap xmap;
+  {
+    const EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const int es = cfg.act == GDN_BF16 ? 2 : 4;
+    const cuuint64_t dims[2] = {(cuuint64_t)(n_heads * D), (cuuint64_t)(n_tok > 0 ? n_tok : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld_x * es};
+    const cuuint32_t box[2] = {(cuuint32_t)CONV_HALF_COLS, (cuuint32_t)CHUNK};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&xmap, cfg.act == GDN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                           2, const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
 #define GDN_CONV_ARGS                                                                     \
   x, ld_x, y, ld_y, conv_w, conv_state, slot_idx, cu, has_init, n_seq, n_tok, n_heads,   \
-      cfg.n_qk_heads, cfg.n_slots, cfg.eps, cfg.dev_err
-  cudaError_t e;
+      cfg.n_qk_heads, cfg.n_slots, cfg.eps, cfg.dev_err, n_items, n_hgroups, xmap
   if (cfg.act == GDN_BF16) {
     e = fuse_norm ? launch_conv_variant<BF16, true>(grid, stream, GDN_CONV_ARGS)
                   : launch_conv_variant<BF16, false>(grid, stream, GDN_CONV_ARGS);

@@ -25,7 +25,29 @@ gdn_status check_cfg(const gdn_config* cfg) {
   if (!(cfg->eps >= 0.f)) return GDN_ERR_INVALID;
   if (cfg->dev_err && (reinterpret_cast<uintptr_t>(cfg->dev_err) & 3u)) return GDN_ERR_INVALID;
   if (cfg->gates != GDN_GATES_ACTIVATED && cfg->gates != GDN_GATES_RAW) return GDN_ERR_INVALID;
+  if (cfg->gate_dtype != GDN_F32 && cfg->gate_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (cfg->out_f32 != 0 && cfg->out_f32 != 1) return GDN_ERR_INVALID;
   return GDN_OK;
+}
+
+// Bytes of one element of `out`.
+size_t out_esize(const gdn_config* cfg) { return cfg->out_f32 ? 4 : (cfg->act == GDN_BF16 ? 2 : 4); }
+
+// The arguments shared by the step launches (verify, decode, commit, lazy).
+gdn::StepArgs step_args(const gdn_config* cfg, int B, int T) {
+  gdn::StepArgs a{};
+  a.B = B;
+  a.T = T;
+  a.Hk = cfg->n_qk_heads;
+  a.Hv = cfg->n_v_heads;
+  a.n_slots = cfg->n_slots;
+  a.eps = cfg->eps;
+  a.q_scale = cfg->q_scale;
+  a.dev_err = cfg->dev_err;
+  a.raw_gates = cfg->gates == GDN_GATES_RAW;
+  a.gate_bf16 = cfg->gate_dtype == GDN_BF16;
+  a.out_f32 = cfg->out_f32;
+  return a;
 }
 
 int64_t channels(const gdn_config* cfg) {
@@ -96,8 +118,8 @@ gdn_status gdn_postconv_norm(const gdn_config* cfg, int32_t in_t, const void* y_
                                              static_cast<cudaStream_t>(stream)));
 }
 
-gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const float* alpha,
-                             const float* beta, const void* z, const float* norm_w, void* out,
+gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const void* alpha,
+                             const void* beta, const void* z, const float* norm_w, void* out,
                              float* state, const int32_t* slot_idx, const int32_t* cu_seqlens,
                              const uint8_t* has_init, int32_t n_seq, int64_t n_tok,
                              int32_t chunk, void* stream) {
@@ -110,15 +132,20 @@ gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const float
       !has_init)
     return GDN_ERR_INVALID;
   if (!aligned16(qkv) || !aligned16(z) || !aligned16(out) || !aligned16(state)) return GDN_ERR_INVALID;
-  const size_t es = esize(cfg->act);
+  const size_t es = esize(cfg->act), eo = out_esize(cfg);
   const size_t HvD = (size_t)cfg->n_v_heads * GDN_HEAD_DIM;
-  if (overlap(out, (size_t)n_tok * HvD * es, qkv, (size_t)n_tok * channels(cfg) * es) ||
-      overlap(out, (size_t)n_tok * HvD * es, z, (size_t)n_tok * HvD * es))
+  if (overlap(out, (size_t)n_tok * HvD * eo, qkv, (size_t)n_tok * channels(cfg) * es) ||
+      overlap(out, (size_t)n_tok * HvD * eo, z, (size_t)n_tok * HvD * es))
     return GDN_ERR_INVALID;
   if (n_seq > 65535) return GDN_ERR_UNSUPPORTED;
-  gdn::PrefillArgs a{qkv, alpha, beta, z, norm_w, out, state, slot_idx, cu_seqlens, has_init,
-                     n_seq, cfg->n_qk_heads, cfg->n_v_heads, cfg->n_slots, n_tok, cfg->eps,
-                     cfg->q_scale, cfg->dev_err, cfg->gates == GDN_GATES_RAW};
+  gdn::PrefillArgs a{};
+  a.qkv = qkv; a.alpha = alpha; a.beta = beta; a.z = z; a.norm_w = norm_w; a.out = out;
+  a.state = state; a.slot_idx = slot_idx; a.cu = cu_seqlens; a.has_init = has_init;
+  a.n_seq = n_seq; a.Hk = cfg->n_qk_heads; a.Hv = cfg->n_v_heads; a.n_slots = cfg->n_slots;
+  a.n_tok = n_tok; a.eps = cfg->eps; a.q_scale = cfg->q_scale; a.dev_err = cfg->dev_err;
+  a.raw_gates = cfg->gates == GDN_GATES_RAW;
+  a.gate_bf16 = cfg->gate_dtype == GDN_BF16;
+  a.out_f32 = cfg->out_f32;
   return from_cuda(gdn::launch_prefill(a, cfg->act, static_cast<cudaStream_t>(stream)));
 }
 
@@ -128,8 +155,8 @@ int64_t gdn_verify_workspace_bytes(const gdn_config* cfg, int32_t B, int32_t T) 
 }
 
 gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* conv_w,
-                           void* conv_state, float* state, const float* alpha,
-                           const float* beta, const void* z, const float* norm_w, void* out,
+                           void* conv_state, float* state, const void* alpha,
+                           const void* beta, const void* z, const float* norm_w, void* out,
                            const int32_t* slot_idx, int32_t B, int32_t T, uint32_t flags,
                            void* postconv_out, void* workspace, int64_t workspace_bytes,
                            void* stream) {
@@ -146,23 +173,29 @@ gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* con
       !aligned16(z) || !aligned16(out) || !aligned16(norm_w) ||
       (postconv_out && !aligned16(postconv_out)))
     return GDN_ERR_INVALID;
-  const size_t es = esize(cfg->act);
+  const size_t es = esize(cfg->act), eo = out_esize(cfg);
   const size_t HvD = (size_t)cfg->n_v_heads * GDN_HEAD_DIM, nt = (size_t)B * T;
-  if (overlap(out, nt * HvD * es, x, nt * channels(cfg) * es) ||
-      overlap(out, nt * HvD * es, z, nt * HvD * es))
+  const size_t C = (size_t)channels(cfg);
+  if (overlap(out, nt * HvD * eo, x, nt * C * es) || overlap(out, nt * HvD * eo, z, nt * HvD * es))
+    return GDN_ERR_INVALID;
+  // the post-conv copy is written while other blocks still read x, z and the pools
+  if (postconv_out && (overlap(postconv_out, nt * C * es, x, nt * C * es) ||
+                       overlap(postconv_out, nt * C * es, z, nt * HvD * es) ||
+                       overlap(postconv_out, nt * C * es, out, nt * HvD * eo)))
     return GDN_ERR_INVALID;
   if (workspace_bytes < 0 || (!workspace && workspace_bytes != 0)) return GDN_ERR_INVALID;
-  gdn::StepArgs a{x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, postconv_out,
-                  slot_idx, nullptr, nullptr, B, T, cfg->n_qk_heads, cfg->n_v_heads,
-                  cfg->n_slots, cfg->eps, cfg->q_scale, cfg->dev_err, cfg->gates == GDN_GATES_RAW};
+  gdn::StepArgs a = step_args(cfg, B, T);
+  a.x = x; a.conv_w = conv_w; a.conv_state = conv_state; a.state = state; a.alpha = alpha;
+  a.beta = beta; a.z = z; a.norm_w = norm_w; a.out = out; a.postconv = postconv_out;
+  a.slot_idx = slot_idx;
   return from_cuda(gdn::launch_verify(a, (flags & GDN_VERIFY_COMMIT_ALL) != 0, cfg->act,
                                       static_cast<cudaStream_t>(stream)));
 }
 
-gdn_status gdn_verify_step_lazy(const gdn_config* cfg, const void* prev_x, const float* prev_alpha,
-                                const float* prev_beta, const int32_t* prev_n_keep, int32_t prev_T,
+gdn_status gdn_verify_step_lazy(const gdn_config* cfg, const void* prev_x, const void* prev_alpha,
+                                const void* prev_beta, const int32_t* prev_n_keep, int32_t prev_T,
                                 const void* x, const void* conv_w, void* conv_state, float* state,
-                                const float* alpha, const float* beta, const void* z,
+                                const void* alpha, const void* beta, const void* z,
                                 const float* norm_w, void* out, const int32_t* slot_idx, int32_t B,
                                 int32_t T, void* postconv_out, void* stream) {
   gdn_status st = check_cfg(cfg);
@@ -178,16 +211,22 @@ gdn_status gdn_verify_step_lazy(const gdn_config* cfg, const void* prev_x, const
       !aligned16(state) || !aligned16(z) || !aligned16(out) || !aligned16(norm_w) ||
       (postconv_out && !aligned16(postconv_out)))
     return GDN_ERR_INVALID;
-  const size_t es = esize(cfg->act);
+  const size_t es = esize(cfg->act), eo = out_esize(cfg);
   const size_t HvD = (size_t)cfg->n_v_heads * GDN_HEAD_DIM, C = (size_t)channels(cfg);
   const size_t nt = (size_t)B * T, np = (size_t)B * prev_T;
-  if (overlap(out, nt * HvD * es, x, nt * C * es) || overlap(out, nt * HvD * es, z, nt * HvD * es) ||
-      overlap(out, nt * HvD * es, prev_x, np * C * es))
+  if (overlap(out, nt * HvD * eo, x, nt * C * es) || overlap(out, nt * HvD * eo, z, nt * HvD * es) ||
+      overlap(out, nt * HvD * eo, prev_x, np * C * es))
     return GDN_ERR_INVALID;
-  gdn::StepArgs a{x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, postconv_out,
-                  slot_idx, prev_n_keep, nullptr, B, T, cfg->n_qk_heads, cfg->n_v_heads,
-                  cfg->n_slots, cfg->eps, cfg->q_scale, cfg->dev_err, cfg->gates == GDN_GATES_RAW,
-                  prev_x, prev_alpha, prev_beta, prev_T};
+  if (postconv_out && (overlap(postconv_out, nt * C * es, x, nt * C * es) ||
+                       overlap(postconv_out, nt * C * es, z, nt * HvD * es) ||
+                       overlap(postconv_out, nt * C * es, out, nt * HvD * eo) ||
+                       overlap(postconv_out, nt * C * es, prev_x, np * C * es)))
+    return GDN_ERR_INVALID;
+  gdn::StepArgs a = step_args(cfg, B, T);
+  a.x = x; a.conv_w = conv_w; a.conv_state = conv_state; a.state = state; a.alpha = alpha;
+  a.beta = beta; a.z = z; a.norm_w = norm_w; a.out = out; a.postconv = postconv_out;
+  a.slot_idx = slot_idx; a.n_keep = prev_n_keep;
+  a.prev_x = prev_x; a.prev_alpha = prev_alpha; a.prev_beta = prev_beta; a.prev_T = prev_T;
   return from_cuda(gdn::launch_verify_lazy(a, cfg->act, static_cast<cudaStream_t>(stream)));
 }
 
@@ -201,27 +240,32 @@ gdn_status gdn_commit_layers(const gdn_config* cfg, const gdn_layer_view* layers
   if (B > 65535 || L > 65535) return GDN_ERR_UNSUPPORTED;
   if (!layers || !slot_idx || !n_keep || (reinterpret_cast<uintptr_t>(layers) & 7u))
     return GDN_ERR_INVALID;
-  gdn::StepArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                  nullptr, nullptr, slot_idx, n_keep, layers, B, T, cfg->n_qk_heads,
-                  cfg->n_v_heads, cfg->n_slots, cfg->eps, 1.0f, cfg->dev_err,
-                  cfg->gates == GDN_GATES_RAW};
+  gdn::StepArgs a = step_args(cfg, B, T);
+  a.q_scale = 1.0f;
+  a.slot_idx = slot_idx; a.n_keep = n_keep; a.layers = layers;
   return from_cuda(gdn::launch_commit(a, L, cfg->act, static_cast<cudaStream_t>(stream)));
 }
 
-gdn_status gdn_gates(const gdn_config* cfg, const float* a, const float* b, float* alpha,
-                     float* beta, int64_t n_tok, void* stream) {
+gdn_status gdn_gates(const gdn_config* cfg, const void* a, const void* b, void* alpha,
+                     void* beta, int64_t n_tok, void* stream) {
   if (!cfg) return GDN_ERR_INVALID;
   if (cfg->n_v_heads < 1 || n_tok < 0) return GDN_ERR_INVALID;
+  if (cfg->gate_dtype != GDN_F32 && cfg->gate_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if (n_tok == 0) return GDN_OK;
   if (!a || !b || !alpha || !beta) return GDN_ERR_INVALID;
   const int64_t n = n_tok * cfg->n_v_heads;
   if (n / cfg->n_v_heads != n_tok) return GDN_ERR_INVALID;
-  const size_t nb = (size_t)n * sizeof(float);
+  const size_t ge = cfg->gate_dtype == GDN_BF16 ? 2 : 4;
+  if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(alpha) |
+       reinterpret_cast<uintptr_t>(beta)) & (ge - 1))
+    return GDN_ERR_INVALID;
+  const size_t nb = (size_t)n * ge;
   // in place is allowed (alpha = a, beta = b); any other overlap is not
   if ((alpha != a && overlap(alpha, nb, a, nb)) || (beta != b && overlap(beta, nb, b, nb)) ||
       overlap(alpha, nb, beta, nb) || overlap(alpha, nb, b, nb) || overlap(beta, nb, a, nb))
     return GDN_ERR_INVALID;
-  return from_cuda(gdn::launch_gates(a, b, alpha, beta, n, static_cast<cudaStream_t>(stream)));
+  return from_cuda(gdn::launch_gates(a, b, alpha, beta, n, cfg->gate_dtype == GDN_BF16,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -56,8 +56,8 @@ struct StepArgs {
   const void* conv_w;       // [C][4]
   void* conv_state;         // pool
   float* state;             // pool
-  const float* alpha;       // [B][T][Hv]
-  const float* beta;
+  const void* alpha;        // [B][T][Hv] gate dtype
+  const void* beta;
   const void* z;            // [B][T][Hv*D]
   const float* norm_w;      // [D]
   void* out;                // [B][T][Hv*D]
@@ -69,17 +69,19 @@ struct StepArgs {
   float eps, q_scale;
   uint32_t* dev_err;
   int raw_gates;            // alpha / beta hold raw projections: apply the gate step
+  int gate_bf16;            // gate arrays hold bf16 values
+  int out_f32;              // out is f32 (else the activation dtype)
   // verify with the previous window's commit folded in (n_keep: its accepted prefixes)
   const void* prev_x;       // [B][prev_T][C]
-  const float* prev_alpha;  // [B][prev_T][Hv]
-  const float* prev_beta;
+  const void* prev_alpha;   // [B][prev_T][Hv]
+  const void* prev_beta;
   int prev_T;
 };
 
 struct PrefillArgs {
   const void* qkv;
-  const float* alpha;
-  const float* beta;
+  const void* alpha;        // [n_tok][Hv] gate dtype
+  const void* beta;
   const void* z;
   const float* norm_w;
   void* out;
@@ -92,6 +94,8 @@ struct PrefillArgs {
   float eps, q_scale;
   uint32_t* dev_err;
   int raw_gates;            // alpha / beta hold raw projections: apply the gate step
+  int gate_bf16;            // gate arrays hold bf16 values
+  int out_f32;              // out is f32 (else the activation dtype)
 };
 
 // Encodes a 2-D row-major bf16 tensor map (rows x cols, row pitch in elements)
@@ -116,7 +120,7 @@ cudaError_t launch_commit(const StepArgs& a, int L, int act, cudaStream_t stream
 cudaError_t launch_verify_lazy(const StepArgs& a, int act, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, int act, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
-cudaError_t launch_gates(const float* a, const float* b, float* alpha, float* beta, int64_t n,
+cudaError_t launch_gates(const void* a, const void* b, void* alpha, void* beta, int64_t n, int bf16,
                          cudaStream_t stream);
 
 }  // namespace gdn

@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_ffma_kernel(PrefillArgs
     if (warp == 0) {                       // chunk-local log-decay scan (2 tokens per lane)
       const int t0 = 2 * lane;
       // raw projections: the gate step on the values read
-      auto alpha_of = [&](int64_t gi) { const float v = p.alpha[gi]; return p.raw_gates ? gate_alpha(v) : v; };
-      auto beta_of = [&](int64_t gi) { const float v = p.beta[gi]; return p.raw_gates ? gate_beta(v) : v; };
+      auto alpha_of = [&](int64_t gi) { const float v = load_gate(p.alpha, gi, p.gate_bf16); return p.raw_gates ? gate_alpha(v) : v; };
+      auto beta_of = [&](int64_t gi) { const float v = load_gate(p.beta, gi, p.gate_bf16); return p.raw_gates ? gate_beta(v) : v; };
       const float la0 = t0 < m ? logf(alpha_of((c0 + t0) * Hv + h)) : 0.f;
       const float la1 = t0 + 1 < m ? logf(alpha_of((c0 + t0 + 1) * Hv + h)) : 0.f;
       const float pair = la0 + la1;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_ffma_kernel(PrefillArgs
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu_gate(zv[j]));
-        store8<A>(p.out, zo, res);
+        store_out8<A>(p.out, zo, res, p.out_f32);
       }
     }
     __syncthreads();

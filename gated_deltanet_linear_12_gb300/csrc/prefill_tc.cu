@@ -259,8 +259,14 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
     }
     if (tid < C64) {
       const int t = tid, tt = t < pm ? t : 0;
-      cp_async4(al_raw + t, p.alpha + (pc0 + tt) * Hv + h, t < pm ? 4u : 0u);
-      cp_async4(b_s + t, p.beta + (pc0 + tt) * Hv + h, t < pm ? 4u : 0u);
+      const int64_t gi = (pc0 + tt) * Hv + h;
+      if (p.gate_bf16) {                                 // 2-byte gates: plain loads
+        al_raw[t] = t < pm ? load_gate(p.alpha, gi, 1) : 0.f;
+        b_s[t] = t < pm ? load_gate(p.beta, gi, 1) : 0.f;
+      } else {
+        cp_async4(al_raw + t, static_cast<const float*>(p.alpha) + gi, t < pm ? 4u : 0u);
+        cp_async4(b_s + t, static_cast<const float*>(p.beta) + gi, t < pm ? 4u : 0u);
+      }
     }
     cp_async_commit();
   };
@@ -299,7 +305,7 @@ prefill_tc_kernel(PrefillArgs p, const __grid_constant__ CUtensorMap vmap, const
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[it][j], r), nw[j]), silu_gate(zv[it][j]));
-            store8<BF16>(p.out, (ec0 + t) * Hv * D + (int64_t)h * D + l16 * 8, res);
+            store_out8<BF16>(p.out, (ec0 + t) * Hv * D + (int64_t)h * D + l16 * 8, res, p.out_f32);
           }
         }
       }

@@ -40,8 +40,9 @@ constexpr int MAX_HEADS = 16;                    // v heads per block (Hv / Hk l
 
 
 // Post-conv activation of 8 channels of draft token t: rows t..t+3 of
-// (conv_state rows ++ draft rows), SiLU, then (q/k heads) the L2 norm, rounded
-// to the activation type. All 32 lanes of the warp must call it together.
+// (conv_state rows ++ draft rows), SiLU, then (q/k heads) the L2 norm, in f32:
+// the recurrence takes them unrounded (they are never stored on this path).
+// All 32 lanes of the warp must call it together.
 template <int A>
 __device__ __forceinline__ void draft_act8(const void* __restrict__ x_b, const void* __restrict__ cs,
                                            const void* __restrict__ conv_w, int C, int c, int t,
@@ -74,8 +75,6 @@ __device__ __forceinline__ void draft_act8(const void* __restrict__ x_b, const v
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], r);
   }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = round_act<A>(v[j]);
 }
 
 // Warp dot product of two 128-vectors in shared memory; every lane gets the
@@ -124,8 +123,8 @@ __device__ __forceinline__ void rows_dot(const float4 (&S)[2][8], const float* v
 // with VIEWS those of layer blockIdx.z of the view table. Returns false when the
 // sequence is skipped (padding, or a bad slot or n_keep, reported).
 template <int A, int MODE, bool VIEWS>
-__device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, const float* alpha,
-                                          const float* beta, const int T, float* smem) {
+__device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, const void* alpha,
+                                          const void* beta, const int T, float* smem) {
   constexpr bool OUTPUTS = MODE != COMMIT;
   constexpr bool WRITES = MODE != VERIFY_ONLY;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -203,7 +202,7 @@ __device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, cons
   for (int e = tid; e < nh * n; e += STEP_THREADS) {
     const int g = e / n, t = e % n;
     const int64_t gi = ((int64_t)b * T + t) * Hv + h0 + g;
-    const float ga = alpha[gi], gb = beta[gi];
+    const float ga = load_gate(alpha, gi, p.gate_bf16), gb = load_gate(beta, gi, p.gate_bf16);
     al_s[g * MAXT + t] = p.raw_gates ? gate_alpha(ga) : ga;      // raw projections: the gate step
     be_s[g * MAXT + t] = p.raw_gates ? gate_beta(gb) : gb;
   }
@@ -410,7 +409,7 @@ __device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, cons
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             res[j] = __fmul_rn(__fmul_rn(__fmul_rn(o[j], r), p.norm_w[l16 * 8 + j]), silu_gate(zv[j]));
-          store8<A>(p.out, zo, res);
+          store_out8<A>(p.out, zo, res, p.out_f32);
         }
       }
     }

@@ -20,7 +20,10 @@
 // is both a bank-conflict-free row for thread r and the canonical K-major
 // operand layout of the tensor core. The block computes its q, k and v conv rows
 // itself (the two v heads of a q/k head each redo the q, k part: sharing it
-// through memory was measured slower), and
+// through memory was measured slower); thread r convolves v channel r itself, so
+// v_t[r] stays in its registers. The activations enter the recurrence unrounded
+// (f32); only the optional post-conv copy is rounded to the activation dtype.
+// Then
 //   - T <= 4 (and f32 activations): the 2T dot products of every row on the CUDA
 //     cores, in the step kernel's order, so that at T = 1 the outputs are
 //     bitwise equal to those of the decode mode;
@@ -116,15 +119,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 //       the outputs o_t (f32 [T][128])
 //   SR  the state, four TMA boxes [32 columns][128 rows] f32, 128-byte swizzle
 //       (1024-byte aligned)
-//   VS  v rows [8][128] (activation dtype)
+//   VS  v rows [T][128] f32 (CUDA-core variants; the tensor-core one keeps v in
+//       registers)
 //   TB  the table of gate products and dot products (TAB floats)
 //   GS  alpha, beta of this head [2][8]
-//   BR  the state, product and Gram barriers, the TMEM address
+//   BR  the state, product and Gram barriers, the TMEM address, the issued flag
 template <int A, bool TC> __host__ __device__ constexpr int qk_bytes() { return 2 * MAXT * D * 4; }
 template <int A, bool TC> __host__ __device__ constexpr int qk_region() { return (qk_bytes<A, TC>() + 1023) & ~1023; }
-template <int A> __host__ __device__ constexpr int rows_bytes() { return MAXT * D * (A == BF16 ? 2 : 4); }
-template <int A, bool TC> __host__ __device__ constexpr int verify_smem() {
-  return qk_region<A, TC>() + S_BYTES + rows_bytes<A>() + TAB * 4 + 2 * MAXT * 4 + 32;
+// v rows [NT][128] f32 of the CUDA-core variants (the tensor-core variant keeps
+// them in registers)
+template <bool TC, int NT> __host__ __device__ constexpr int vs_bytes() { return TC ? 0 : NT * D * 4; }
+template <int A, bool TC, int NT> __host__ __device__ constexpr int verify_smem() {
+  return qk_region<A, TC>() + S_BYTES + vs_bytes<TC, NT>() + TAB * 4 + 2 * MAXT * 4 + 32;
 }
 
 // Byte offset of f32 element (row, k) of the [16][128] tf32 operand in the
@@ -149,9 +155,14 @@ __device__ __forceinline__ void put_act8(uint8_t* QK, int which, int t, int c, c
   *reinterpret_cast<float4*>(QK + bsw_off(8 * which + t, c + 4)) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-template <int A> __device__ __forceinline__ float row_at(const uint8_t* R, int t, int i) {
-  if constexpr (A == BF16) return bf2f(reinterpret_cast<const uint16_t*>(R)[t * D + i]);
-  else return reinterpret_cast<const float*>(R)[t * D + i];
+// One activation of `base` widened to f32, and one stored (rounded) from f32.
+template <int A> __device__ __forceinline__ float load1(const void* base, int64_t i) {
+  if constexpr (A == BF16) return bf2f(static_cast<const uint16_t*>(base)[i]);
+  else return static_cast<const float*>(base)[i];
+}
+template <int A> __device__ __forceinline__ void store1(void* base, int64_t i, float v) {
+  if constexpr (A == BF16) static_cast<uint16_t*>(base)[i] = f2bf(v);
+  else static_cast<float*>(base)[i] = v;
 }
 
 // Programmatic dependent launch: let the next grid start / wait for the previous one.
@@ -207,7 +218,8 @@ __device__ __forceinline__ void hint_rows(const StepArgs& p, int u, int T, int w
   }
 }
 
-// Resident blocks per SM (shared memory: bf16 76.5 KB, f32 79.6 KB per block).
+// Resident blocks per SM (shared memory at most 74.7 KiB per bf16 block, 76.7
+// KiB per f32 block).
 template <int A> __host__ __device__ constexpr int blocks_per_sm() { return A == BF16 ? 3 : 2; }
 
 // One block per (sequence b, v head h), launched as a programmatic dependent of
@@ -250,17 +262,19 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
 
   uint8_t* QK = smem;                                     // q, k; then the outputs
   uint8_t* SR = smem + qk_region<A, TC>();                // the state
-  uint8_t* VS = SR + S_BYTES;                             // v rows
-  float* tb = reinterpret_cast<float*>(VS + rows_bytes<A>());       // the table
+  uint8_t* VS = SR + S_BYTES;                             // v rows (CUDA-core variants)
+  float* tb = reinterpret_cast<float*>(VS + vs_bytes<TC, NT>());    // the table
   float* al_s = tb + TAB;                                           // alpha, beta
   float* be_s = al_s + MAXT;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(be_s + MAXT);      // 8-byte aligned
   uint64_t* tc_bar = s_bar + 1;
   uint64_t* g_bar = s_bar + 2;
   uint32_t* tc_slot = reinterpret_cast<uint32_t*>(s_bar + 3);
+  uint32_t* issued = tc_slot + 1;                         // 1 once the products were issued
 
   if (tid == 0) {
     tc::mbar_init(s_bar, 1);
+    *issued = 0u;
     if constexpr (TC) {
       tc::mbar_init(tc_bar, 1);
       tc::mbar_init(g_bar, 1);
@@ -302,17 +316,20 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   else raw_zero<A>(zr);
   load8<F32>(p.norm_w, el16 * 8, nwr);
 
-  // ---- post-conv activations. Item (part, head, l16) = thread: 8 channels of
-  // head `head` (0 q, 1 k, 2 v) for the IT tokens IT part .. IT part + IT - 1
-  // (at most 96 items). 16-lane groups share (part, head).
-  auto conv_heads = [&]() {
-    // tokens per item: 2 for the CUDA-core variants at T = 3, 4 (96 items in
-    // place of 48, half the serial work each), else 4
-    constexpr int IT = (!TC && (NT == 3 || NT == 4)) ? 2 : 4;
+  // ---- post-conv activations, f32 (unrounded; only the post-conv copy is
+  // rounded to the activation dtype).
+  float vr[MAXT];                                         // tensor-core variant: v_t[r]
+  const int64_t xb = (int64_t)b * T * C;
+  const int64_t cs = (int64_t)slot * KS * C;
+  const bool write_qk = p.postconv && (h % G) == 0;       // one v head of the group writes q, k
+  // CUDA-core variants: item (part, head, l16) = thread: 8 channels of head `head`
+  // (0 q, 1 k, 2 v) for the IT tokens IT part .. IT part + IT - 1 (at most 96
+  // items); 16-lane groups share (part, head); v rows go to VS as f32.
+  auto conv_items = [&]() {
+    // tokens per item: 2 at T = 3, 4 (96 items in place of 48, half the serial
+    // work each), else 4
+    constexpr int IT = (NT == 3 || NT == 4) ? 2 : 4;
     const int n_items = (T + IT - 1) / IT * 3 * 16;
-    const int64_t xb = (int64_t)b * T * C;
-    const int64_t cs = (int64_t)slot * KS * C;
-    const bool write_qk = p.postconv && (h % G) == 0;     // one v head of the group writes q, k
     const bool grp = tid < n_items;                       // uniform per 16 lanes
     const int l16 = tid & 15, head = (tid >> 4) % 3, part = (tid >> 4) / 3;
     const int t0 = IT * part;
@@ -355,9 +372,9 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
         raw_unpack<A>(rw[uu + 3], r3);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float2 a = silu2(conv4x2(w[q][0], w[q][1], w[q][2], w[q][3], make_float2(r0[2 * q], r0[2 * q + 1]),
-                                         make_float2(r1[2 * q], r1[2 * q + 1]), make_float2(r2[2 * q], r2[2 * q + 1]),
-                                         make_float2(r3[2 * q], r3[2 * q + 1])));
+          const float2 a = silu2(conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], make_float2(r0[2 * q], r0[2 * q + 1]),
+                                            make_float2(r1[2 * q], r1[2 * q + 1]), make_float2(r2[2 * q], r2[2 * q + 1]),
+                                            make_float2(r3[2 * q], r3[2 * q + 1])));
           v[2 * q] = a.x;
           v[2 * q + 1] = a.y;
         }
@@ -371,19 +388,98 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], rr);
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = round_act<A>(v[j]);
       if (live) {
         if (p.postconv && (head == 2 || write_qk)) store8<A>(p.postconv, xb + (int64_t)t * C + c, v);
-        if (head == 2) store8<A>(VS, (int64_t)t * D + l16 * 8, v);
+        if (head == 2) store8<F32>(VS, (int64_t)t * D + l16 * 8, v);
         else put_act8<A, TC>(QK, head ^ 1, t, l16 * 8, v);   // k rows 0..7, q rows 8..15
       }
     }
-    if constexpr (TC) {                                   // rows of absent tokens are zero operands
-      for (int e = tid; e < 16 * (D / 4); e += VT) {
-        const int row = e >> 5, kc = e & 31;
-        if ((row & 7) >= T) *reinterpret_cast<float4*>(QK + bsw_off(row, 4 * kc)) = make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  // Tensor-core variant (T >= 5): q and k: warp w takes tokens 2w, 2w + 1, lanes
+  // 0..15 the q head and 16..31 the k head; v: thread r convolves channel r of
+  // the v head for every draft token and keeps v_t[r] in its registers (the v
+  // rows in f32 would not fit the shared memory of three blocks per SM).
+  auto conv_tc = [&]() {
+    constexpr int IT = 2;
+    const int n_parts = (T + IT - 1) / IT;
+    // v channel r: its taps and column values go in flight before the q, k work
+    const int cv = (2 * Hk + h) * D + tid;
+    float w4[4], col[MAXT + KS];
+    if constexpr (A == BF16) {
+      const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.conv_w) + (int64_t)cv * KW);
+      w4[0] = __uint_as_float(u.x << 16); w4[1] = __uint_as_float(u.x & 0xffff0000u);
+      w4[2] = __uint_as_float(u.y << 16); w4[3] = __uint_as_float(u.y & 0xffff0000u);
+    } else {
+      const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(p.conv_w) + (int64_t)cv * KW);
+      w4[0] = f.x; w4[1] = f.y; w4[2] = f.z; w4[3] = f.w;
+    }
+#pragma unroll
+    for (int j = 0; j < MAXT + KS; ++j) {
+      if (j < KS) col[j] = load1<A>(p.conv_state, cs + (int64_t)j * C + cv);
+      else col[j] = j - KS < T ? load1<A>(p.x, xb + (int64_t)(j - KS) * C + cv) : 0.f;
+    }
+    if (warp < n_parts) {                                 // uniform per warp
+      const int l16 = lane & 15, head = lane >> 4, t0 = IT * warp;
+      const int c = (head == 0 ? hq * D : (Hk + hq) * D) + l16 * 8;
+      Raw8<A> wr[4], rw[IT + 3];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) raw_load<A>(p.conv_w, (int64_t)c * KW + 8 * q, wr[q]);
+#pragma unroll
+      for (int j = 0; j < IT + 3; ++j) {
+        const int idx = t0 + j;
+        if (idx < KS) raw_load<A>(p.conv_state, cs + (int64_t)idx * C + c, rw[j]);
+        else if (idx - KS < T) raw_load<A>(p.x, xb + (int64_t)(idx - KS) * C + c, rw[j]);
+        else raw_zero<A>(rw[j]);
       }
+      float2 w[4][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float t8[8];
+        raw_unpack<A>(wr[q], t8);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) w[q][jj] = make_float2(t8[jj], t8[4 + jj]);
+      }
+#pragma unroll
+      for (int uu = 0; uu < IT; ++uu) {
+        const int t = t0 + uu;
+        const bool live = t < T;                          // uniform per warp
+        float v[8];
+        if (live) {
+          float r0[8], r1[8], r2[8], r3[8];
+          raw_unpack<A>(rw[uu], r0);
+          raw_unpack<A>(rw[uu + 1], r1);
+          raw_unpack<A>(rw[uu + 2], r2);
+          raw_unpack<A>(rw[uu + 3], r3);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 a = silu2(conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], make_float2(r0[2 * q], r0[2 * q + 1]),
+                                              make_float2(r1[2 * q], r1[2 * q + 1]), make_float2(r2[2 * q], r2[2 * q + 1]),
+                                              make_float2(r3[2 * q], r3[2 * q + 1])));
+            v[2 * q] = a.x;
+            v[2 * q + 1] = a.y;
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) v[jj] = 0.f;
+        }
+        const float ss = head_sum_sq16(v);                // all 32 lanes of the warp
+        if (live) {
+          const float rr = inv_norm(ss, p.eps);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) v[jj] = __fmul_rn(v[jj], rr);
+          if (write_qk) store8<A>(p.postconv, xb + (int64_t)t * C + c, v);
+          put_act8<A, TC>(QK, head ^ 1, t, l16 * 8, v);   // k rows 0..7, q rows 8..15
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < MAXT; ++t) {
+      vr[t] = t < T ? silu(conv4(w4, col[t], col[t + 1], col[t + 2], col[t + 3])) : 0.f;
+      if (p.postconv && t < T) store1<A>(p.postconv, xb + (int64_t)t * C + cv, vr[t]);
+    }
+    for (int e = tid; e < 16 * (D / 4); e += VT) {        // rows of absent tokens are zero operands
+      const int row = e >> 5, kc = e & 31;
+      if ((row & 7) >= T) *reinterpret_cast<float4*>(QK + bsw_off(row, 4 * kc)) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
 
@@ -391,10 +487,11 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     float ga = 0.f, gb = 0.f;
     if (tid < T) {
       const int64_t gi = ((int64_t)b * T + tid) * Hv + h;
-      ga = p.alpha[gi];
-      gb = p.beta[gi];
+      ga = load_gate(p.alpha, gi, p.gate_bf16);
+      gb = load_gate(p.beta, gi, p.gate_bf16);
     }
-    conv_heads();
+    if constexpr (TC) conv_tc();
+    else conv_items();
     if (tid < T) {                                       // raw projections: the gate step
       al_s[tid] = p.raw_gates ? gate_alpha(ga) : ga;
       be_s[tid] = p.raw_gates ? gate_beta(gb) : gb;
@@ -411,33 +508,38 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     if (!valid) break;                                    // padding entry or bad slot: no outputs
     bool ok = true;
     if constexpr (TC) {
-      // ---- warp 0: thread 0 issues the Gram product and, as soon as the state is
-      // in, the state product (the tensor core runs
-      // them in order); the warp moves the Gram values into the table while the
-      // state product runs. Four independent accumulators (one per 32-column
-      // block of K) keep the accumulation chains short; their sum is formed on the
-      // CUDA cores.
+      // ---- warp 0: thread 0 waits for the state, then issues the Gram product
+      // and the state product (the tensor core runs them in order); the warp
+      // moves the Gram values into the table while the state product runs. The
+      // Gram product's A operand has M = 128 rows, of which rows 16..127 lie past
+      // the q/k tile, in the state region: issuing it only once the state's copy
+      // is complete means those rows (whose results land in TMEM lanes nobody
+      // reads) are settled memory, not memory the copy engine is still writing.
+      // By the time the conv is done the state has almost always arrived. Four
+      // independent accumulators (one per 32-column block of K) keep the
+      // accumulation chains short; their sum is formed on the CUDA cores.
       if (warp == 0) {
         if (lane == 0) {
           const uint32_t bq = tc::smem_u32(QK), sa = tc::smem_u32(SR);
           const uint32_t id = tc::idesc_tf32_f32(128, 16);
-#pragma unroll 1
-          for (int ks = 0; ks < 16; ++ks) {
-            const uint64_t dq = smem_desc_sw128(bq + (ks >> 2) * 2048 + (ks & 3) * 32);
-            tc::mma_tf32(tbase + 64 + 16 * (ks & 3), dq, dq, id, ks > 3);
-          }
-          tc::mma_commit(g_bar);
           ok = tc::mbar_wait(s_bar, 0, 1u << 24);
           if (ok) {
+#pragma unroll 1
+            for (int ks = 0; ks < 16; ++ks) {
+              const uint64_t dq = smem_desc_sw128(bq + (ks >> 2) * 2048 + (ks & 3) * 32);
+              tc::mma_tf32(tbase + 64 + 16 * (ks & 3), dq, dq, id, ks > 3);
+            }
+            tc::mma_commit(g_bar);
 #pragma unroll 1
             for (int ks = 0; ks < 16; ++ks)
               tc::mma_tf32(tbase + 16 * (ks & 3), smem_desc_sw128(sa + (ks >> 2) * 16384 + (ks & 3) * 32),
                            smem_desc_sw128(bq + (ks >> 2) * 2048 + (ks & 3) * 32), id, ks > 3);
             tc::mma_commit(tc_bar);
+            *issued = 1u;
           }
         }
         const bool ok0 = __shfl_sync(0xffffffffu, ok, 0);   // thread 0's state wait
-        const bool okg = tc::mbar_wait(g_bar, 0, 1u << 24);
+        const bool okg = ok0 && tc::mbar_wait(g_bar, 0, 1u << 24);
         tc::fence_after_sync();
         ok = ok0 && okg;
         if (__all_sync(0xffffffffu, okg)) {
@@ -554,7 +656,8 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
 #pragma unroll
       for (int t = 0; t < MAXT; ++t) {
         if (t < T) {
-          float xx = __fmaf_rn(-tb[TAB_BG + t], sk[t], __fmul_rn(tb[TAB_B + t], row_at<A>(VS, t, r)));
+          const float vt = TC ? vr[t] : reinterpret_cast<const float*>(VS)[t * D + r];
+          float xx = __fmaf_rn(-tb[TAB_BG + t], sk[t], __fmul_rn(tb[TAB_B + t], vt));
 #pragma unroll
           for (int w = 0; w < t; ++w) xx = __fmaf_rn(-tb[TAB_A + t * MAXT + w], dr[w], xx);
           dr[t] = xx;
@@ -592,7 +695,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           res[j] = __fmul_rn(__fmul_rn(__fmul_rn(ov[j], rn), nwr[j]), silu_gate(zv[j]));
-        store8<A>(p.out, ((int64_t)b * T + et) * Hv * D + (int64_t)h * D + el16 * 8, res);
+        store_out8<A>(p.out, ((int64_t)b * T + et) * Hv * D + (int64_t)h * D + el16 * 8, res, p.out_f32);
       }
     }
   } while (false);
@@ -601,8 +704,10 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     if (tid == 0) report(p.dev_err, GDN_DEVERR_TIMEOUT);
     tc::mbar_wait(s_bar, 0, 1u << 24);                    // the state copy, if still in flight
     if constexpr (TC) {
-      tc::mbar_wait(g_bar, 0, 1u << 24);                  // the Gram product, if still running
-      if (fail == 2) tc::mbar_wait(tc_bar, 0, 1u << 24);  // the state product, if still running
+      if (*issued) {                                      // set before the failing barrier
+        tc::mbar_wait(g_bar, 0, 1u << 24);                // the Gram product, if still running
+        tc::mbar_wait(tc_bar, 0, 1u << 24);               // the state product, if still running
+      }
     }
   }
   if constexpr (TC) {
@@ -634,7 +739,7 @@ cudaError_t state_map(const StepArgs& a, CUtensorMap* m) {
 template <int A, bool TC, int NT>
 cudaError_t launch_kernel(const StepArgs& a, const CUtensorMap& smap, cudaStream_t stream) {
   auto kern = verify_kernel<A, TC, NT>;
-  const int smem = verify_smem<A, TC>();
+  const int smem = verify_smem<A, TC, NT>();
   cudaError_t e = set_smem_once<verify_kernel<A, TC, NT>>(smem, true);
   if (e != cudaSuccess) return e;
   int n_sm = 0;

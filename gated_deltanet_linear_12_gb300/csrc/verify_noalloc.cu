@@ -9,8 +9,8 @@
 #include "gdn.h"
 
 extern "C" gdn_status gdn_verify_step_noalloc(const gdn_config* cfg, const void* x, const void* conv_w,
-                                              const void* conv_state, const float* state, const float* alpha,
-                                              const float* beta, const void* z, const float* norm_w, void* out,
+                                              const void* conv_state, const float* state, const void* alpha,
+                                              const void* beta, const void* z, const float* norm_w, void* out,
                                               const int32_t* slot_idx, int32_t B, int32_t T, void* postconv_out,
                                               void* stream) {
   // The read-only verify never writes conv_state or state.

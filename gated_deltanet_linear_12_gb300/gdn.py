@@ -38,7 +38,8 @@ class GdnConfig(ctypes.Structure):
     _fields_ = [("n_qk_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("conv_width", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("eps", ctypes.c_float), ("q_scale", ctypes.c_float),
-                ("n_slots", ctypes.c_int32), ("dev_err", ctypes.c_void_p), ("gates", ctypes.c_int32)]
+                ("n_slots", ctypes.c_int32), ("dev_err", ctypes.c_void_p), ("gates", ctypes.c_int32),
+                ("gate_dtype", ctypes.c_int32), ("out_f32", ctypes.c_int32)]
 
 
 class GdnLayerView(ctypes.Structure):
@@ -108,13 +109,17 @@ def act_of(dtype: torch.dtype) -> int:
 
 
 def make_config(n_qk_heads, n_v_heads, act, n_slots, *, eps=1e-6, q_scale=1.0, dev_err=None,
-                gates=GDN_GATES_ACTIVATED):
-    """gdn_config; act is GDN_F32/GDN_BF16 or a torch dtype; dev_err a CUDA int32 tensor;
-    gates GDN_GATES_RAW makes alpha / beta arguments raw projections."""
+                gates=GDN_GATES_ACTIVATED, gate_dtype=GDN_F32, out_f32=False):
+    """gdn_config; act and gate_dtype are GDN_F32/GDN_BF16 or torch dtypes; dev_err a
+    CUDA int32 tensor; gates GDN_GATES_RAW makes alpha / beta arguments raw
+    projections; out_f32 makes `out` f32 whatever the activation dtype."""
     if isinstance(act, torch.dtype):
         act = act_of(act)
+    if isinstance(gate_dtype, torch.dtype):
+        gate_dtype = act_of(gate_dtype)
     return GdnConfig(n_qk_heads, n_v_heads, HEAD_DIM, CONV_WIDTH, act, eps, q_scale, n_slots,
-                     dev_err.data_ptr() if dev_err is not None else None, gates)
+                     dev_err.data_ptr() if dev_err is not None else None, gates, gate_dtype,
+                     int(bool(out_f32)))
 
 
 def _ptr(t):
@@ -216,8 +221,8 @@ def make_layer_views(layers, device):
 
 def gdn_verify_step_noalloc(cfg, x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, *,
                             postconv_out=None, stream=None):
-    """Read-only verify with the library's own fixed workspace: nothing is
-    allocated, here or in the library. Same arrays as gdn_verify_step."""
+    """Read-only verify that allocates nothing and takes no workspace: it
+    launches the same kernel as gdn_verify_step. Same arrays as gdn_verify_step."""
     _dense(x, conv_w, conv_state, state, alpha, beta, z, norm_w, out, slot_idx, postconv_out)
     B, T = x.shape[0], x.shape[1]
     _check("gdn_verify_step_noalloc", load().gdn_verify_step_noalloc(
@@ -252,13 +257,15 @@ def gdn_verify_step_lazy(cfg, prev_x, prev_alpha, prev_beta, prev_n_keep, x, con
 
 
 def gdn_gates(cfg, a, b, alpha, beta, *, stream=None):
-    """alpha = exp(-softplus(a)), beta = sigmoid(b) for f32 tensors of the same
-    shape whose last dimension is Hv ([n_tok][Hv] or [B][T][Hv])."""
+    """alpha = exp(-softplus(a)), beta = sigmoid(b) for tensors of the same shape
+    whose last dimension is Hv ([n_tok][Hv] or [B][T][Hv]), of the config's
+    gate dtype (float32 or bfloat16)."""
     _dense(a, b, alpha, beta)
     if not (a.shape == b.shape == alpha.shape == beta.shape) or a.shape[-1] != cfg.n_v_heads:
         raise ValueError("a, b, alpha, beta must share one shape [..., Hv]")
-    if any(t.dtype != torch.float32 for t in (a, b, alpha, beta)):
-        raise ValueError("gates are float32")
+    want = torch.bfloat16 if cfg.gate_dtype == GDN_BF16 else torch.float32
+    if any(t.dtype != want for t in (a, b, alpha, beta)):
+        raise ValueError(f"gates must be {want} (the config's gate_dtype)")
     _check("gdn_gates", load().gdn_gates(ctypes.byref(cfg), _ptr(a), _ptr(b), _ptr(alpha), _ptr(beta),
                                          a.numel() // cfg.n_v_heads, _stream(a, stream)))
 

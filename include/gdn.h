@@ -29,7 +29,9 @@
  *   - C = (2*Hk + Hv) * 128 packed channels [q heads | k heads | v heads]; v head
  *     h reads q/k head h / (Hv/Hk).
  *   - Activations (x, post-conv rows, z, out, conv_w, conv_state) have the dtype
- *     cfg->act: GDN_F32 or GDN_BF16. alpha, beta, norm_w and the state S are f32.
+ *     cfg->act: GDN_F32 or GDN_BF16 (out may be f32 instead, cfg->out_f32). The
+ *     gates alpha, beta (or raw a, b) have the dtype cfg->gate_dtype. norm_w and
+ *     the state S are f32.
  *   - Layouts are row-major: x/qkv [n_tok][C]; conv_w [C][4] (tap 3 multiplies
  *     the current token); conv_state pool [n_slots][3][C] (oldest row first);
  *     state pool [n_slots][Hv][128 value rows][128 key columns] f32;
@@ -45,6 +47,12 @@
  *     outside [0, T], inconsistent cu_seqlens) skip the affected sequence and OR
  *     a GDN_DEVERR_* bit into *cfg->dev_err when that pointer is non-null. A
  *     negative slot index marks padding: the entry is skipped without error.
+ *   - In a call that writes conv_state or state (gdn_conv_fwd, gdn_delta_prefill,
+ *     gdn_verify_step with GDN_VERIFY_COMMIT_ALL, gdn_commit_layers,
+ *     gdn_verify_step_lazy) the non-negative slot indices must be pairwise
+ *     distinct: entries naming the same slot would update it from different
+ *     blocks at once, and the result is undefined. Read-only calls may repeat
+ *     slots.
  */
 #ifndef GDN_H
 #define GDN_H
@@ -98,6 +106,12 @@ typedef struct gdn_config {
   int32_t gates;        /* GDN_GATES_ACTIVATED (0) or GDN_GATES_RAW: applies to the
                            alpha / beta arguments of gdn_delta_prefill and
                            gdn_verify_step and to the layer views of gdn_commit_layers */
+  int32_t gate_dtype;   /* element type of every gate array (alpha, beta, raw a, b, and
+                           the outputs of gdn_gates): GDN_F32 (0) or GDN_BF16. A bf16
+                           gate is widened exactly to f32 where it is read. */
+  int32_t out_f32;      /* 0: out has the activation dtype; 1: out is f32 (the z-gated
+                           RMSNorm's result stored without rounding), for
+                           gdn_delta_prefill, gdn_verify_step(_noalloc, _lazy) */
 } gdn_config;
 
 /* One layer's device views for gdn_commit_layers (the array itself lives in
@@ -105,8 +119,8 @@ typedef struct gdn_config {
  * projections a, b when the config's gates is GDN_GATES_RAW). */
 typedef struct gdn_layer_view {
   const void* x;         /* [B][T][C] act */
-  const float* alpha;    /* [B][T][Hv] */
-  const float* beta;     /* [B][T][Hv] */
+  const void* alpha;     /* [B][T][Hv] gate_dtype */
+  const void* beta;      /* [B][T][Hv] gate_dtype */
   const void* conv_w;    /* [C][4] act */
   void* conv_state;      /* [n_slots][3][C] act, updated in place */
   float* state;          /* [n_slots][Hv][128][128], updated in place */
@@ -156,16 +170,18 @@ gdn_status gdn_postconv_norm(const gdn_config* cfg, int32_t in_t, const void* y_
  * o_t = S_t q_t, and "Strata PR #3226" (output norm after the recurrence).
  *   qkv     [n_tok][C] act: post-conv rows (q, k L2-normalised), e.g. from
  *           gdn_conv_fwd(fuse_norm=1)
- *   alpha, beta [n_tok][Hv] f32: the gates, or the raw a, b when cfg->gates is
- *               GDN_GATES_RAW
- *   z, out  [n_tok][Hv*128] act; out = RMSNorm(o) * norm_w * silu(z)
+ *   alpha, beta [n_tok][Hv] gate_dtype: the gates, or the raw a, b when
+ *               cfg->gates is GDN_GATES_RAW
+ *   z       [n_tok][Hv*128] act
+ *   out     [n_tok][Hv*128] act (f32 when cfg->out_f32); out = RMSNorm(o) *
+ *           norm_w * silu(z)
  *   norm_w  [128] f32
  *   state   pool: read at slot_idx[s] when has_init[s] (else zero), always
  *           written with the state after the last token of s
  *   chunk   must be GDN_CHUNK (64)
  */
-gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const float* alpha,
-                             const float* beta, const void* z, const float* norm_w, void* out,
+gdn_status gdn_delta_prefill(const gdn_config* cfg, const void* qkv, const void* alpha,
+                             const void* beta, const void* z, const float* norm_w, void* out,
                              float* state, const int32_t* slot_idx, const int32_t* cu_seqlens,
                              const uint8_t* has_init, int32_t n_seq, int64_t n_tok,
                              int32_t chunk, void* stream);
@@ -185,8 +201,15 @@ int64_t gdn_verify_workspace_bytes(const gdn_config* cfg, int32_t B, int32_t T);
  * state, and the gated RMSNorm, for every draft token.
  * Source: "Strata PR #3226" ("Summary": verify forward launched once per layer).
  *   x       [B][T][C] act (raw, pre-conv rows of the draft tokens)
- *   alpha, beta [B][T][Hv] f32 (raw a, b when cfg->gates is GDN_GATES_RAW);
- *   z, out [B][T][Hv*128] act; norm_w [128] f32
+ *   alpha, beta [B][T][Hv] gate_dtype (raw a, b when cfg->gates is GDN_GATES_RAW)
+ *   z       [B][T][Hv*128] act; norm_w [128] f32
+ *   out     [B][T][Hv*128] act (f32 when cfg->out_f32)
+ *   The post-conv activations enter the recurrence unrounded (f32): they are
+ *   never stored here (only their rounded copy, postconv_out, when asked for).
+ *   Products: f32 on the CUDA cores, except bf16 activations with T >= 5, whose
+ *   S0 k_t, S0 q_t and k.k, q.k products run on the tensor core in tf32 (10
+ *   explicit mantissa bits): their f32 outputs are within 4e-3 * max(1, |exact|)
+ *   of the exact value, their bf16 outputs within the bf16 rounding.
  *   slot_idx [B] int32 into both pools
  *   flags   0: conv_state and state are only read;
  *           GDN_VERIFY_COMMIT_ALL: both advance in place by all T tokens,
@@ -200,8 +223,8 @@ int64_t gdn_verify_workspace_bytes(const gdn_config* cfg, int32_t B, int32_t T);
  *   T in 1..GDN_MAX_DRAFT.
  */
 gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* conv_w,
-                           void* conv_state, float* state, const float* alpha,
-                           const float* beta, const void* z, const float* norm_w, void* out,
+                           void* conv_state, float* state, const void* alpha,
+                           const void* beta, const void* z, const float* norm_w, void* out,
                            const int32_t* slot_idx, int32_t B, int32_t T, uint32_t flags,
                            void* postconv_out, void* workspace, int64_t workspace_bytes,
                            void* stream);
@@ -223,8 +246,8 @@ gdn_status gdn_verify_step(const gdn_config* cfg, const void* x, const void* con
  * but their arguments).
  */
 gdn_status gdn_verify_step_noalloc(const gdn_config* cfg, const void* x, const void* conv_w,
-                                   const void* conv_state, const float* state, const float* alpha,
-                                   const float* beta, const void* z, const float* norm_w, void* out,
+                                   const void* conv_state, const float* state, const void* alpha,
+                                   const void* beta, const void* z, const float* norm_w, void* out,
                                    const int32_t* slot_idx, int32_t B, int32_t T, void* postconv_out,
                                    void* stream);
 
@@ -265,7 +288,7 @@ gdn_status gdn_commit_layers(const gdn_config* cfg, const gdn_layer_view* layers
  * tolerances of gdn_verify_step's).
  *
  *   prev_x        [B][prev_T][C] act: the previous window's draft rows of this layer
- *   prev_alpha, prev_beta  [B][prev_T][Hv] f32 (raw a, b in GDN_GATES_RAW mode)
+ *   prev_alpha, prev_beta  [B][prev_T][Hv] gate_dtype (raw a, b in GDN_GATES_RAW mode)
  *   prev_n_keep   [B] int32 in [0, prev_T]: accepted tokens of the previous window
  *                 (0: nothing to commit for that sequence)
  *   the other arguments as gdn_verify_step's (without flags and workspace); row b
@@ -274,10 +297,10 @@ gdn_status gdn_commit_layers(const gdn_config* cfg, const gdn_layer_view* layers
  * misalignment, out overlapping x, z or prev_x. A prev_n_keep outside
  * [0, prev_T] sets GDN_DEVERR_NKEEP and skips that sequence (nothing written).
  */
-gdn_status gdn_verify_step_lazy(const gdn_config* cfg, const void* prev_x, const float* prev_alpha,
-                                const float* prev_beta, const int32_t* prev_n_keep, int32_t prev_T,
+gdn_status gdn_verify_step_lazy(const gdn_config* cfg, const void* prev_x, const void* prev_alpha,
+                                const void* prev_beta, const int32_t* prev_n_keep, int32_t prev_T,
                                 const void* x, const void* conv_w, void* conv_state, float* state,
-                                const float* alpha, const float* beta, const void* z,
+                                const void* alpha, const void* beta, const void* z,
                                 const float* norm_w, void* out, const int32_t* slot_idx, int32_t B,
                                 int32_t T, void* postconv_out, void* stream);
 
@@ -292,17 +315,19 @@ gdn_status gdn_verify_step_lazy(const gdn_config* cfg, const void* prev_x, const
  * so their results are bitwise those of gdn_gates followed by the same call in
  * GDN_GATES_ACTIVATED mode.
  *
- *   a, b          [n_tok][Hv] f32 raw projections (device)
- *   alpha, beta   [n_tok][Hv] f32 results (device, caller-owned); alpha may be a
- *                 and beta may be b (in place), other overlaps are invalid
+ *   a, b          [n_tok][Hv] raw projections (device), cfg->gate_dtype
+ *   alpha, beta   [n_tok][Hv] results (device, caller-owned), cfg->gate_dtype
+ *                 (bf16 results are rounded to nearest even from the f32 values);
+ *                 alpha may be a and beta may be b (in place), other overlaps are
+ *                 invalid
  *   cfg->gates is not read (the call always applies the gate step).
  * Accuracy: CUDA's expf / log1pf and a correctly rounded divide, within a few
  * ulp of the exact gates (alpha's relative error grows with softplus(a)).
  * Errors: GDN_ERR_INVALID for null pointers (n_tok > 0), n_tok < 0 or bad
  * overlaps; GDN_ERR_CUDA if the launch fails. n_tok == 0 enqueues nothing.
  */
-gdn_status gdn_gates(const gdn_config* cfg, const float* a, const float* b, float* alpha,
-                     float* beta, int64_t n_tok, void* stream);
+gdn_status gdn_gates(const gdn_config* cfg, const void* a, const void* b, void* alpha,
+                     void* beta, int64_t n_tok, void* stream);
 
 /* Static description of a status code (never NULL; "unknown status" for a value
  * outside gdn_status; the string is owned by the library). The pages have no

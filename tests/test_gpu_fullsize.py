@@ -40,7 +40,9 @@ def _gpu_prefill_chain(G, inp):
 
 
 def _oracle_chain(orc, inp, s, h):
-    """Oracle conv + prefill of sequence s, v head h, on its own channels."""
+    """Oracle conv + prefill of sequence s, v head h, on its own channels: the
+    double conv (returned unrounded), rounded to bf16 as stored rows, then the
+    token-by-token recurrence."""
     Hk, Hv = inp["Hk"], inp["Hv"]
     hq = h // (Hv // Hk)
     chans = np.r_[hq * D:(hq + 1) * D, (Hk + hq) * D:(Hk + hq + 1) * D,
@@ -50,13 +52,13 @@ def _oracle_chain(orc, inp, s, h):
     x = inp["x"][t0:t1][:, chans]
     cu = np.array([0, t1 - t0], np.int32)
     y, _ = orc.conv_fwd(x, inp["conv_w"][chans], inp["conv_state"][slot:slot + 1][:, :, chans], [0],
-                        cu, inp["has_init_conv"][s:s + 1], 1, 1, prec="f32")
-    qkv = syn.to_act(y.astype(np.float32), "bf16")
+                        cu, inp["has_init_conv"][s:s + 1], 1, 1)
+    qkv = syn.to_act(orc.round_bf16(y).astype(np.float32), "bf16")
     hd = slice(h * D, (h + 1) * D)
     out, st = orc.prefill(qkv, inp["alpha"][t0:t1, h:h + 1], inp["beta"][t0:t1, h:h + 1],
                           inp["z"][t0:t1, hd], inp["norm_w"], inp["state"][slot:slot + 1, h:h + 1],
                           [0], cu, inp["has_init_state"][s:s + 1], 1, 1)
-    return qkv, out, st[0, 0], (t0, t1, slot, chans)
+    return y, out, st[0, 0], (t0, t1, slot, chans)
 
 
 @pytest.mark.parametrize("name,samples", [
@@ -67,9 +69,9 @@ def test_prefill_workload_full_size(G, orc, name, samples):
     inp = syn.workload_prefill(name)
     y, out, S, cs = _gpu_prefill_chain(G, inp)
     for s, h in samples:
-        qkv, ro, rs, (t0, t1, slot, chans) = _oracle_chain(orc, inp, s, h)
+        y64, ro, rs, (t0, t1, slot, chans) = _oracle_chain(orc, inp, s, h)
         ci = torch.as_tensor(chans, device="cuda")
-        assert np.array_equal(bits(y[t0:t1].index_select(1, ci)), qkv.view(np.int16)), "post-conv bitwise"
+        check_bf16(to_np(y[t0:t1].index_select(1, ci)), y64, what=f"{name} post-conv seq {s}")
         check_bf16(to_np(out[t0:t1, h * D:(h + 1) * D]), ro, what=f"{name} seq {s} head {h}")
         check_states(to_np(S[slot:slot + 1, h:h + 1]), rs[None, None], [0], 1e-4, f"{name} state")
 
@@ -103,10 +105,10 @@ def test_spec_verify_window_full_size(G, orc):
     for l, inp in enumerate(inps):
         ro, _, _, _ = orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"],
                                  inp["alpha"], inp["beta"], inp["z"], inp["norm_w"], inp["slot_idx"],
-                                 16, 32, act32=True)
+                                 16, 32)
         check_bf16(to_np(outs[l]), ro, what=f"layer {l} verify")
         rcs, rst = orc.commit(inp["x"], inp["alpha"], inp["beta"], inp["conv_w"], inp["conv_state"],
-                              inp["state"], inp["slot_idx"], n_keep, 16, 32, act32=True)
+                              inp["state"], inp["slot_idx"], n_keep, 16, 32)
         assert np.array_equal(to_np(layers[l]["conv_state"]), rcs), "conv_state commit bit-exact"
         check_states(to_np(layers[l]["state"]), rst, range(rst.shape[0]), 1e-4, f"layer {l} commit")
 
@@ -125,7 +127,7 @@ def test_decode_layer_full_size(G, orc):
     torch.cuda.synchronize()
     ro, _, rcs, rst = orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"],
                                  inp["alpha"], inp["beta"], inp["z"], inp["norm_w"], inp["slot_idx"],
-                                 16, 32, commit_all=True, act32=True)
+                                 16, 32, commit_all=True)
     check_bf16(to_np(out), ro, what="decode outputs")
     assert np.array_equal(to_np(cs), rcs), "conv_state commit bit-exact"
     check_states(to_np(S), rst, range(rst.shape[0]), 1e-4, "decode state")

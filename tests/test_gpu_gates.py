@@ -87,8 +87,12 @@ def test_gates_empty_is_a_no_op(G):
 
 # ------------------------------------------------------------------ prefill
 def _post_conv(orc, inp):
+    """Post-conv rows as stored: the double oracle's values rounded to the
+    activation dtype (an input of both sides)."""
     y, _ = orc.conv_fwd(inp["x"], inp["conv_w"], inp["conv_state"], inp["slot_idx"],
-                        inp["cu_seqlens"], inp["has_init_conv"], inp["Hk"], inp["Hv"], prec="f32")
+                        inp["cu_seqlens"], inp["has_init_conv"], inp["Hk"], inp["Hv"])
+    if inp["act"] == "bf16":
+        y = orc.round_bf16(y)
     return syn.to_act(y.astype(np.float32), inp["act"])
 
 
@@ -175,7 +179,7 @@ def test_verify_and_decode_raw_gates(G, orc, T, act, commit_all):
     ra, rb = orc.gates(inp["alpha"], inp["beta"])
     out, _, cs, st = orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"], ra, rb,
                                 inp["z"], inp["norm_w"], inp["slot_idx"], inp["Hk"], inp["Hv"],
-                                round_act=act == "bf16", commit_all=commit_all, act32=True)
+                                commit_all=commit_all)
     if act == "bf16":
         check_bf16(to_np(R.out), out, what=f"verify raw gates T={T}")
     else:
@@ -207,6 +211,102 @@ def test_commit_raw_gates(G, orc, T):
         assert np.array_equal(bits(R.cs), bits(A.cs))
         ra, rb = orc.gates(inp["alpha"], inp["beta"])
         cs, st = orc.commit(inp["x"], ra, rb, inp["conv_w"], inp["conv_state"], inp["state"],
-                            inp["slot_idx"], n_keep, 2, 4, act32=True)
+                            inp["slot_idx"], n_keep, 2, 4)
         assert np.array_equal(to_np(R.cs), cs), "conv_state commit must be bit-exact"
         check_states(to_np(R.S), st, range(st.shape[0]), 1e-4, "commit raw gates state")
+
+
+# ------------------------------------------------------------------ bf16 gate arrays
+def _bf16(a):
+    return syn.f32_to_bf16_bits(np.asarray(a, np.float32))
+
+
+def test_gates_kernel_bf16_io(G, orc):
+    """gdn_gates with bfloat16 a, b, alpha, beta: the results are the f32 gates
+    of the widened inputs rounded to nearest even; the f32-output arm (f32
+    arrays holding the same bf16 values) gives those unrounded gates."""
+    n_tok, Hv = 41, 5
+    rng = np.random.default_rng(615)
+    a16 = _bf16(3.0 * rng.standard_normal((n_tok, Hv)))
+    b16 = _bf16(3.0 * rng.standard_normal((n_tok, Hv)))
+    a32, b32 = syn.bf16_bits_to_f32(a16), syn.bf16_bits_to_f32(b16)      # exact widening
+    cfg16 = G.make_config(1, Hv, torch.bfloat16, 1, gate_dtype=torch.bfloat16)
+    al16, be16 = _gates_dev(G, cfg16, to_dev(a16), to_dev(b16))
+    cfg32 = G.make_config(1, Hv, torch.bfloat16, 1)
+    al32, be32 = _gates_dev(G, cfg32, to_dev(a32), to_dev(b32))
+    torch.cuda.synchronize()
+    _check_gates(orc, a32, b32, to_np(al32), to_np(be32), "gdn_gates f32 arm of bf16 inputs")
+    ra, rb = orc.gates(a32.astype(np.float64), b32.astype(np.float64))
+    check_bf16(to_np(al16), ra, atol=0.0, what="bf16 alpha")
+    check_bf16(to_np(be16), rb, atol=0.0, what="bf16 beta")
+    # bitwise: the bf16 results are the f32 results rounded
+    assert np.array_equal(bits(al16), _bf16(to_np(al32)).view(np.int16))
+    assert np.array_equal(bits(be16), _bf16(to_np(be32)).view(np.int16))
+
+
+@pytest.mark.parametrize("gates", ["raw", "activated"])
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_prefill_bf16_gate_arrays(G, orc, gates, out_f32):
+    """bf16 gate arrays (raw a, b or activated alpha, beta) in the tensor-core
+    prefill: bitwise equal to the f32 arrays holding the same values, and
+    against the oracle on the widened gates, with an f32-output arm."""
+    inp = syn.prefill_inputs([70, 129, 5], 2, 4, "bf16", seed=625, init_mask=np.array([1, 0, 1]),
+                             gate_form="raw" if gates == "raw" else "softplus")
+    qkv = _post_conv(orc, inp)
+    g16 = (_bf16(inp["alpha"]), _bf16(inp["beta"]))
+    g32 = tuple(syn.bf16_bits_to_f32(g) for g in g16)
+    mode = G.GDN_GATES_RAW if gates == "raw" else G.GDN_GATES_ACTIVATED
+    res = []
+    for gd, (al, be) in ((torch.bfloat16, g16), (torch.float32, g32)):
+        S = to_dev(inp["state"])
+        out = torch.zeros(inp["n_tok"], inp["Hv"] * 128, dtype=torch.float32 if out_f32 else torch.bfloat16,
+                          device="cuda")
+        cfg = G.make_config(inp["Hk"], inp["Hv"], torch.bfloat16, S.shape[0], gates=mode, gate_dtype=gd,
+                            out_f32=out_f32)
+        G.gdn_delta_prefill(cfg, to_dev(qkv), to_dev(al), to_dev(be), to_dev(inp["z"]), to_dev(inp["norm_w"]),
+                            out, S, to_dev(inp["slot_idx"]), to_dev(inp["cu_seqlens"]),
+                            to_dev(inp["has_init_state"]))
+        res.append((out, S))
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(res[0][0]), bits(res[1][0])), "bf16 gates == the same values in f32 (bitwise)"
+    assert np.array_equal(bits(res[0][1]), bits(res[1][1]))
+    ra, rb = (orc.gates(*g32) if gates == "raw" else g32)
+    ro, rs = orc.prefill(qkv, ra, rb, inp["z"], inp["norm_w"], inp["state"], inp["slot_idx"],
+                         inp["cu_seqlens"], inp["has_init_state"], inp["Hk"], inp["Hv"])
+    if out_f32:
+        check_f32_out(to_np(res[0][0]), ro, 1e-4, "prefill bf16 gates, f32 out")
+    else:
+        check_bf16(to_np(res[0][0]), ro, what="prefill bf16 gates out")
+    check_states(to_np(res[0][1]), rs, [int(s) for s in inp["slot_idx"]], 1e-4, "prefill bf16 gates state")
+
+
+@pytest.mark.parametrize("T,commit_all", [(3, False), (8, False), (1, True), (5, True)])
+def test_verify_bf16_gate_arrays(G, orc, T, commit_all):
+    """bf16 raw gates in verify / decode and the batched commit: bitwise equal to
+    f32 arrays holding the same values, and against the oracle."""
+    inp = syn.verify_inputs(5, T, 2, 4, "bf16", seed=640 + T, pad_slots=1, gate_form="raw")
+    a16, b16 = _bf16(inp["alpha"]), _bf16(inp["beta"])
+    a32, b32 = syn.bf16_bits_to_f32(a16), syn.bf16_bits_to_f32(b16)
+    wins = []
+    for gd, (a, b) in ((torch.bfloat16, (a16, b16)), (torch.float32, (a32, b32))):
+        w = Win(inp, to_dev(a), to_dev(b))
+        cfg = G.make_config(2, 4, torch.bfloat16, w.S.shape[0], gates=G.GDN_GATES_RAW, gate_dtype=gd)
+        G.gdn_verify_step(cfg, w.x, w.conv_w, w.cs, w.S, w.al, w.be, w.z, w.norm_w, w.out, w.slot,
+                          commit_all=commit_all)
+        if not commit_all:
+            views = G.make_layer_views([w.view()], "cuda")
+            G.gdn_commit_layers(cfg, views, 1, w.slot, to_dev(inp["n_keep"]), T)
+        wins.append(w)
+    torch.cuda.synchronize()
+    for x, y in ((wins[0].out, wins[1].out), (wins[0].S, wins[1].S), (wins[0].cs, wins[1].cs)):
+        assert np.array_equal(bits(x), bits(y)), "bf16 gates == the same values in f32 (bitwise)"
+    ra, rb = orc.gates(a32, b32)
+    out, _, cs, st = orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"], ra, rb,
+                                inp["z"], inp["norm_w"], inp["slot_idx"], 2, 4, commit_all=commit_all)
+    check_bf16(to_np(wins[0].out), out, what=f"verify bf16 gates T={T}")
+    if not commit_all:
+        cs, st = orc.commit(inp["x"], ra, rb, inp["conv_w"], inp["conv_state"], inp["state"],
+                            inp["slot_idx"], inp["n_keep"], 2, 4)
+    assert np.array_equal(to_np(wins[0].cs), cs)
+    used = [int(s) for s in inp["slot_idx"] if s >= 0]
+    check_states(to_np(wins[0].S), st, used, 1e-4, "bf16 gates state")

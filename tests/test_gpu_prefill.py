@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 from gated_deltanet_linear_12_gb300 import synthetic as syn
-from tests.helpers import bits, check_bf16, check_f32_out, check_states, to_dev, to_np
+from tests.helpers import Canary, bits, check_bf16, check_f32_out, check_states, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -21,22 +21,27 @@ def G():
 
 
 def _oracle_qkv(orc, inp):
-    """Post-conv activations as stored (oracle float order, rounded to act)."""
+    """Post-conv activations as stored: the double oracle's values rounded to
+    the activation dtype (to nearest even for bf16, to f32 otherwise)."""
     y, _ = orc.conv_fwd(inp["x"], inp["conv_w"], inp["conv_state"], inp["slot_idx"],
-                        inp["cu_seqlens"], inp["has_init_conv"], inp["Hk"], inp["Hv"], prec="f32")
-    y = y.astype(np.float32)
-    return syn.to_act(y, inp["act"])
+                        inp["cu_seqlens"], inp["has_init_conv"], inp["Hk"], inp["Hv"])
+    if inp["act"] == "bf16":
+        y = orc.round_bf16(y)
+    return syn.to_act(y.astype(np.float32), inp["act"])
 
 
 def _run_prefill(G, inp, qkv, dev_err=None, q_scale=1.0, eps=1e-6):
+    """The prefill with its outputs and state pool between NaN guard bands."""
     act = torch.bfloat16 if inp["act"] == "bf16" else torch.float32
-    S = to_dev(inp["state"])
-    out = torch.zeros(inp["n_tok"], inp["Hv"] * 128, dtype=act, device="cuda")
+    guard = Canary()
+    S = guard.wrap(to_dev(inp["state"]))
+    out = guard.wrap(torch.zeros(inp["n_tok"], inp["Hv"] * 128, dtype=act, device="cuda"))
     cfg = G.make_config(inp["Hk"], inp["Hv"], act, S.shape[0], dev_err=dev_err, q_scale=q_scale, eps=eps)
-    G.gdn_delta_prefill(cfg, to_dev(qkv), to_dev(inp["alpha"]), to_dev(inp["beta"]),
-                        to_dev(inp["z"]), to_dev(inp["norm_w"]), out, S, to_dev(inp["slot_idx"]),
-                        to_dev(inp["cu_seqlens"]), to_dev(inp["has_init_state"]))
+    G.gdn_delta_prefill(cfg, guard.wrap(to_dev(qkv)), to_dev(inp["alpha"]), to_dev(inp["beta"]),
+                        guard.wrap(to_dev(inp["z"])), to_dev(inp["norm_w"]), out, S,
+                        to_dev(inp["slot_idx"]), to_dev(inp["cu_seqlens"]), to_dev(inp["has_init_state"]))
     torch.cuda.synchronize()
+    guard.check("prefill")
     return out, S
 
 
@@ -87,6 +92,25 @@ def test_prefill_q_scale_and_eps(G, orc, act):
     check_states(to_np(S), rs, [int(s) for s in inp["slot_idx"]], 1e-4, "prefill q_scale state")
 
 
+@pytest.mark.parametrize("lens,init", [([1, 63, 64, 65, 200, 3], [1, 0, 1, 1, 0, 1]), ([300, 17], [0, 1])])
+def test_prefill_tc_f32_out(G, orc, lens, init):
+    """The f32-output arm of the tensor-core prefill (bf16 activations): the
+    outputs before any rounding against the f32 recurrence tolerance."""
+    inp = syn.prefill_inputs(lens, 2, 4, "bf16", seed=560 + len(lens), init_mask=np.array(init),
+                             gate_form="softplus")
+    qkv = _oracle_qkv(orc, inp)
+    S = to_dev(inp["state"])
+    out = torch.zeros(inp["n_tok"], inp["Hv"] * 128, dtype=torch.float32, device="cuda")
+    cfg = G.make_config(inp["Hk"], inp["Hv"], torch.bfloat16, S.shape[0], out_f32=True)
+    G.gdn_delta_prefill(cfg, to_dev(qkv), to_dev(inp["alpha"]), to_dev(inp["beta"]), to_dev(inp["z"]),
+                        to_dev(inp["norm_w"]), out, S, to_dev(inp["slot_idx"]), to_dev(inp["cu_seqlens"]),
+                        to_dev(inp["has_init_state"]))
+    torch.cuda.synchronize()
+    ro, rs = _oracle_prefill(orc, inp, qkv)
+    check_f32_out(to_np(out), ro, 1e-4, "prefill tc f32 out")
+    check_states(to_np(S), rs, [int(s) for s in inp["slot_idx"]], 1e-4, "prefill tc f32-out state")
+
+
 def test_prefill_group_of_three(G, orc):
     inp = syn.prefill_inputs([90, 17], 2, 6, "bf16", seed=520, init_mask=np.array([1, 0]))
     qkv = _oracle_qkv(orc, inp)
@@ -112,16 +136,21 @@ def test_conv_then_prefill_end_to_end(G, orc):
                         to_dev(inp["norm_w"]), out, S, to_dev(inp["slot_idx"]),
                         to_dev(inp["cu_seqlens"]), to_dev(inp["has_init_state"]))
     torch.cuda.synchronize()
+    y64, _ = orc.conv_fwd(inp["x"], inp["conv_w"], inp["conv_state"], inp["slot_idx"],
+                          inp["cu_seqlens"], inp["has_init_conv"], 2, 4)
+    check_bf16(to_np(y), y64, what="chain post-conv")
     qkv = _oracle_qkv(orc, inp)
-    assert np.array_equal(bits(y), qkv.view(np.int16)), "post-conv activations bitwise"
     ro, rs = _oracle_prefill(orc, inp, qkv)
     check_bf16(to_np(out), ro, what="chain out")
     check_states(to_np(S), rs, [int(s) for s in inp["slot_idx"]], 1e-4, "chain state")
 
 
 def test_prefill_then_verify_equals_longer_prefill(G, orc):
-    """Phase consistency on the GPU: prefill(n) + verify(T) outputs match the
-    oracle's prefill(n + T) outputs on the last T tokens."""
+    """Phase composition on the GPU: prefill(n) then a verify of the next T
+    tokens from the committed pools, against the oracle's prefill(n) then
+    verify(T). The oracle pins (P8) show that chain equals one prefill of n + T
+    tokens when the activations are rounded alike; here the verify keeps them
+    unrounded, as the fused kernel does."""
     n, T = 100, 5
     inp = syn.prefill_inputs([n + T], 2, 4, "bf16", seed=540, init_mask=np.array([1]),
                              slot_perm=False, n_slots=1)
@@ -149,5 +178,12 @@ def test_prefill_then_verify_equals_longer_prefill(G, orc):
     torch.cuda.synchronize()
     qkv = _oracle_qkv(orc, inp)
     ro, _ = _oracle_prefill(orc, inp, qkv)
-    check_bf16(to_np(out_v)[0], ro[n:], what="verify after prefill")
     check_bf16(to_np(out_p), ro[:n], what="prefill part")
+    # the oracle's chain: prefill of the first n tokens, then the verify
+    sub = dict(inp, x=inp["x"][:n], alpha=inp["alpha"][:n], beta=inp["beta"][:n], z=inp["z"][:n],
+               cu_seqlens=np.array([0, n], np.int32), n_tok=n)
+    _, cs1 = orc.conv_fwd(sub["x"], inp["conv_w"], inp["conv_state"], [0], sub["cu_seqlens"], [1], 2, 4)
+    _, st1 = _oracle_prefill(orc, sub, qkv[:n])
+    rv, _, _, _ = orc.verify(inp["x"][None, n:], inp["conv_w"], cs1, st1, inp["alpha"][None, n:],
+                             inp["beta"][None, n:], inp["z"][None, n:], inp["norm_w"], [0], 2, 4)
+    check_bf16(to_np(out_v), rv, what="verify after prefill")

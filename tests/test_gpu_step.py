@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 from gated_deltanet_linear_12_gb300 import synthetic as syn
-from tests.helpers import bits, check_bf16, check_f32_out, check_states, to_dev, to_np
+from tests.helpers import Canary, bits, check_bf16, check_f32_out, check_states, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -27,18 +27,19 @@ class Layer:
     def __init__(self, inp):
         self.inp = inp
         self.act = torch.bfloat16 if inp["act"] == "bf16" else torch.float32
-        self.x = to_dev(inp["x"])
+        self.guard = Canary()                      # pools, drafts and outputs between NaN bands
+        self.x = self.guard.wrap(to_dev(inp["x"]))
         self.conv_w = to_dev(inp["conv_w"])
-        self.cs = to_dev(inp["conv_state"])
-        self.S = to_dev(inp["state"])
+        self.cs = self.guard.wrap(to_dev(inp["conv_state"]))
+        self.S = self.guard.wrap(to_dev(inp["state"]))
         self.alpha = to_dev(inp["alpha"])
         self.beta = to_dev(inp["beta"])
         self.z = to_dev(inp["z"])
         self.norm_w = to_dev(inp["norm_w"])
         self.slot = to_dev(inp["slot_idx"])
         B, T, Hv = inp["B"], inp["T"], inp["Hv"]
-        self.out = torch.zeros(B, T, Hv * 128, dtype=self.act, device="cuda")
-        self.pc = torch.zeros(B, T, inp["C"], dtype=self.act, device="cuda")
+        self.out = self.guard.wrap(torch.zeros(B, T, Hv * 128, dtype=self.act, device="cuda"))
+        self.pc = self.guard.wrap(torch.zeros(B, T, inp["C"], dtype=self.act, device="cuda"))
 
     def cfg(self, G, dev_err=None):
         return G.make_config(self.inp["Hk"], self.inp["Hv"], self.act, self.S.shape[0],
@@ -55,16 +56,20 @@ class Layer:
 
 
 def _oracle_verify(orc, inp, commit_all=False):
-    """Oracle verify: activations in the float order (bitwise the GPU's), the
-    recurrence and norm in double."""
+    """Oracle verify in double: the plain conv, SiLU and norms, the activations
+    unrounded into the token-by-token recurrence (the fused kernels keep them
+    on chip), then the gated RMSNorm."""
     return orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"], inp["alpha"],
                       inp["beta"], inp["z"], inp["norm_w"], inp["slot_idx"], inp["Hk"], inp["Hv"],
-                      round_act=inp["act"] == "bf16", commit_all=commit_all, act32=True)
+                      commit_all=commit_all)
 
 
-def _act_bits(pc, act):
-    pc = np.asarray(pc, np.float32)
-    return syn.f32_to_bf16_bits(pc).view(np.int16) if act == "bf16" else pc.view(np.int32)
+def _check_postconv(pc_gpu, pc_ref, act, what="post-conv"):
+    """The stored post-conv copy against the double oracle's unrounded values."""
+    if act == "bf16":
+        check_bf16(to_np(pc_gpu), pc_ref, what=what)
+    else:
+        check_f32_out(to_np(pc_gpu), pc_ref, 1e-5, what)
 
 
 def _used_slots(inp):
@@ -79,11 +84,12 @@ def test_verify_bf16(G, orc, T):
     torch.cuda.synchronize()
     out, pc, cs, st = _oracle_verify(orc, inp)
     check_bf16(to_np(L.out), out, what=f"verify out T={T}")
-    assert np.array_equal(bits(L.pc)[:5], _act_bits(pc[:5], "bf16")), "post-conv bitwise"
+    _check_postconv(L.pc[:5], pc[:5], "bf16")
     # verify is read-only
     assert np.array_equal(bits(L.cs), inp["conv_state"].view(np.int16))
     assert np.array_equal(bits(L.S), inp["state"].view(np.int32))
     assert np.all(to_np(L.out)[5] == 0), "padding entry must not be written"
+    L.guard.check(f"verify T={T}")
 
 
 @pytest.mark.parametrize("T", range(1, 9))                 # every compiled variant
@@ -94,6 +100,49 @@ def test_verify_f32_arm(G, orc, T):
     torch.cuda.synchronize()
     out, pc, _, _ = _oracle_verify(orc, inp)
     check_f32_out(to_np(L.out), out, 1e-4, f"verify f32 out T={T}")
+
+
+# Tolerance of f32 outputs computed with the tensor core's tf32 products (bf16
+# activations, T >= 5): the state and the f32 activations enter with 10 explicit
+# mantissa bits, a relative error up to 2^-10 per operand (truncation); the
+# products and dot products then carry about 2^-9 of the sum of |terms| and the
+# normalised outputs (RMS 1 before the weight and gate) an error near 2^-9.
+TF32_OUT_TOL = 4e-3
+
+
+@pytest.mark.parametrize("T", range(1, 9))
+def test_verify_bf16_act_f32_out(G, orc, T):
+    """The f32-output arm of the bf16 verify: the CUDA-core variants (T <= 4) at
+    the f32 recurrence tolerance, the tensor-core variant (T >= 5) at the bound
+    of its tf32 products, which stays 5x under the bf16 output tolerance."""
+    inp = syn.verify_inputs(6, T, 2, 4, "bf16", seed=230 + T, pad_slots=1)
+    L = Layer(inp)
+    L.out = torch.zeros(inp["B"], T, inp["Hv"] * 128, dtype=torch.float32, device="cuda")
+    cfg = G.make_config(2, 4, torch.bfloat16, L.S.shape[0], out_f32=True)
+    G.gdn_verify_step(cfg, L.x, L.conv_w, L.cs, L.S, L.alpha, L.beta, L.z, L.norm_w, L.out, L.slot,
+                      postconv_out=L.pc)
+    torch.cuda.synchronize()
+    out, pc, _, _ = _oracle_verify(orc, inp)
+    tol = 1e-4 if T <= 4 else TF32_OUT_TOL
+    check_f32_out(to_np(L.out)[:5], out[:5], tol, f"verify bf16 act, f32 out, T={T}")
+    assert np.all(to_np(L.out)[5] == 0), "padding entry must not be written"
+    assert np.array_equal(bits(L.S), inp["state"].view(np.int32))
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_decode_bf16_act_f32_out(G, orc, T):
+    """Decode (commit-all) with f32 outputs: CUDA-core products at every T."""
+    inp = syn.verify_inputs(4, T, 2, 4, "bf16", seed=240 + T)
+    L = Layer(inp)
+    L.out = torch.zeros(inp["B"], T, inp["Hv"] * 128, dtype=torch.float32, device="cuda")
+    cfg = G.make_config(2, 4, torch.bfloat16, L.S.shape[0], out_f32=True)
+    G.gdn_verify_step(cfg, L.x, L.conv_w, L.cs, L.S, L.alpha, L.beta, L.z, L.norm_w, L.out, L.slot,
+                      commit_all=True)
+    torch.cuda.synchronize()
+    out, _, cs, st = _oracle_verify(orc, inp, commit_all=True)
+    check_f32_out(to_np(L.out), out, 1e-4, f"decode f32 out T={T}")
+    assert np.array_equal(to_np(L.cs), cs)
+    check_states(to_np(L.S), st, _used_slots(inp), 1e-4, "decode f32-out state")
 
 
 @pytest.mark.parametrize("T", [1, 3, 8])
@@ -107,6 +156,7 @@ def test_commit_all_equals_verify_then_commit_bitwise(G, orc, T):
     n_keep = torch.full((5,), T, dtype=torch.int32, device="cuda")
     G.gdn_commit_layers(Bl.cfg(G), views, 1, Bl.slot, n_keep, T)
     torch.cuda.synchronize()
+    A.guard.check("decode")
     assert np.array_equal(bits(A.S), bits(Bl.S)), "decode == verify + commit(T), bitwise"
     assert np.array_equal(bits(A.cs), bits(Bl.cs))
     if T == 1:                       # same variant: outputs bitwise too
@@ -140,10 +190,11 @@ def test_commit_layers_against_oracle_and_per_layer(G, orc, T):
         torch.cuda.synchronize()
     torch.cuda.synchronize()
     for lb, ls, inp in zip(batched, single, inps):
+        lb.guard.check("batched commit")
         assert np.array_equal(bits(lb.S), bits(ls.S)), "batched == per-layer commit (bitwise)"
         assert np.array_equal(bits(lb.cs), bits(ls.cs))
         cs, st = orc.commit(inp["x"], inp["alpha"], inp["beta"], inp["conv_w"], inp["conv_state"],
-                            inp["state"], inp["slot_idx"], n_keep, 2, 4, act32=True)
+                            inp["state"], inp["slot_idx"], n_keep, 2, 4)
         assert np.array_equal(to_np(lb.cs), cs), "conv_state commit must be bit-exact"
         check_states(to_np(lb.S), st, range(st.shape[0]), 1e-4, "committed state")
         # slots with n_keep == 0 and slots nobody references stay bitwise untouched
@@ -198,7 +249,7 @@ def test_verify_window_geometry_48_v_heads(G, orc, T):
     torch.cuda.synchronize()
     out, pc, _, _ = _oracle_verify(orc, inp)
     check_bf16(to_np(L.out), out, what=f"verify Hv=48 T={T}")
-    assert np.array_equal(bits(L.pc), _act_bits(pc, "bf16")), "post-conv bitwise"
+    _check_postconv(L.pc, pc, "bf16")
     assert np.array_equal(bits(L.S), inp["state"].view(np.int32))
     L.verify(G, commit_all=True)
     torch.cuda.synchronize()
@@ -221,11 +272,10 @@ def test_verify_q_scale_and_eps(G, orc, T, act):
     torch.cuda.synchronize()
     out, pc, _, _ = orc.verify(inp["x"], inp["conv_w"], inp["conv_state"], inp["state"], inp["alpha"],
                                inp["beta"], inp["z"], inp["norm_w"], inp["slot_idx"], inp["Hk"],
-                               inp["Hv"], q_scale=qs, eps=eps, round_act=act == "bf16",
-                               act32=True)
+                               inp["Hv"], q_scale=qs, eps=eps)
+    _check_postconv(L.pc, pc, act)
     if act == "bf16":
         check_bf16(to_np(L.out), out, what=f"verify q_scale T={T}")
-        assert np.array_equal(bits(L.pc), _act_bits(pc, act)), "post-conv bitwise"
     else:
         check_f32_out(to_np(L.out), out, 1e-4, f"verify q_scale f32 T={T}")
 

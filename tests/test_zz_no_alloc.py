@@ -1,7 +1,11 @@
 """The allocation-free verify entry point (gdn_verify_step_noalloc), for callers
-that cannot allocate device memory themselves, against gdn_verify_step with a
-caller-provided workspace argument. Two calls in a row of different shapes.
-This file is collected last."""
+that cannot allocate device memory themselves (code hosted in a runtime that
+owns every device allocation, services on a fixed memory budget, loops that
+must not synchronise through cudaMalloc). It is the read-only verify with no
+workspace; it launches the same kernel as gdn_verify_step. Checked against
+gdn_verify_step on two calls in a row of different shapes, and the device's
+free memory around a pair of calls on two streams. This file is collected
+last."""
 import ctypes
 
 import numpy as np
@@ -50,6 +54,27 @@ def test_noalloc_matches_workspace_verify_two_calls(G):
     for inp in (first, second):
         ref, new = _verify_both(G, inp)
         check_bf16(new, ref, what=f"no-alloc verify B={inp['B']} T={inp['T']}")
+
+
+def test_noalloc_leaves_free_memory_unchanged(G):
+    """Two calls on two streams, free device memory read before and after."""
+    inp = syn.verify_inputs(8, 5, 2, 4, "bf16", seed=902)
+    d = {k: to_dev(inp[k]) for k in ("x", "conv_w", "conv_state", "state", "alpha", "beta", "z",
+                                      "norm_w", "slot_idx")}
+    cfg = G.make_config(2, 4, torch.bfloat16, d["state"].shape[0])
+    outs = [torch.zeros(8, 5, 4 * D, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    G.gdn_verify_step_noalloc(cfg, d["x"], d["conv_w"], d["conv_state"], d["state"], d["alpha"],
+                              d["beta"], d["z"], d["norm_w"], outs[0], d["slot_idx"])   # warm-up
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for o, st in zip(outs, streams):
+        G.gdn_verify_step_noalloc(cfg, d["x"], d["conv_w"], d["conv_state"], d["state"], d["alpha"],
+                                  d["beta"], d["z"], d["norm_w"], o, d["slot_idx"], stream=st)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+    assert np.array_equal(bits(outs[0]), bits(outs[1]))
 
 
 def test_noalloc_needs_no_memory_of_its_own(G):
