@@ -126,9 +126,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 //   BR  the state, product and Gram barriers, the TMEM address, the issued flag
 template <int A, bool TC> __host__ __device__ constexpr int qk_bytes() { return 2 * MAXT * D * 4; }
 template <int A, bool TC> __host__ __device__ constexpr int qk_region() { return (qk_bytes<A, TC>() + 1023) & ~1023; }
-// v rows [NT][128] f32 of the CUDA-core variants (the tensor-core variant keeps
-// them in registers)
-template <bool TC, int NT> __host__ __device__ constexpr int vs_bytes() { return TC ? 0 : NT * D * 4; }
+// Where the v rows live: shared memory [NT][128] f32 for the CUDA-core variants
+// of up to 4 draft tokens; registers (thread r keeps v_t[r]) for the others,
+// whose 8 rows of f32 would not fit three bf16 blocks per SM.
+template <bool TC, int NT> __host__ __device__ constexpr bool v_in_regs() { return TC || NT == 0 || NT > 4; }
+template <bool TC, int NT> __host__ __device__ constexpr int vs_bytes() { return v_in_regs<TC, NT>() ? 0 : NT * D * 4; }
 template <int A, bool TC, int NT> __host__ __device__ constexpr int verify_smem() {
   return qk_region<A, TC>() + S_BYTES + vs_bytes<TC, NT>() + TAB * 4 + 2 * MAXT * 4 + 32;
 }
@@ -395,11 +397,11 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
       }
     }
   };
-  // Tensor-core variant (T >= 5): q and k: warp w takes tokens 2w, 2w + 1, lanes
-  // 0..15 the q head and 16..31 the k head; v: thread r convolves channel r of
-  // the v head for every draft token and keeps v_t[r] in its registers (the v
-  // rows in f32 would not fit the shared memory of three blocks per SM).
-  auto conv_tc = [&]() {
+  // Variants with v in registers (T >= 5): q and k: warp w takes tokens 2w,
+  // 2w + 1, lanes 0..15 the q head and 16..31 the k head; v: thread r convolves
+  // channel r of the v head for every draft token and keeps v_t[r] in its
+  // registers.
+  auto conv_regs = [&]() {
     constexpr int IT = 2;
     const int n_parts = (T + IT - 1) / IT;
     // v channel r: its taps and column values go in flight before the q, k work
@@ -477,9 +479,11 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
       vr[t] = t < T ? silu(conv4(w4, col[t], col[t + 1], col[t + 2], col[t + 3])) : 0.f;
       if (p.postconv && t < T) store1<A>(p.postconv, xb + (int64_t)t * C + cv, vr[t]);
     }
-    for (int e = tid; e < 16 * (D / 4); e += VT) {        // rows of absent tokens are zero operands
-      const int row = e >> 5, kc = e & 31;
-      if ((row & 7) >= T) *reinterpret_cast<float4*>(QK + bsw_off(row, 4 * kc)) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (TC) {                                   // rows of absent tokens are zero operands
+      for (int e = tid; e < 16 * (D / 4); e += VT) {
+        const int row = e >> 5, kc = e & 31;
+        if ((row & 7) >= T) *reinterpret_cast<float4*>(QK + bsw_off(row, 4 * kc)) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   };
 
@@ -490,7 +494,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
       ga = load_gate(p.alpha, gi, p.gate_bf16);
       gb = load_gate(p.beta, gi, p.gate_bf16);
     }
-    if constexpr (TC) conv_tc();
+    if constexpr (v_in_regs<TC, NT>()) conv_regs();
     else conv_items();
     if (tid < T) {                                       // raw projections: the gate step
       al_s[tid] = p.raw_gates ? gate_alpha(ga) : ga;
@@ -656,7 +660,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
 #pragma unroll
       for (int t = 0; t < MAXT; ++t) {
         if (t < T) {
-          const float vt = TC ? vr[t] : reinterpret_cast<const float*>(VS)[t * D + r];
+          const float vt = v_in_regs<TC, NT>() ? vr[t] : reinterpret_cast<const float*>(VS)[t * D + r];
           float xx = __fmaf_rn(-tb[TAB_BG + t], sk[t], __fmul_rn(tb[TAB_B + t], vt));
 #pragma unroll
           for (int w = 0; w < t; ++w) xx = __fmaf_rn(-tb[TAB_A + t * MAXT + w], dr[w], xx);
