@@ -37,8 +37,10 @@ constexpr int CONV_ROWS = KS + CHUNK;                 // staged rows: 3 before t
 
 constexpr int CONV_HALF_COLS = 2 * D;                 // two heads per TMA box
 template <int A> __host__ __device__ constexpr int conv_half_bytes() { return CONV_ROWS * CONV_HALF_COLS * (A == BF16 ? 2 : 4); }
-template <int A> __host__ __device__ constexpr int conv_tile_bytes() { return 2 * conv_half_bytes<A>(); }
-// Tile buffers: three for bf16 (201 KiB), one for f32 (134 KiB; the f32 path is
+// The item's conv_w rows ([4 heads x 128 channels][4 taps]) follow the two halves.
+template <int A> __host__ __device__ constexpr int conv_w_bytes() { return CONV_HEADS_PER_BLOCK * D * KW * (A == BF16 ? 2 : 4); }
+template <int A> __host__ __device__ constexpr int conv_tile_bytes() { return 2 * conv_half_bytes<A>() + conv_w_bytes<A>(); }
+// Tile buffers: three for bf16 (213 KiB), one for f32 (142 KiB; the f32 path is
 // the test arm, not a streaming workload).
 template <int A> __host__ __device__ constexpr int conv_stages() { return A == BF16 ? 3 : 1; }
 
@@ -140,11 +142,15 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
     const int heads_here = m.flags & CI_VALID ? min(CONV_HEADS_PER_BLOCK, n_heads - m.head0) : 0;
     const uint32_t bytes = n_here > 0 ? (uint32_t)halves * CHUNK * ROW * asz : 0u;
     const uint32_t halo_bytes = halo ? (uint32_t)(KS * heads_here * D * asz) : 0u;   // exact channels
+    const uint32_t w_bytes = (uint32_t)(heads_here * D * KW * asz);   // the item's conv_w rows
     if (lane == 0) {
       meta[st] = m;
       ++n_produced;
       tc::fence_async_smem();                            // earlier reads of the stage come first
-      tc::mbar_arrive_expect_tx(&bar[st], bytes + halo_bytes);
+      tc::mbar_arrive_expect_tx(&bar[st], bytes + halo_bytes + w_bytes);
+      if (w_bytes)
+        tc::bulk_load(tile + 2 * HALF, static_cast<const char*>(conv_w) + (size_t)m.head0 * D * KW * asz, w_bytes,
+                      &bar[st]);
       for (int hf = 0; hf < halves && n_here > 0; ++hf)
         tma_box(tile + (size_t)hf * HALF + (size_t)KS * ROW * asz, &xmap, (m.head0 + 2 * hf) * D,
                 (int)t_chunk, &bar[st]);
@@ -209,6 +215,7 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
       continue;
     }
     const uint8_t* tile = tiles + (size_t)st * TILE + (size_t)(warp & 1) * HALF;   // this warp's half
+    const uint8_t* wtile = tiles + (size_t)st * TILE + 2 * HALF;                    // the item's conv_w rows
     const int slot = m.slot;
     const int64_t seq0 = m.seq0, len = m.len, t_chunk = m.t_chunk;
     const int n_here = m.n_here;
@@ -228,7 +235,7 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
         Raw8<A> wr[4];
         if (active) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) raw_load<A>(conv_w, (int64_t)c0 * KW + 8 * q, wr[q]);
+          for (int q = 0; q < 4; ++q) raw_load<A>(wtile, (int64_t)(c0 - m.head0 * D) * KW + 8 * q, wr[q]);
         } else {
 #pragma unroll
           for (int q = 0; q < 4; ++q) raw_zero<A>(wr[q]);
@@ -256,45 +263,45 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
           p2[q] = make_float2(r2[2 * q], r2[2 * q + 1]);
         }
       }
-      // 8 tokens in pairs, fully unrolled so the three-row window rotates through
-      // registers. A pair's second token may lie past the chunk's end: its tile
-      // row was not staged and its values are discarded.
+      // Conv + SiLU of all 8 tokens first (independent chains for the scheduler),
+      // then the norms and stores in pairs. Tokens past the chunk's end read
+      // stale tile rows; their values are discarded.
+      float v[CONV_TOK][8];
+#pragma unroll
+      for (int u = 0; u < CONV_TOK; ++u) {
+        float xv[8];
+        load8<A>(tile, (int64_t)(u0 + u + KS) * ROW + cb, xv);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 cv = make_float2(xv[2 * q], xv[2 * q + 1]);
+          const float2 a = silu2(conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cv));
+          v[u][2 * q] = a.x;
+          v[u][2 * q + 1] = a.y;
+          p0[q] = p1[q]; p1[q] = p2[q]; p2[q] = cv;
+        }
+      }
 #pragma unroll
       for (int u = 0; u < CONV_TOK; u += 2) {
         if (u >= n_mine) break;                           // uniform per warp
-        float v[2][8];
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          float xv[8];
-          load8<A>(tile, (int64_t)(u0 + u + kk + KS) * ROW + cb, xv);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 cv = make_float2(xv[2 * q], xv[2 * q + 1]);
-            const float2 a = silu2(conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cv));
-            v[kk][2 * q] = a.x;
-            v[kk][2 * q + 1] = a.y;
-            p0[q] = p1[q]; p1[q] = p2[q]; p2[q] = cv;
-          }
-        }
         if constexpr (NORM) {
-          const float ss0 = head_sum_sq16(v[0]);          // all lanes take part
-          const float ss1 = head_sum_sq16(v[1]);
+          const float ss0 = head_sum_sq16(v[u]);          // all lanes take part
+          const float ss1 = head_sum_sq16(v[u + 1]);
           const float rm = inv_norm((lane & 1) ? ss1 : ss0, eps);   // even lanes token u, odd u + 1
           const float rn0 = __shfl_sync(FULL, rm, lane & ~1);
           const float rn1 = __shfl_sync(FULL, rm, lane | 1);
           if (is_qk) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float2 o0 = __fmul2_rn(make_float2(v[0][2 * q], v[0][2 * q + 1]), make_float2(rn0, rn0));
-              const float2 o1 = __fmul2_rn(make_float2(v[1][2 * q], v[1][2 * q + 1]), make_float2(rn1, rn1));
-              v[0][2 * q] = o0.x; v[0][2 * q + 1] = o0.y;
-              v[1][2 * q] = o1.x; v[1][2 * q + 1] = o1.y;
+              const float2 o0 = __fmul2_rn(make_float2(v[u][2 * q], v[u][2 * q + 1]), make_float2(rn0, rn0));
+              const float2 o1 = __fmul2_rn(make_float2(v[u + 1][2 * q], v[u + 1][2 * q + 1]), make_float2(rn1, rn1));
+              v[u][2 * q] = o0.x; v[u][2 * q + 1] = o0.y;
+              v[u + 1][2 * q] = o1.x; v[u + 1][2 * q + 1] = o1.y;
             }
           }
         }
         if (active) {
-          store8<A>(y, (t_chunk + u0 + u) * ld_y + c0, v[0]);
-          if (u + 1 < n_mine) store8<A>(y, (t_chunk + u0 + u + 1) * ld_y + c0, v[1]);
+          store8<A>(y, (t_chunk + u0 + u) * ld_y + c0, v[u]);
+          if (u + 1 < n_mine) store8<A>(y, (t_chunk + u0 + u + 1) * ld_y + c0, v[u + 1]);
         }
       }
     }
