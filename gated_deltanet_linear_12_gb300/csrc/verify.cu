@@ -301,112 +301,70 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
 
   pdl_wait();                                             // inputs of the previous grid are visible
   const int slot = *reinterpret_cast<const volatile int32_t*>(p.slot_idx + b);
-  const bool valid = slot >= 0 && slot < p.n_slots;
-  if (slot >= p.n_slots && tid == 0 && h == 0) report(p.dev_err, GDN_DEVERR_SLOT);
-  if (tid == 0 && valid) {                                // thread 0 initialised the barrier
-    tc::mbar_arrive_expect_tx(s_bar, S_BYTES);
-#pragma unroll
-    for (int bx = 0; bx < 4; ++bx) tma_load_2d(SR + bx * 16384, &smap, 32 * bx, (slot * Hv + h) * D, s_bar);
-  }
   int fail = 0;                                           // 1: before the product, 2: the product
 
-  // z rows and norm_w of this thread's part of the epilogue
+  // Every load that does not depend on the slot goes in flight before the slot
+  // is used (b < B, so each of these addresses is in bounds whatever the slot
+  // holds): the gates, the z rows and norm_w of the epilogue, the taps and the
+  // draft rows of the conv. Then the TMA copy of the state and the conv_state
+  // rows, which need the slot.
   const int et = tid >> 4, el16 = tid & 15;
   Raw8<A> zr;
   float nwr[8];
-  if (valid && et < T) raw_load<A>(p.z, (((int64_t)b * T + et) * Hv + h) * D + el16 * 8, zr);
+  if (et < T) raw_load<A>(p.z, (((int64_t)b * T + et) * Hv + h) * D + el16 * 8, zr);
   else raw_zero<A>(zr);
   load8<F32>(p.norm_w, el16 * 8, nwr);
+  float ga = 0.f, gb = 0.f;
+  if (tid < T) {
+    const int64_t gi = ((int64_t)b * T + tid) * Hv + h;
+    ga = load_gate(p.alpha, gi, p.gate_bf16);
+    gb = load_gate(p.beta, gi, p.gate_bf16);
+  }
 
   // ---- post-conv activations, f32 (unrounded; only the post-conv copy is
-  // rounded to the activation dtype).
-  float vr[MAXT];                                         // tensor-core variant: v_t[r]
+  // rounded to the activation dtype). Two layouts:
+  //   CUDA-core variants up to 4 draft tokens: item (part, head, l16) = thread:
+  //     8 channels of head `head` (0 q, 1 k, 2 v) for the IT tokens IT part ..
+  //     IT part + IT - 1 (at most 96 items); 16-lane groups share (part, head);
+  //     v rows go to VS as f32;
+  //   the others (v in registers): q and k: warp w takes tokens 2w, 2w + 1, lanes
+  //     0..15 the q head and 16..31 the k head; v: thread r convolves channel r of
+  //     the v head for every draft token and keeps v_t[r] in its registers.
+  constexpr bool VREG = v_in_regs<TC, NT>();
+  // tokens per item: 2 at T = 3, 4 (96 items in place of 48, half the serial
+  // work each), else 4; 2 in the register layout
+  constexpr int IT = VREG ? 2 : ((NT == 3 || NT == 4) ? 2 : 4);
+  float vr[MAXT];                                         // register layout: v_t[r]
   const int64_t xb = (int64_t)b * T * C;
-  const int64_t cs = (int64_t)slot * KS * C;
   const bool write_qk = p.postconv && (h % G) == 0;       // one v head of the group writes q, k
-  // CUDA-core variants: item (part, head, l16) = thread: 8 channels of head `head`
-  // (0 q, 1 k, 2 v) for the IT tokens IT part .. IT part + IT - 1 (at most 96
-  // items); 16-lane groups share (part, head); v rows go to VS as f32.
-  auto conv_items = [&]() {
-    // tokens per item: 2 at T = 3, 4 (96 items in place of 48, half the serial
-    // work each), else 4
-    constexpr int IT = (NT == 3 || NT == 4) ? 2 : 4;
-    const int n_items = (T + IT - 1) / IT * 3 * 16;
-    const bool grp = tid < n_items;                       // uniform per 16 lanes
-    const int l16 = tid & 15, head = (tid >> 4) % 3, part = (tid >> 4) / 3;
-    const int t0 = IT * part;
-    const int c = (head == 0 ? hq * D : head == 1 ? (Hk + hq) * D : (2 * Hk + h) * D) + l16 * 8;
-    Raw8<A> wr[4], rw[IT + 3];
-    if (grp) {
+  int l16, head, t0;
+  bool grp;                                               // a q/k (or q/k/v) item: uniform per 16 lanes
+  if constexpr (VREG) {
+    grp = warp < (T + IT - 1) / IT;
+    l16 = lane & 15; head = lane >> 4; t0 = IT * warp;
+  } else {
+    grp = tid < (T + IT - 1) / IT * 3 * 16;
+    l16 = tid & 15; head = (tid >> 4) % 3; t0 = IT * ((tid >> 4) / 3);
+  }
+  const int c = (head == 0 ? hq * D : head == 1 ? (Hk + hq) * D : (2 * Hk + h) * D) + l16 * 8;
+  Raw8<A> wr[4], rw[IT + 3];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) raw_load<A>(p.conv_w, (int64_t)c * KW + 8 * q, wr[q]);
+  for (int j = 0; j < IT + 3; ++j) raw_zero<A>(rw[j]);
+  if (grp) {
 #pragma unroll
-      for (int j = 0; j < IT + 3; ++j) {
-        const int idx = t0 + j;
-        if (idx < KS) raw_load<A>(p.conv_state, cs + (int64_t)idx * C + c, rw[j]);
-        else if (idx - KS < T) raw_load<A>(p.x, xb + (int64_t)(idx - KS) * C + c, rw[j]);
-        else raw_zero<A>(rw[j]);
-      }
-    } else {
+    for (int q = 0; q < 4; ++q) raw_load<A>(p.conv_w, (int64_t)c * KW + 8 * q, wr[q]);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) raw_zero<A>(wr[q]);
-#pragma unroll
-      for (int j = 0; j < IT + 3; ++j) raw_zero<A>(rw[j]);
+    for (int j = 0; j < IT + 3; ++j) {
+      const int idx = t0 + j;
+      if (idx >= KS && idx - KS < T) raw_load<A>(p.x, xb + (int64_t)(idx - KS) * C + c, rw[j]);
     }
-    float2 w[4][4];
+  } else {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float t8[8];
-      raw_unpack<A>(wr[q], t8);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w[q][j] = make_float2(t8[j], t8[4 + j]);
-    }
-#pragma unroll
-    for (int uu = 0; uu < IT; ++uu) {
-      const int t = t0 + uu;
-      const bool live = grp && t < T;
-      float v[8];
-      if (live) {
-        float r0[8], r1[8], r2[8], r3[8];
-        raw_unpack<A>(rw[uu], r0);
-        raw_unpack<A>(rw[uu + 1], r1);
-        raw_unpack<A>(rw[uu + 2], r2);
-        raw_unpack<A>(rw[uu + 3], r3);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 a = silu2(conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], make_float2(r0[2 * q], r0[2 * q + 1]),
-                                            make_float2(r1[2 * q], r1[2 * q + 1]), make_float2(r2[2 * q], r2[2 * q + 1]),
-                                            make_float2(r3[2 * q], r3[2 * q + 1])));
-          v[2 * q] = a.x;
-          v[2 * q + 1] = a.y;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = 0.f;
-      }
-      const float ss = head_sum_sq16(v);                  // all 32 lanes of the warp
-      if (live && head < 2) {
-        const float rr = inv_norm(ss, p.eps);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], rr);
-      }
-      if (live) {
-        if (p.postconv && (head == 2 || write_qk)) store8<A>(p.postconv, xb + (int64_t)t * C + c, v);
-        if (head == 2) store8<F32>(VS, (int64_t)t * D + l16 * 8, v);
-        else put_act8<A, TC>(QK, head ^ 1, t, l16 * 8, v);   // k rows 0..7, q rows 8..15
-      }
-    }
-  };
-  // Variants with v in registers (T >= 5): q and k: warp w takes tokens 2w,
-  // 2w + 1, lanes 0..15 the q head and 16..31 the k head; v: thread r convolves
-  // channel r of the v head for every draft token and keeps v_t[r] in its
-  // registers.
-  auto conv_regs = [&]() {
-    constexpr int IT = 2;
-    const int n_parts = (T + IT - 1) / IT;
-    // v channel r: its taps and column values go in flight before the q, k work
-    const int cv = (2 * Hk + h) * D + tid;
-    float w4[4], col[MAXT + KS];
+    for (int q = 0; q < 4; ++q) raw_zero<A>(wr[q]);
+  }
+  const int cv = (2 * Hk + h) * D + tid;                  // register layout: v channel r
+  float w4[4], col[MAXT + KS];
+  if constexpr (VREG) {
     if constexpr (A == BF16) {
       const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.conv_w) + (int64_t)cv * KW);
       w4[0] = __uint_as_float(u.x << 16); w4[1] = __uint_as_float(u.x & 0xffff0000u);
@@ -416,35 +374,41 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
       w4[0] = f.x; w4[1] = f.y; w4[2] = f.z; w4[3] = f.w;
     }
 #pragma unroll
-    for (int j = 0; j < MAXT + KS; ++j) {
-      if (j < KS) col[j] = load1<A>(p.conv_state, cs + (int64_t)j * C + cv);
-      else col[j] = j - KS < T ? load1<A>(p.x, xb + (int64_t)(j - KS) * C + cv) : 0.f;
+    for (int j = KS; j < MAXT + KS; ++j) col[j] = j - KS < T ? load1<A>(p.x, xb + (int64_t)(j - KS) * C + cv) : 0.f;
+  }
+
+  const bool valid = slot >= 0 && slot < p.n_slots;
+  if (slot >= p.n_slots && tid == 0 && h == 0) report(p.dev_err, GDN_DEVERR_SLOT);
+  if (tid == 0 && valid) {                                // thread 0 initialised the barrier
+    tc::mbar_arrive_expect_tx(s_bar, S_BYTES);
+#pragma unroll
+    for (int bx = 0; bx < 4; ++bx) tma_load_2d(SR + bx * 16384, &smap, 32 * bx, (slot * Hv + h) * D, s_bar);
+  }
+
+  if (valid) {
+    const int64_t cs = (int64_t)slot * KS * C;
+    if (grp) {                                            // the conv_state rows of the item
+#pragma unroll
+      for (int j = 0; j < IT + 3; ++j)
+        if (t0 + j < KS) raw_load<A>(p.conv_state, cs + (int64_t)(t0 + j) * C + c, rw[j]);
     }
-    if (warp < n_parts) {                                 // uniform per warp
-      const int l16 = lane & 15, head = lane >> 4, t0 = IT * warp;
-      const int c = (head == 0 ? hq * D : (Hk + hq) * D) + l16 * 8;
-      Raw8<A> wr[4], rw[IT + 3];
+    if constexpr (VREG) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) raw_load<A>(p.conv_w, (int64_t)c * KW + 8 * q, wr[q]);
+      for (int j = 0; j < KS; ++j) col[j] = load1<A>(p.conv_state, cs + (int64_t)j * C + cv);
+    }
+    float2 w[4][4];
 #pragma unroll
-      for (int j = 0; j < IT + 3; ++j) {
-        const int idx = t0 + j;
-        if (idx < KS) raw_load<A>(p.conv_state, cs + (int64_t)idx * C + c, rw[j]);
-        else if (idx - KS < T) raw_load<A>(p.x, xb + (int64_t)(idx - KS) * C + c, rw[j]);
-        else raw_zero<A>(rw[j]);
-      }
-      float2 w[4][4];
+    for (int q = 0; q < 4; ++q) {
+      float t8[8];
+      raw_unpack<A>(wr[q], t8);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float t8[8];
-        raw_unpack<A>(wr[q], t8);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) w[q][jj] = make_float2(t8[jj], t8[4 + jj]);
-      }
+      for (int j = 0; j < 4; ++j) w[q][j] = make_float2(t8[j], t8[4 + j]);
+    }
+    if (!VREG || grp) {                                   // uniform per warp
 #pragma unroll
       for (int uu = 0; uu < IT; ++uu) {
         const int t = t0 + uu;
-        const bool live = t < T;                          // uniform per warp
+        const bool live = grp && t < T;
         float v[8];
         if (live) {
           float r0[8], r1[8], r2[8], r3[8];
@@ -462,22 +426,27 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
           }
         } else {
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) v[jj] = 0.f;
+          for (int j = 0; j < 8; ++j) v[j] = 0.f;
         }
         const float ss = head_sum_sq16(v);                // all 32 lanes of the warp
-        if (live) {
+        if (live && head < 2) {
           const float rr = inv_norm(ss, p.eps);
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) v[jj] = __fmul_rn(v[jj], rr);
-          if (write_qk) store8<A>(p.postconv, xb + (int64_t)t * C + c, v);
-          put_act8<A, TC>(QK, head ^ 1, t, l16 * 8, v);   // k rows 0..7, q rows 8..15
+          for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], rr);
+        }
+        if (live) {
+          if (p.postconv && (head == 2 || write_qk)) store8<A>(p.postconv, xb + (int64_t)t * C + c, v);
+          if (head == 2) store8<F32>(VS, (int64_t)t * D + l16 * 8, v);
+          else put_act8<A, TC>(QK, head ^ 1, t, l16 * 8, v);   // k rows 0..7, q rows 8..15
         }
       }
     }
+    if constexpr (VREG) {
 #pragma unroll
-    for (int t = 0; t < MAXT; ++t) {
-      vr[t] = t < T ? silu(conv4(w4, col[t], col[t + 1], col[t + 2], col[t + 3])) : 0.f;
-      if (p.postconv && t < T) store1<A>(p.postconv, xb + (int64_t)t * C + cv, vr[t]);
+      for (int t = 0; t < MAXT; ++t) {
+        vr[t] = t < T ? silu(conv4(w4, col[t], col[t + 1], col[t + 2], col[t + 3])) : 0.f;
+        if (p.postconv && t < T) store1<A>(p.postconv, xb + (int64_t)t * C + cv, vr[t]);
+      }
     }
     if constexpr (TC) {                                   // rows of absent tokens are zero operands
       for (int e = tid; e < 16 * (D / 4); e += VT) {
@@ -485,17 +454,6 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
         if ((row & 7) >= T) *reinterpret_cast<float4*>(QK + bsw_off(row, 4 * kc)) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-  };
-
-  if (valid) {
-    float ga = 0.f, gb = 0.f;
-    if (tid < T) {
-      const int64_t gi = ((int64_t)b * T + tid) * Hv + h;
-      ga = load_gate(p.alpha, gi, p.gate_bf16);
-      gb = load_gate(p.beta, gi, p.gate_bf16);
-    }
-    if constexpr (v_in_regs<TC, NT>()) conv_regs();
-    else conv_items();
     if (tid < T) {                                       // raw projections: the gate step
       al_s[tid] = p.raw_gates ? gate_alpha(ga) : ga;
       be_s[tid] = p.raw_gates ? gate_beta(gb) : gb;
