@@ -264,9 +264,9 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
         }
       }
       // Conv + SiLU of all 8 tokens first (independent chains for the scheduler),
-      // then the norms and stores in pairs. Tokens past the chunk's end read
-      // stale tile rows; their values are discarded.
-      float v[CONV_TOK][8];
+      // then the q/k norms of the 8 tokens together, then the stores. Tokens
+      // past the chunk's end read stale tile rows; their values are discarded.
+      float v[CONV_TOK][8], g[CONV_TOK];
 #pragma unroll
       for (int u = 0; u < CONV_TOK; ++u) {
         float xv[8];
@@ -274,35 +274,35 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float2 cv = make_float2(xv[2 * q], xv[2 * q + 1]);
-          const float2 a = silu2(conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cv));
+          const float2 y2 = conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cv);
+          const float2 a = make_float2(silu_hw(y2.x), silu_hw(y2.y));
           v[u][2 * q] = a.x;
           v[u][2 * q + 1] = a.y;
           p0[q] = p1[q]; p1[q] = p2[q]; p2[q] = cv;
         }
+        if constexpr (NORM) g[u] = lane_sum_sq8(v[u]);
       }
+      if constexpr (NORM) {
+        if (__any_sync(FULL, is_qk)) {                  // warps of v heads only skip it
+          const float r = lanes_inv_norm8(g, eps);      // tokens past n_mine: discarded
 #pragma unroll
-      for (int u = 0; u < CONV_TOK; u += 2) {
-        if (u >= n_mine) break;                           // uniform per warp
-        if constexpr (NORM) {
-          const float ss0 = head_sum_sq16(v[u]);          // all lanes take part
-          const float ss1 = head_sum_sq16(v[u + 1]);
-          const float rm = inv_norm((lane & 1) ? ss1 : ss0, eps);   // even lanes token u, odd u + 1
-          const float rn0 = __shfl_sync(FULL, rm, lane & ~1);
-          const float rn1 = __shfl_sync(FULL, rm, lane | 1);
-          if (is_qk) {
+          for (int u = 0; u < CONV_TOK; ++u) {
+            const float rn = __shfl_sync(FULL, r, (lane & 16) | token_lane(u));
+            if (is_qk) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float2 o0 = __fmul2_rn(make_float2(v[u][2 * q], v[u][2 * q + 1]), make_float2(rn0, rn0));
-              const float2 o1 = __fmul2_rn(make_float2(v[u + 1][2 * q], v[u + 1][2 * q + 1]), make_float2(rn1, rn1));
-              v[u][2 * q] = o0.x; v[u][2 * q + 1] = o0.y;
-              v[u + 1][2 * q] = o1.x; v[u + 1][2 * q + 1] = o1.y;
+              for (int q = 0; q < 4; ++q) {
+                const float2 o = __fmul2_rn(make_float2(v[u][2 * q], v[u][2 * q + 1]), make_float2(rn, rn));
+                v[u][2 * q] = o.x;
+                v[u][2 * q + 1] = o.y;
+              }
             }
           }
         }
-        if (active) {
-          store8<A>(y, (t_chunk + u0 + u) * ld_y + c0, v[u]);
-          if (u + 1 < n_mine) store8<A>(y, (t_chunk + u0 + u + 1) * ld_y + c0, v[u + 1]);
-        }
+      }
+      if (active) {
+#pragma unroll
+        for (int u = 0; u < CONV_TOK; ++u)
+          if (u < n_mine) store8<A>(y, (t_chunk + u0 + u) * ld_y + c0, v[u]);
       }
     }
 
