@@ -140,21 +140,13 @@ __device__ __forceinline__ float2 conv4x2(float2 w0, float2 w1, float2 w2, float
   }
 }
 
-// SiLU y / (1 + e^-y) with the hardware exponential and reciprocal (__expf,
-// __fdividef). Relative error against the exact value: a few ulp plus
-// |y| 2^-24 from the rounding of the exponent's argument (below 2e-6 for
-// |y| <= 30); for y < -87 the exponential overflows and the result is -0,
-// against an exact value below 6e-37 in magnitude.
-__device__ __forceinline__ float silu(float y) {
-  return __fdividef(y, 1.0f + __expf(-y));
-}
-__device__ __forceinline__ float2 silu2(float2 y) { return make_float2(silu(y.x), silu(y.y)); }
-
-// SiLU y * 1 / (1 + 2^(-y log2 e)) with the hardware power of two and
-// reciprocal approximations (ftz) written out: one multiply, two MUFU operations,
-// one add and one multiply, fewer instructions than silu's __expf / __fdividef.
-// Error of the same order as silu's (a few ulp plus |y| 2^-24 from the rounding
-// of the exponent's argument); y < -88 gives -0 as silu does.
+// SiLU y / (1 + e^-y), computed as y * 1 / (1 + 2^(-y log2 e)) with the
+// hardware power of two and reciprocal approximations (ftz) written out: one
+// multiply, two MUFU operations, one add and one multiply. Relative error
+// against the exact value: a few ulp plus |y| 2^-24 from the rounding of the
+// exponent's argument (below 2e-6 for |y| <= 30); for y < -88 the power
+// overflows and the result is -0, against an exact value below 6e-37 in
+// magnitude.
 __device__ __forceinline__ float hw_ex2(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -165,10 +157,11 @@ __device__ __forceinline__ float hw_rcp(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
-__device__ __forceinline__ float silu_hw(float y) {
-  constexpr float kNegLog2e = -1.4426950408889634f;
+__device__ __forceinline__ float silu(float y) {
+  constexpr float kNegLog2e = -1.4426950408889634f;     // -1 / ln 2
   return __fmul_rn(y, hw_rcp(__fadd_rn(1.0f, hw_ex2(__fmul_rn(y, kNegLog2e)))));
 }
+__device__ __forceinline__ float2 silu2(float2 y) { return make_float2(silu(y.x), silu(y.y)); }
 
 // SiLU of the output gate z: the same function.
 __device__ __forceinline__ float silu_gate(float z) { return silu(z); }

@@ -274,8 +274,7 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float2 cv = make_float2(xv[2 * q], xv[2 * q + 1]);
-          const float2 y2 = conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cv);
-          const float2 a = make_float2(silu_hw(y2.x), silu_hw(y2.y));
+          const float2 a = silu2(conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], p0[q], p1[q], p2[q], cv));
           v[u][2 * q] = a.x;
           v[u][2 * q + 1] = a.y;
           p0[q] = p1[q]; p1[q] = p2[q]; p2[q] = cv;
