@@ -327,9 +327,13 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   //     8 channels of head `head` (0 q, 1 k, 2 v) for the IT tokens IT part ..
   //     IT part + IT - 1 (at most 96 items); 16-lane groups share (part, head);
   //     v rows go to VS as f32;
-  //   the others (v in registers): q and k: warp w takes tokens 2w, 2w + 1, lanes
+  //   the others (v in registers): q and k: warp w takes tokens w + 4 and w, lanes
   //     0..15 the q head and 16..31 the k head; v: thread r convolves channel r of
   //     the v head for every draft token and keeps v_t[r] in its registers.
+  // Tokens 0..2 read conv_state rows, which wait for the slot index; in the
+  // register layout every thread convolves its tokens that read draft rows only
+  // first (tokens 3.. in the v loop, token w + 4 in the q/k pairs), so that those
+  // rows' latency hides behind that work.
   constexpr bool VREG = v_in_regs<TC, NT>();
   // tokens per item: 2 at T = 3, 4 (96 items in place of 48, half the serial
   // work each), else 4; 2 in the register layout
@@ -340,22 +344,27 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   int l16, head, t0;
   bool grp;                                               // a q/k (or q/k/v) item: uniform per 16 lanes
   if constexpr (VREG) {
-    grp = warp < (T + IT - 1) / IT;
-    l16 = lane & 15; head = lane >> 4; t0 = IT * warp;
+    grp = warp < (T < 4 ? T : 4);
+    l16 = lane & 15; head = lane >> 4; t0 = warp;
   } else {
     grp = tid < (T + IT - 1) / IT * 3 * 16;
     l16 = tid & 15; head = (tid >> 4) % 3; t0 = IT * ((tid >> 4) / 3);
   }
   const int c = (head == 0 ? hq * D : head == 1 ? (Hk + hq) * D : (2 * Hk + h) * D) + l16 * 8;
-  Raw8<A> wr[4], rw[IT + 3];
+  // conv rows held per thread: the four rows of each of the two tokens (register
+  // layout), else the item's IT + 3 consecutive rows; prow(k) = the row of slot k
+  // in the sequence (3 conv_state rows, then the T draft rows)
+  constexpr int NR = VREG ? 8 : IT + 3;
+  auto prow = [&](int k) { return VREG ? (k < 4 ? t0 + 4 + k : t0 + k - 4) : t0 + k; };
+  Raw8<A> wr[4], rw[NR];
 #pragma unroll
-  for (int j = 0; j < IT + 3; ++j) raw_zero<A>(rw[j]);
+  for (int j = 0; j < NR; ++j) raw_zero<A>(rw[j]);
   if (grp) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) raw_load<A>(p.conv_w, (int64_t)c * KW + 8 * q, wr[q]);
 #pragma unroll
-    for (int j = 0; j < IT + 3; ++j) {
-      const int idx = t0 + j;
+    for (int j = 0; j < NR; ++j) {
+      const int idx = prow(j);
       if (idx >= KS && idx - KS < T) raw_load<A>(p.x, xb + (int64_t)(idx - KS) * C + c, rw[j]);
     }
   } else {
@@ -389,8 +398,8 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     const int64_t cs = (int64_t)slot * KS * C;
     if (grp) {                                            // the conv_state rows of the item
 #pragma unroll
-      for (int j = 0; j < IT + 3; ++j)
-        if (t0 + j < KS) raw_load<A>(p.conv_state, cs + (int64_t)(t0 + j) * C + c, rw[j]);
+      for (int j = 0; j < NR; ++j)
+        if (prow(j) < KS) raw_load<A>(p.conv_state, cs + (int64_t)prow(j) * C + c, rw[j]);
     }
     if constexpr (VREG) {
 #pragma unroll
@@ -407,15 +416,16 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     if (!VREG || grp) {                                   // uniform per warp
 #pragma unroll
       for (int uu = 0; uu < IT; ++uu) {
-        const int t = t0 + uu;
+        const int t = VREG ? (uu == 0 ? t0 + 4 : t0) : t0 + uu;
+        const int k0 = VREG ? 4 * uu : uu;                // the token's first row slot
         const bool live = grp && t < T;
         float v[8];
         if (live) {
           float r0[8], r1[8], r2[8], r3[8];
-          raw_unpack<A>(rw[uu], r0);
-          raw_unpack<A>(rw[uu + 1], r1);
-          raw_unpack<A>(rw[uu + 2], r2);
-          raw_unpack<A>(rw[uu + 3], r3);
+          raw_unpack<A>(rw[k0], r0);
+          raw_unpack<A>(rw[k0 + 1], r1);
+          raw_unpack<A>(rw[k0 + 2], r2);
+          raw_unpack<A>(rw[k0 + 3], r3);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const float2 a = silu2(conv4x2<A>(w[q][0], w[q][1], w[q][2], w[q][3], make_float2(r0[2 * q], r0[2 * q + 1]),
@@ -443,7 +453,8 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     }
     if constexpr (VREG) {
 #pragma unroll
-      for (int t = 0; t < MAXT; ++t) {
+      for (int k = 0; k < MAXT; ++k) {                    // tokens 3 .. 7, then 0 .. 2
+        const int t = (k + KS) % MAXT;
         vr[t] = t < T ? silu(conv4(w4, col[t], col[t + 1], col[t + 2], col[t + 3])) : 0.f;
         if (p.postconv && t < T) store1<A>(p.postconv, xb + (int64_t)t * C + cv, vr[t]);
       }
