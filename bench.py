@@ -108,6 +108,7 @@ def prefill_roofline(kernel, flops, nbytes, ms, peaks, peak_src, traffic):
     floor_hbm_us = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
     floor_c_us = flops / (c_peak * 1e12) * 1e6
     common = {"algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
+              "traffic_per": "launch (ncu, one pass)",
               "floor_us": {"hbm": round(floor_hbm_us, 2), c_bound: round(floor_c_us, 2)},
               "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
               f"{c_bound}_tflops": round(tflops, 3), f"{c_bound}_frac": round(tflops / c_peak, 4)}
@@ -636,7 +637,9 @@ def run_workload(name, T, args, torch, G, dev, world, barrier, flush, lazy=False
                 "achieved": ka["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ka["frac_hbm"], "traffic": ncu_traffic(vk, W.name + f"/T{W.T}"),
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                "algorithmic_bytes": W.bytes["verify"], "per": "window of all layers"}
+                "algorithmic_bytes_per_window": W.bytes["verify"],
+                "algorithmic_bytes_per_launch": W.bytes["verify"] // W.LAYERS,
+                "traffic_per": "launch (ncu, one pass)"}
         value = whole_job_rate(W.tokens * W.LAYERS, world, ms_max)
     else:
         pf_tflops = W.flops["prefill"] / (b_avg * 1e-3) / 1e12
@@ -651,7 +654,8 @@ def run_workload(name, T, args, torch, G, dev, world, barrier, flush, lazy=False
                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(conv_gbs / peaks["hbm_gbs"], 4),
                     "traffic": ncu_traffic("conv_fwd_kernel", W.name),
-                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                    "algorithmic_bytes_per_launch": W.bytes["conv"], "traffic_per": "launch (ncu, one pass)"}
         kernels = {
             "conv_fwd_kernel": {"ms": round(a_avg, 4), "bytes": W.bytes["conv"],
                                 "GB/s": round(conv_gbs, 1),
