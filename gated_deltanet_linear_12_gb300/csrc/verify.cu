@@ -229,9 +229,10 @@ template <int A> __host__ __device__ constexpr int blocks_per_sm() { return A ==
 // Before waiting for the previous grid the block sets up its barriers (and TMEM)
 // and, in the CUDA-core variants, gives L2 hints: its own state (for the blocks
 // that become resident while the previous grid drains) and the rows of the unit
-// one wave of resident blocks later. Everything the block reads is read after the wait (a hint only uses a
-// slot index that may still change). Then thread 0 starts the four TMA copies of
-// the state, and per block:
+// one wave of resident blocks later. Everything the block reads is read after
+// the wait (a hint only uses a slot index that may still change). Then the
+// conv's loads, the conv_state rows and thread 0's four TMA copies of the state
+// (after its conv for T = 3, 4), and per block:
 //   - the conv + SiLU of the unit's q, k and v heads for the T draft rows (rows
 //     t..t+3 of conv_state ++ x feed token t) and the L2 norms of q and k; q, k, v
 //     rounded to the activation dtype are kept in shared memory;
@@ -308,8 +309,8 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   // Every load that does not depend on the slot goes in flight before the slot
   // is used (b < B, so each of these addresses is in bounds whatever the slot
   // holds): the gates, the z rows and norm_w of the epilogue, the taps and the
-  // draft rows of the conv. Then the TMA copy of the state and the conv_state
-  // rows, which need the slot.
+  // draft rows of the conv. Then the conv_state rows and the TMA copy of the
+  // state, which need the slot.
   const int et = tid >> 4, el16 = tid & 15;
   Raw8<A> zr;
   float nwr[8];
@@ -390,12 +391,19 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
 
   const bool valid = slot >= 0 && slot < p.n_slots;
   if (slot >= p.n_slots && tid == 0 && h == 0) report(p.dev_err, GDN_DEVERR_SLOT);
-  if (tid == 0 && valid) {                                // thread 0 initialised the barrier
-    tc::mbar_arrive_expect_tx(s_bar, S_BYTES);
-#pragma unroll
-    for (int bx = 0; bx < 4; ++bx) tma_load_2d(SR + bx * 16384, &smap, 32 * bx, (slot * Hv + h) * D, s_bar);
-  }
 
+  // Thread 0 (which initialised the barrier) starts the TMA copies of the state
+  // after its conv_state loads, or, for the 2-token items at T = 3, 4, after its
+  // conv: the small loads the conv waits on go first (a state copy issued before
+  // them delayed them and made every window slower, by up to 23 %).
+  constexpr bool STATE_AFTER_CONV = !TC && (NT == 3 || NT == 4);
+  auto start_state_copy = [&]() {
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(s_bar, S_BYTES);
+#pragma unroll
+      for (int bx = 0; bx < 4; ++bx) tma_load_2d(SR + bx * 16384, &smap, 32 * bx, (slot * Hv + h) * D, s_bar);
+    }
+  };
   if (valid) {
     const int64_t cs = (int64_t)slot * KS * C;
     if (grp) {                                            // the conv_state rows of the item
@@ -407,6 +415,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
 #pragma unroll
       for (int j = 0; j < KS; ++j) col[j] = load1<A>(p.conv_state, cs + (int64_t)j * C + cv);
     }
+    if constexpr (!STATE_AFTER_CONV) start_state_copy();
     float2 w[4][4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -467,6 +476,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
         if ((row & 7) >= T) *reinterpret_cast<float4*>(QK + bsw_off(row, 4 * kc)) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
+    if constexpr (STATE_AFTER_CONV) start_state_copy();
     if (tid < T) {                                       // raw projections: the gate step
       al_s[tid] = p.raw_gates ? gate_alpha(ga) : ga;
       be_s[tid] = p.raw_gates ? gate_beta(gb) : gb;
