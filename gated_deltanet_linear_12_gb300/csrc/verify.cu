@@ -162,6 +162,16 @@ template <int A> __device__ __forceinline__ float load1(const void* base, int64_
   if constexpr (A == BF16) return bf2f(static_cast<const uint16_t*>(base)[i]);
   else return static_cast<const float*>(base)[i];
 }
+// The same as raw bits (bf16 in the low half, or the f32 bits), widened later:
+// a load whose value is not used at once does not stall the loads after it.
+template <int A> __device__ __forceinline__ uint32_t load1_bits(const void* base, int64_t i) {
+  if constexpr (A == BF16) return static_cast<const uint16_t*>(base)[i];
+  else return static_cast<const uint32_t*>(base)[i];
+}
+template <int A> __device__ __forceinline__ float bits_to_f(uint32_t b) {
+  if constexpr (A == BF16) return __uint_as_float(b << 16);
+  else return __uint_as_float(b);
+}
 template <int A> __device__ __forceinline__ void store1(void* base, int64_t i, float v) {
   if constexpr (A == BF16) static_cast<uint16_t*>(base)[i] = f2bf(v);
   else static_cast<float*>(base)[i] = v;
@@ -375,18 +385,19 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     for (int q = 0; q < 4; ++q) raw_zero<A>(wr[q]);
   }
   const int cv = (2 * Hk + h) * D + tid;                  // register layout: v channel r
-  float w4[4], col[MAXT + KS];
+  // register layout: the v channel's taps and rows as raw bits, widened at the v
+  // conv, so that the conv_state loads and the state copy are not held up
+  uint4 w4r = make_uint4(0u, 0u, 0u, 0u);
+  uint32_t colr[MAXT + KS];
   if constexpr (VREG) {
     if constexpr (A == BF16) {
       const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.conv_w) + (int64_t)cv * KW);
-      w4[0] = __uint_as_float(u.x << 16); w4[1] = __uint_as_float(u.x & 0xffff0000u);
-      w4[2] = __uint_as_float(u.y << 16); w4[3] = __uint_as_float(u.y & 0xffff0000u);
+      w4r.x = u.x; w4r.y = u.y;
     } else {
-      const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(p.conv_w) + (int64_t)cv * KW);
-      w4[0] = f.x; w4[1] = f.y; w4[2] = f.z; w4[3] = f.w;
+      w4r = *reinterpret_cast<const uint4*>(static_cast<const float*>(p.conv_w) + (int64_t)cv * KW);
     }
 #pragma unroll
-    for (int j = KS; j < MAXT + KS; ++j) col[j] = j - KS < T ? load1<A>(p.x, xb + (int64_t)(j - KS) * C + cv) : 0.f;
+    for (int j = KS; j < MAXT + KS; ++j) colr[j] = j - KS < T ? load1_bits<A>(p.x, xb + (int64_t)(j - KS) * C + cv) : 0u;
   }
 
   const bool valid = slot >= 0 && slot < p.n_slots;
@@ -413,7 +424,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     }
     if constexpr (VREG) {
 #pragma unroll
-      for (int j = 0; j < KS; ++j) col[j] = load1<A>(p.conv_state, cs + (int64_t)j * C + cv);
+      for (int j = 0; j < KS; ++j) colr[j] = load1_bits<A>(p.conv_state, cs + (int64_t)j * C + cv);
     }
     if constexpr (!STATE_AFTER_CONV) start_state_copy();
     float2 w[4][4];
@@ -463,6 +474,16 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
       }
     }
     if constexpr (VREG) {
+      float w4[4], col[MAXT + KS];
+      if constexpr (A == BF16) {
+        w4[0] = __uint_as_float(w4r.x << 16); w4[1] = __uint_as_float(w4r.x & 0xffff0000u);
+        w4[2] = __uint_as_float(w4r.y << 16); w4[3] = __uint_as_float(w4r.y & 0xffff0000u);
+      } else {
+        w4[0] = __uint_as_float(w4r.x); w4[1] = __uint_as_float(w4r.y);
+        w4[2] = __uint_as_float(w4r.z); w4[3] = __uint_as_float(w4r.w);
+      }
+#pragma unroll
+      for (int j = 0; j < MAXT + KS; ++j) col[j] = bits_to_f<A>(colr[j]);
 #pragma unroll
       for (int k = 0; k < MAXT; ++k) {                    // tokens 3 .. 7, then 0 .. 2
         const int t = (k + KS) % MAXT;
