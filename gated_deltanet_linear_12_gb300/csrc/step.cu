@@ -162,20 +162,22 @@ __device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, cons
   const int h0 = blockIdx.x * G;                                   // first v head
   const int nh = G;                                                // v heads here
 
-  // The first head's state rows go in flight before anything else, so the
-  // 64 KiB read overlaps the conv and table phases (coalesced: 4 lanes cover
-  // 64 contiguous bytes of a row; this thread owns rows 2rp, 2rp+1).
+  // The first head's state rows (coalesced: 4 lanes cover 64 contiguous bytes of
+  // a row; this thread owns rows 2rp, 2rp+1) go in flight after the small loads
+  // the block waits on first: after the conv in decode and verify (7.53 -> 7.13 ms
+  // per decode window), after the gates in the commit (0.914 -> 0.881 ms at
+  // T = 8). Issued before them, the 64 KiB read delayed those loads.
   const int rp = tid >> 2, cg = tid & 3;
   const int row0 = 2 * rp;
   float4 S[2][8];
-  {
+  auto load_first_state = [&]() {
     const float* Sg0 = state + (((int64_t)slot * Hv + h0) * D) * D;
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
       for (int m = 0; m < 8; ++m)
         S[rr][m] = reinterpret_cast<const float4*>(Sg0 + (int64_t)(row0 + rr) * D)[4 * m + cg];
-  }
+  };
 
   // shared memory: q[T][D], k[T][D], v[nh][T][D], o[T][D], small tables
   float* q_s = smem;
@@ -206,6 +208,8 @@ __device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, cons
     al_s[g * MAXT + t] = p.raw_gates ? gate_alpha(ga) : ga;      // raw projections: the gate step
     be_s[g * MAXT + t] = p.raw_gates ? gate_beta(gb) : gb;
   }
+
+  if constexpr (MODE == COMMIT) load_first_state();
 
   // ---- phase 1: post-conv activations of the block's channels, tokens < n
   {
@@ -269,6 +273,8 @@ __device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, cons
       }
     }
   }
+
+  if constexpr (MODE != COMMIT) load_first_state();
 
   // ---- phase 2: key/key and query/key dot products (shared by the group)
   for (int pr = warp; pr < 2 * MAXT * MAXT; pr += STEP_THREADS / 32) {
