@@ -281,6 +281,11 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
         }
         if constexpr (NORM) g[u] = lane_sum_sq8(v[u]);
       }
+      // The tile is read: release the stage now, so that its next copies start
+      // while this warp takes the norms and stores (the loads, not the
+      // arithmetic, set the item period).
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[st]);
       if constexpr (NORM) {
         if (__any_sync(FULL, is_qk)) {                  // warps of v heads only skip it
           const float r = lanes_inv_norm8(g, eps);      // tokens past n_mine: discarded
@@ -303,6 +308,9 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
         for (int u = 0; u < CONV_TOK; ++u)
           if (u < n_mine) store8<A>(y, (t_chunk + u0 + u) * ld_y + c0, v[u]);
       }
+    } else {
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[st]);          // nothing of the tile to read
     }
 
     // Final conv_state: rows len, len+1, len+2 of (initial rows ++ x rows),
@@ -326,8 +334,6 @@ conv_fwd_kernel(const void* __restrict__ x, int64_t ld_x, void* __restrict__ y, 
         store8<A>(conv_state, st_base + (int64_t)r * C + c0, v);
       }
     }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&empty[st]);            // this warp is done with the stage
   }
   // Before the block exits no copy into its shared memory may still be in
   // flight: after a failed wait, wait (bounded) for the last copy of each stage.
