@@ -338,7 +338,7 @@ class StepWorkload:
 
     LAYERS = 36
 
-    def __init__(self, name, torch, G, device, T=None, gates="activated", lazy=False):
+    def __init__(self, name, torch, G, device, T=None, gates="activated", lazy=False, batch=None):
         self.name, self.torch, self.G, self.dev = name, torch, G, device
         self.gates = gates
         raw = gates == "raw"
@@ -347,7 +347,7 @@ class StepWorkload:
         decode = name == "decode-bf16"
         self.decode = decode
         h48 = name == "spec-verify-bf16-h48"
-        self.B = 256 if decode else 1 if h48 else 32
+        self.B = batch or (256 if decode else 1 if h48 else 32)
         self.T = 1 if decode else (T or 8)
         self.Hk, self.Hv = 16, 48 if h48 else 32
         self.C = (2 * self.Hk + self.Hv) * D
@@ -561,13 +561,13 @@ CPU_PREFILL_TOKENS = {"tiny-f32": None, "varlen-prefill-bf16": None, "long-prefi
 
 
 def run_workload(name, T, args, torch, G, dev, world, barrier, flush, lazy=False, steps=None,
-                 cpu=True):
+                 cpu=True, batch=None):
     """Times one workload (value: device time of the step, CUDA events on the
     launching stream; e2e: the same calls with host copies). Returns the fields
     of its JSON entry; every rank returns, rank 0's is printed."""
     steps = steps or args.steps
     if name in WINDOWS:
-        W = StepWorkload(name, torch, G, dev, T=T, gates=args.gates, lazy=lazy)
+        W = StepWorkload(name, torch, G, dev, T=T, gates=args.gates, lazy=lazy, batch=batch)
     else:
         W = PrefillWorkload(name, torch, G, dev, gates=args.gates)
     for _ in range(max(args.warmup, 3)):
@@ -698,6 +698,9 @@ def main():
                     help=f"one workload only (default: {HEADLINE} as the headline, then the others)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--T", type=int, default=8, help="draft tokens of spec-verify-bf16")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="sequences of the --workload window (decode-bf16, spec-verify-bf16): "
+                         "a smaller case of the same kernels for profiling; not a bench line")
     ap.add_argument("--lazy", action="store_true",
                     help="verify windows: fold each window's commit into the next window's verify")
     ap.add_argument("--gates", default="activated", choices=["activated", "raw"],
@@ -729,7 +732,8 @@ def main():
 
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     name = args.workload or HEADLINE
-    head = run_workload(name, args.T, args, torch, G, dev, world, barrier, flush, lazy=args.lazy)
+    head = run_workload(name, args.T, args, torch, G, dev, world, barrier, flush, lazy=args.lazy,
+                        batch=args.batch)
     extras = {}
     if args.workload is None:
         for wname, T in EXTRAS:
