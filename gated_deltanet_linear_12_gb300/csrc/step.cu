@@ -331,15 +331,8 @@ __device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, cons
     if constexpr (MODE == COMMIT) {
       if (tid == 0 && g + 1 < nh) prefetch_state_l2(state + (((int64_t)slot * Hv + h + 1) * D) * D);
     }
-    // state rows of head h (the first head's are already in flight)
+    // state rows of head h: in flight since the previous head's products / commit
     float* Sg = state + (((int64_t)slot * Hv + h) * D) * D;
-    if (g > 0) {
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-          S[rr][m] = reinterpret_cast<const float4*>(Sg + (int64_t)(row0 + rr) * D)[4 * m + cg];
-    }
     __syncthreads();                                      // tables ready
 
     float d0[MAXT], d1[MAXT];
@@ -405,6 +398,14 @@ __device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, cons
         reinterpret_cast<float4*>(Sg + (int64_t)row0 * D)[4 * m + cg] = a;
         reinterpret_cast<float4*>(Sg + (int64_t)(row0 + 1) * D)[4 * m + cg] = c;
       }
+    }
+    if (g + 1 < nh) {                                     // the next head's rows go in flight now,
+      const float* Sn = Sg + (int64_t)D * D;              // under this head's epilogue
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+          S[rr][m] = reinterpret_cast<const float4*>(Sn + (int64_t)(row0 + rr) * D)[4 * m + cg];
     }
 
     // z-gated RMSNorm of the outputs: one 16-lane group per token
