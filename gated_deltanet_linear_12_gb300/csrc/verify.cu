@@ -565,19 +565,49 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
       // first T tokens are the first T^2. Lane l holds columns 4l..4l+3 (a product
       // and three fused multiply-adds), then an xor butterfly 16, 8, 4, 2, 1: the
       // step kernel's warp dot product.
+      if constexpr (NT >= 3) {
+        // T = 3, 4: an 8-lane group per pair (lane holds 16 columns, a product and
+        // 15 fused multiply-adds, then an xor butterfly 4, 2, 1), four pairs per
+        // warp at once: the T^2 pairs in one round instead of T^2 / 4 serial ones
+        // (these outputs are held to the oracle's tolerance, not to the step
+        // kernel's bits, which only T = 1 shares)
+        const int sub = lane & 7;
 #pragma unroll 1
-      for (int i = warp; i < T * T; i += VT / 32) {
-        const int t = (i >= 1) + (i >= 4) + (i >= 9) + (i >= 16) + (i >= 25) + (i >= 36) + (i >= 49);
-        const int j = i - t * t, which = j >= t, s = which ? j - t : j;
-        const float4 x = act4<A, TC>(QK, which, t, lane);
-        const float4 y = act4<A, TC>(QK, 0, s, lane);
-        float d = __fmul_rn(x.x, y.x);
-        d = __fmaf_rn(x.y, y.y, d);
-        d = __fmaf_rn(x.z, y.z, d);
-        d = __fmaf_rn(x.w, y.w, d);
+        for (int i0 = 4 * warp; i0 < T * T; i0 += VT / 8) {
+          const int i = i0 + (lane >> 3);
+          const bool live = i < T * T;
+          const int ii = live ? i : 0;
+          const int t = (ii >= 1) + (ii >= 4) + (ii >= 9) + (ii >= 16) + (ii >= 25) + (ii >= 36) + (ii >= 49);
+          const int j = ii - t * t, which = j >= t, s = which ? j - t : j;
+          float d = 0.f;
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, m));
-        if (lane == 0) tb[(which ? TAB_OC : TAB_A) + t * MAXT + s] = d;
+          for (int c = 0; c < 4; ++c) {
+            const float4 x = act4<A, TC>(QK, which, t, sub + 8 * c);
+            const float4 y = act4<A, TC>(QK, 0, s, sub + 8 * c);
+            d = c == 0 ? __fmul_rn(x.x, y.x) : __fmaf_rn(x.x, y.x, d);
+            d = __fmaf_rn(x.y, y.y, d);
+            d = __fmaf_rn(x.z, y.z, d);
+            d = __fmaf_rn(x.w, y.w, d);
+          }
+#pragma unroll
+          for (int m = 4; m >= 1; m >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, m));
+          if (live && sub == 0) tb[(which ? TAB_OC : TAB_A) + t * MAXT + s] = d;
+        }
+      } else {
+#pragma unroll 1
+        for (int i = warp; i < T * T; i += VT / 32) {
+          const int t = (i >= 1) + (i >= 4) + (i >= 9) + (i >= 16) + (i >= 25) + (i >= 36) + (i >= 49);
+          const int j = i - t * t, which = j >= t, s = which ? j - t : j;
+          const float4 x = act4<A, TC>(QK, which, t, lane);
+          const float4 y = act4<A, TC>(QK, 0, s, lane);
+          float d = __fmul_rn(x.x, y.x);
+          d = __fmaf_rn(x.y, y.y, d);
+          d = __fmaf_rn(x.z, y.z, d);
+          d = __fmaf_rn(x.w, y.w, d);
+#pragma unroll
+          for (int m = 16; m >= 1; m >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, m));
+          if (lane == 0) tb[(which ? TAB_OC : TAB_A) + t * MAXT + s] = d;
+        }
       }
     }
     if (__syncthreads_or(!ok)) { fail = 1; break; }     // also: the dot products are in
