@@ -17,12 +17,14 @@
 // the 3 rows before it as three row copies. One thread owns 8 contiguous
 // channels of an eighth of the chunk (8 tokens) and walks them with the 3
 // previous rows in registers. A warp holds two heads x 16 lanes, which is
-// exactly the lane layout of the fixed sum-of-squares tree; tokens go in pairs
-// so that even lanes take the 1/sqrt of the first token and odd lanes of the
-// second. The chunk-0 thread that reads a channel's initial rows is the one that
-// later writes that channel's final rows: the final rows are taken from x (or
-// from the initial rows when the sequence is shorter than 3), so no other block
-// ever touches conv_state.
+// exactly the lane layout of the fixed sum-of-squares tree; the eight token sums
+// of a head are reduced across its 16 lanes by halving exchanges (each lane ends
+// with one token's sum, the per-token tree's bits), so one 1/sqrt per lane serves
+// the eight tokens. A warp releases its tile stage once its conv loop has read
+// it, before the norms and stores. The chunk-0 thread that reads a channel's
+// initial rows is the one that later writes that channel's final rows: the
+// final rows are taken from x (or from the initial rows when the sequence is
+// shorter than 3), so no other block ever touches conv_state.
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"

@@ -25,6 +25,12 @@
 // are computed by the same instructions in verify+commit and in decode: the
 // bitwise agreement is by construction. No atomics, no inter-block waits.
 //
+// Global traffic goes out in the order the block waits on it: the gates and the
+// conv's rows first, then the first v head's 64 KiB of state rows (issued before
+// the small loads, the state read delayed them); the next head's state is asked
+// into L2 early and its rows are loaded as soon as the current head's state is
+// written, under the current head's epilogue.
+//
 // conv_state ownership: a block owns a whole q/k head group (the q and k heads
 // and the Hv/Hk v heads that read them), so the block that reads a channel's
 // conv_state rows is the only one that rewrites them, after a block barrier.

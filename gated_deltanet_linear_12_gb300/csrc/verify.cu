@@ -32,8 +32,10 @@
 //     tf32: 10 explicit mantissa bits) and a Gram product of the q, k tile for
 //     the k.k and q.k dot products.
 // Launched as a programmatic dependent launch: a block that becomes resident
-// while the previous grid drains sets up and asks L2 for its state before it
-// waits, and every block asks L2 for the rows of the block one wave later.
+// while the previous grid drains sets up before it waits; in the CUDA-core
+// variants it also asks L2 for its state and for the rows of the block one wave
+// later. The small loads of the conv go out before the state's 64 KiB copy:
+// queued behind the copy they arrive late, and every phase waits on them.
 #include <cuda.h>
 
 #include <mutex>
@@ -244,8 +246,9 @@ template <int A> __host__ __device__ constexpr int blocks_per_sm() { return A ==
 // conv's loads, the conv_state rows and thread 0's four TMA copies of the state
 // (after its conv for T = 3, 4), and per block:
 //   - the conv + SiLU of the unit's q, k and v heads for the T draft rows (rows
-//     t..t+3 of conv_state ++ x feed token t) and the L2 norms of q and k; q, k, v
-//     rounded to the activation dtype are kept in shared memory;
+//     t..t+3 of conv_state ++ x feed token t) and the L2 norms of q and k; q, k and
+//     v are kept in f32, unrounded (only the optional post-conv copy is rounded to
+//     the activation dtype);
 //   - the dot products k_t.k_s (s < t), q_t.k_s (s <= t) and the table
 //     b_t r(t,s) (k_t.k_s), r(t,s) (q_t.k_s), g_t, b_t g_t, b_t, with
 //     r(t,s) = a_{s+1} ... a_t and g_t = a_0 ... a_t;
@@ -254,7 +257,8 @@ template <int A> __host__ __device__ constexpr int blocks_per_sm() { return A ==
 // Two variants of the products:
 //   - CUDA cores (T <= 4, and f32 activations): thread r reads its swizzled f32
 //     row with the step kernel's rounding; the dot products are warp dot
-//     products with the step kernel's rounding;
+//     products with the step kernel's rounding for T <= 2 and 8-lane group dot
+//     products (four pairs per warp at once) for T >= 3;
 //   - tensor core (TC: bf16 activations, T >= 5): one tcgen05 kind::tf32 product
 //     S0 [k_0..k_7 ; q_0..q_7]^T (M = 128, N = 16, K = 128) straight from the TMA
 //     boxes, and the Gram product [k ; q] [k ; q]^T of the same operand tile (its
