@@ -28,9 +28,9 @@
 //     cores, in the step kernel's order, so that at T = 1 the outputs are
 //     bitwise equal to those of the decode mode;
 //   - T >= 5 with bf16 activations: one tcgen05 kind::tf32 product
-//     S0 [k_0..k_7 ; q_0..q_7]^T straight from the boxes (the state is read as
-//     tf32: 10 explicit mantissa bits) and a Gram product of the q, k tile for
-//     the k.k and q.k dot products.
+//     S0 [k_0..k_7 ; q_0..q_7]^T straight from the boxes (the state and k, q are
+//     read as tf32: 10 explicit mantissa bits); the k.k and q.k dot products on
+//     the CUDA cores while the state is still arriving.
 // Launched as a programmatic dependent launch: a block that becomes resident
 // while the previous grid drains sets up before it waits; in the CUDA-core
 // variants it also asks L2 for its state and for the rows of the block one wave
@@ -125,7 +125,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 //       registers)
 //   TB  the table of gate products and dot products (TAB floats)
 //   GS  alpha, beta of this head [2][8]
-//   BR  the state, product and Gram barriers, the TMEM address, the issued flag
+//   BR  the state and product barriers (and an unused one), the TMEM address, the
+//       issued flag
 template <int A, bool TC> __host__ __device__ constexpr int qk_bytes() { return 2 * MAXT * D * 4; }
 template <int A, bool TC> __host__ __device__ constexpr int qk_region() { return (qk_bytes<A, TC>() + 1023) & ~1023; }
 // Where the v rows live: shared memory [NT][128] f32 for the CUDA-core variants
@@ -261,10 +262,9 @@ template <int A> __host__ __device__ constexpr int blocks_per_sm() { return A ==
 //     products (four pairs per warp at once) for T >= 3;
 //   - tensor core (TC: bf16 activations, T >= 5): one tcgen05 kind::tf32 product
 //     S0 [k_0..k_7 ; q_0..q_7]^T (M = 128, N = 16, K = 128) straight from the TMA
-//     boxes, and the Gram product [k ; q] [k ; q]^T of the same operand tile (its
-//     rows 16..127 are whatever follows the tile and land in unused TMEM lanes)
-//     for the dot products. The state is read as tf32; k and q, bf16 values, are
-//     exact in tf32.
+//     boxes, the state and k, q read as tf32; the dot products by 8-lane groups
+//     on the CUDA cores, with the table, before the state has arrived (a Gram
+//     product on the tensor core after the state wait was 7 % slower at T = 5).
 // NT > 0: the number of draft tokens as a compile-time constant (CUDA-core
 // variants; keeps the unrolled code small); NT = 0: read from the arguments.
 template <int A, bool TC, int NT>
@@ -285,7 +285,6 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   float* be_s = al_s + MAXT;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(be_s + MAXT);      // 8-byte aligned
   uint64_t* tc_bar = s_bar + 1;
-  uint64_t* g_bar = s_bar + 2;
   uint32_t* tc_slot = reinterpret_cast<uint32_t*>(s_bar + 3);
   uint32_t* issued = tc_slot + 1;                         // 1 once the products were issued
 
@@ -294,7 +293,6 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     *issued = 0u;
     if constexpr (TC) {
       tc::mbar_init(tc_bar, 1);
-      tc::mbar_init(g_bar, 1);
     }
     tc::fence_mbar_init();
   } else if (!TC && warp == 3) {
@@ -311,7 +309,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   }
   if constexpr (TC) {
     if (warp == 1) {
-      tc::tmem_alloc(tc_slot, 128);                       // product: 4 x 16 columns, Gram: 4 x 16
+      tc::tmem_alloc(tc_slot, 64);                        // the product: 4 x 16 columns
       tc::tmem_relinquish();
     }
   }
@@ -517,101 +515,53 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   do {                                                    // once; left early on a failed wait
     if (!valid) break;                                    // padding entry or bad slot: no outputs
     bool ok = true;
-    if constexpr (TC) {
-      // ---- warp 0: thread 0 waits for the state, then issues the Gram product
-      // and the state product (the tensor core runs them in order); the warp
-      // moves the Gram values into the table while the state product runs. The
-      // Gram product's A operand has M = 128 rows, of which rows 16..127 lie past
-      // the q/k tile, in the state region: issuing it only once the state's copy
-      // is complete means those rows (whose results land in TMEM lanes nobody
-      // reads) are settled memory, not memory the copy engine is still writing.
-      // By the time the conv is done the state has almost always arrived. Four
-      // independent accumulators (one per 32-column block of K) keep the
-      // accumulation chains short; their sum is formed on the CUDA cores.
-      if (warp == 0) {
-        if (lane == 0) {
-          const uint32_t bq = tc::smem_u32(QK), sa = tc::smem_u32(SR);
-          const uint32_t id = tc::idesc_tf32_f32(128, 16);
-          ok = tc::mbar_wait(s_bar, 0, 1u << 24);
-          if (ok) {
+    // ---- dot products: warp w takes the pairs w, w + 4, ... of the order
+    // t = 0, 1, ...: (k_t.k_s, s < t) then (q_t.k_s, s <= t); the pairs of the
+    // first T tokens are the first T^2. Lane l holds columns 4l..4l+3 (a product
+    // and three fused multiply-adds), then an xor butterfly 16, 8, 4, 2, 1: the
+    // step kernel's warp dot product.
+    if constexpr (NT >= 3 || TC) {
+      // T >= 3: an 8-lane group per pair (lane holds 16 columns, a product and
+      // 15 fused multiply-adds, then an xor butterfly 4, 2, 1), four pairs per
+      // warp at once: the T^2 pairs in one round instead of T^2 / 4 serial ones
+      // (these outputs are held to the oracle's tolerance, not to the step
+      // kernel's bits, which only T = 1 shares)
+      const int sub = lane & 7;
 #pragma unroll 1
-            for (int ks = 0; ks < 16; ++ks) {
-              const uint64_t dq = smem_desc_sw128(bq + (ks >> 2) * 2048 + (ks & 3) * 32);
-              tc::mma_tf32(tbase + 64 + 16 * (ks & 3), dq, dq, id, ks > 3);
-            }
-            tc::mma_commit(g_bar);
-#pragma unroll 1
-            for (int ks = 0; ks < 16; ++ks)
-              tc::mma_tf32(tbase + 16 * (ks & 3), smem_desc_sw128(sa + (ks >> 2) * 16384 + (ks & 3) * 32),
-                           smem_desc_sw128(bq + (ks >> 2) * 2048 + (ks & 3) * 32), id, ks > 3);
-            tc::mma_commit(tc_bar);
-            *issued = 1u;
-          }
-        }
-        const bool ok0 = __shfl_sync(0xffffffffu, ok, 0);   // thread 0's state wait
-        const bool okg = ok0 && tc::mbar_wait(g_bar, 0, 1u << 24);
-        tc::fence_after_sync();
-        ok = ok0 && okg;
-        if (__all_sync(0xffffffffu, okg)) {
-          float gv[16];
-          sum4_ld16(tbase + 64, gv);                      // lane l: row l (k_l, or q_{l-8})
-          const int t = lane & 7;
-          if (lane < 16 && t < T) {
+      for (int i0 = 4 * warp; i0 < T * T; i0 += VT / 8) {
+        const int i = i0 + (lane >> 3);
+        const bool live = i < T * T;
+        const int ii = live ? i : 0;
+        const int t = (ii >= 1) + (ii >= 4) + (ii >= 9) + (ii >= 16) + (ii >= 25) + (ii >= 36) + (ii >= 49);
+        const int j = ii - t * t, which = j >= t, s = which ? j - t : j;
+        float d = 0.f;
 #pragma unroll
-            for (int s = 0; s < MAXT; ++s)
-              if (lane < 8 ? s < t : s <= t) tb[(lane < 8 ? TAB_A : TAB_OC) + t * MAXT + s] = gv[s];
-          }
-        }
-      }
-    } else {
-      // ---- dot products: warp w takes the pairs w, w + 4, ... of the order
-      // t = 0, 1, ...: (k_t.k_s, s < t) then (q_t.k_s, s <= t); the pairs of the
-      // first T tokens are the first T^2. Lane l holds columns 4l..4l+3 (a product
-      // and three fused multiply-adds), then an xor butterfly 16, 8, 4, 2, 1: the
-      // step kernel's warp dot product.
-      if constexpr (NT >= 3) {
-        // T = 3, 4: an 8-lane group per pair (lane holds 16 columns, a product and
-        // 15 fused multiply-adds, then an xor butterfly 4, 2, 1), four pairs per
-        // warp at once: the T^2 pairs in one round instead of T^2 / 4 serial ones
-        // (these outputs are held to the oracle's tolerance, not to the step
-        // kernel's bits, which only T = 1 shares)
-        const int sub = lane & 7;
-#pragma unroll 1
-        for (int i0 = 4 * warp; i0 < T * T; i0 += VT / 8) {
-          const int i = i0 + (lane >> 3);
-          const bool live = i < T * T;
-          const int ii = live ? i : 0;
-          const int t = (ii >= 1) + (ii >= 4) + (ii >= 9) + (ii >= 16) + (ii >= 25) + (ii >= 36) + (ii >= 49);
-          const int j = ii - t * t, which = j >= t, s = which ? j - t : j;
-          float d = 0.f;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float4 x = act4<A, TC>(QK, which, t, sub + 8 * c);
-            const float4 y = act4<A, TC>(QK, 0, s, sub + 8 * c);
-            d = c == 0 ? __fmul_rn(x.x, y.x) : __fmaf_rn(x.x, y.x, d);
-            d = __fmaf_rn(x.y, y.y, d);
-            d = __fmaf_rn(x.z, y.z, d);
-            d = __fmaf_rn(x.w, y.w, d);
-          }
-#pragma unroll
-          for (int m = 4; m >= 1; m >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, m));
-          if (live && sub == 0) tb[(which ? TAB_OC : TAB_A) + t * MAXT + s] = d;
-        }
-      } else {
-#pragma unroll 1
-        for (int i = warp; i < T * T; i += VT / 32) {
-          const int t = (i >= 1) + (i >= 4) + (i >= 9) + (i >= 16) + (i >= 25) + (i >= 36) + (i >= 49);
-          const int j = i - t * t, which = j >= t, s = which ? j - t : j;
-          const float4 x = act4<A, TC>(QK, which, t, lane);
-          const float4 y = act4<A, TC>(QK, 0, s, lane);
-          float d = __fmul_rn(x.x, y.x);
+        for (int c = 0; c < 4; ++c) {
+          const float4 x = act4<A, TC>(QK, which, t, sub + 8 * c);
+          const float4 y = act4<A, TC>(QK, 0, s, sub + 8 * c);
+          d = c == 0 ? __fmul_rn(x.x, y.x) : __fmaf_rn(x.x, y.x, d);
           d = __fmaf_rn(x.y, y.y, d);
           d = __fmaf_rn(x.z, y.z, d);
           d = __fmaf_rn(x.w, y.w, d);
-#pragma unroll
-          for (int m = 16; m >= 1; m >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, m));
-          if (lane == 0) tb[(which ? TAB_OC : TAB_A) + t * MAXT + s] = d;
         }
+#pragma unroll
+        for (int m = 4; m >= 1; m >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, m));
+        if (live && sub == 0) tb[(which ? TAB_OC : TAB_A) + t * MAXT + s] = d;
+      }
+    } else {
+#pragma unroll 1
+      for (int i = warp; i < T * T; i += VT / 32) {
+        const int t = (i >= 1) + (i >= 4) + (i >= 9) + (i >= 16) + (i >= 25) + (i >= 36) + (i >= 49);
+        const int j = i - t * t, which = j >= t, s = which ? j - t : j;
+        const float4 x = act4<A, TC>(QK, which, t, lane);
+        const float4 y = act4<A, TC>(QK, 0, s, lane);
+        float d = __fmul_rn(x.x, y.x);
+        d = __fmaf_rn(x.y, y.y, d);
+        d = __fmaf_rn(x.z, y.z, d);
+        d = __fmaf_rn(x.w, y.w, d);
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, m));
+        if (lane == 0) tb[(which ? TAB_OC : TAB_A) + t * MAXT + s] = d;
       }
     }
     if (__syncthreads_or(!ok)) { fail = 1; break; }     // also: the dot products are in
@@ -643,6 +593,27 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     const int r = tid;                                    // value row
     float sk[MAXT], sq[MAXT];
     if constexpr (TC) {
+      // thread 0 waits for the state and issues the state product S0 [k ; q]^T
+      // (M = 128, N = 16, K = 128, tf32); four independent accumulators, one per
+      // 32-column block of K, keep the accumulation chains short and are summed
+      // on the CUDA cores. The dot products and the table were formed on the CUDA
+      // cores while the state was still arriving.
+      bool ok0 = true;
+      if (tid == 0) {
+        const uint32_t bq = tc::smem_u32(QK), sa = tc::smem_u32(SR);
+        const uint32_t id = tc::idesc_tf32_f32(128, 16);
+        ok0 = tc::mbar_wait(s_bar, 0, 1u << 24);
+        if (ok0) {
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int ks = 0; ks < 16; ++ks)
+            tc::mma_tf32(tbase + 16 * (ks & 3), smem_desc_sw128(sa + (ks >> 2) * 16384 + (ks & 3) * 32),
+                         smem_desc_sw128(bq + (ks >> 2) * 2048 + (ks & 3) * 32), id, ks > 3);
+          tc::mma_commit(tc_bar);
+          *issued = 1u;
+        }
+      }
+      if (__syncthreads_or(!ok0)) { fail = 1; break; }    // the state wait gave up
       ok = tc::mbar_wait(tc_bar, 0, 1u << 24);
       tc::fence_after_sync();
       if (__syncthreads_or(!ok)) { fail = 2; break; }     // also: the table is complete
@@ -745,7 +716,6 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
     tc::mbar_wait(s_bar, 0, 1u << 24);                    // the state copy, if still in flight
     if constexpr (TC) {
       if (*issued) {                                      // set before the failing barrier
-        tc::mbar_wait(g_bar, 0, 1u << 24);                // the Gram product, if still running
         tc::mbar_wait(tc_bar, 0, 1u << 24);               // the state product, if still running
       }
     }
@@ -753,7 +723,7 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   if constexpr (TC) {
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 1) tc::tmem_dealloc(tbase, 128);
+    if (warp == 1) tc::tmem_dealloc(tbase, 64);
   }
 }
 
