@@ -160,13 +160,9 @@ __device__ __forceinline__ void put_act8(uint8_t* QK, int which, int t, int c, c
   *reinterpret_cast<float4*>(QK + bsw_off(8 * which + t, c + 4)) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// One activation of `base` widened to f32, and one stored (rounded) from f32.
-template <int A> __device__ __forceinline__ float load1(const void* base, int64_t i) {
-  if constexpr (A == BF16) return bf2f(static_cast<const uint16_t*>(base)[i]);
-  else return static_cast<const float*>(base)[i];
-}
-// The same as raw bits (bf16 in the low half, or the f32 bits), widened later:
-// a load whose value is not used at once does not stall the loads after it.
+// One activation of `base` as raw bits (bf16 in the low half, or the f32 bits),
+// widened later: a load whose value is not used at once does not stall the loads
+// after it; and one activation stored (rounded) from f32.
 template <int A> __device__ __forceinline__ uint32_t load1_bits(const void* base, int64_t i) {
   if constexpr (A == BF16) return static_cast<const uint16_t*>(base)[i];
   else return static_cast<const uint32_t*>(base)[i];
