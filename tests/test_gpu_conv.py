@@ -80,6 +80,22 @@ def test_conv_varlen_bf16(G, orc, lens, init):
     assert np.array_equal(to_np(cs), rcs), "conv_state commit must be bit-exact"
 
 
+def test_conv_many_sequences_bf16(G, orc):
+    """40 sequences (more than one 32-lane group of the chunk lookup), with empty
+    and 1..5-token ones among them: outputs against the oracle, conv_state rows
+    of every slot bit-exact."""
+    rng = np.random.default_rng(107)
+    lens = rng.integers(0, 140, size=40)
+    lens[[3, 17, 31]] = 0
+    lens[[5, 6, 7, 8, 9]] = [1, 2, 3, 4, 5]
+    init = rng.integers(0, 2, size=40).astype(np.uint8)
+    inp = syn.prefill_inputs(lens, 2, 4, "bf16", seed=107, init_mask=init)
+    y, cs = _run_conv(G, inp)
+    ry, rcs = _oracle_conv(orc, inp)
+    check_bf16(to_np(y), ry, what="conv bf16, 40 sequences")
+    assert np.array_equal(to_np(cs), rcs), "conv_state commit must be bit-exact"
+
+
 def test_conv_padded_rows_and_padding_sequence(G, orc):
     inp = syn.prefill_inputs([70, 9, 33], 1, 2, "bf16", seed=102, init_mask=np.array([1, 1, 0]))
     inp["slot_idx"][1] = -1

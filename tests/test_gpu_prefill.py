@@ -76,6 +76,25 @@ def test_prefill_varlen_bf16(G, orc, lens, init):
         assert np.array_equal(bits(S)[sl], inp["state"][sl].view(np.int32))
 
 
+def test_prefill_many_sequences_bf16(G, orc):
+    """300 sequences (past the 256 the block ranking by length covers; the blocks
+    then take sequences in index order), lengths 0..100: outputs and every state
+    against the oracle, untouched slots bitwise unchanged."""
+    rng = np.random.default_rng(570)
+    lens = rng.integers(0, 101, size=300)
+    lens[[0, 150, 299]] = 0
+    init = rng.integers(0, 2, size=300).astype(np.uint8)
+    inp = syn.prefill_inputs(lens, 1, 2, "bf16", seed=570, init_mask=init)
+    qkv = _oracle_qkv(orc, inp)
+    out, S = _run_prefill(G, inp, qkv)
+    ro, rs = _oracle_prefill(orc, inp, qkv)
+    check_bf16(to_np(out), ro, what="prefill bf16 out, 300 sequences")
+    check_states(to_np(S), rs, [int(s) for s in inp["slot_idx"]], 1e-4, "prefill bf16 state, 300 sequences")
+    unused = sorted(set(range(inp["state"].shape[0])) - set(int(s) for s in inp["slot_idx"]))
+    for sl in unused:
+        assert np.array_equal(bits(S)[sl], inp["state"][sl].view(np.int32))
+
+
 @pytest.mark.parametrize("act", ["bf16", "f32"])
 def test_prefill_q_scale_and_eps(G, orc, act):
     """q_scale = d^-1/2 (an ABI parameter the definition does not have) with an eps
