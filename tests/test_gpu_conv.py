@@ -96,6 +96,22 @@ def test_conv_many_sequences_bf16(G, orc):
     assert np.array_equal(to_np(cs), rcs), "conv_state commit must be bit-exact"
 
 
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_conv_tail_group_of_one_head(G, orc, act):
+    """Hk = 1, Hv = 3: 5 heads, so the last group of four holds one head and half
+    of each warp's lanes are idle (they still take part in the norm's lane
+    exchanges); outputs against the oracle, conv_state bit-exact."""
+    inp = syn.prefill_inputs([70, 1, 0, 129], 1, 3, act, seed=108, init_mask=np.array([1, 0, 1, 1]))
+    y, cs = _run_conv(G, inp)
+    ry, rcs = _oracle_conv(orc, inp)
+    if act == "bf16":
+        check_bf16(to_np(y), ry, what="conv bf16, 5 heads")
+    else:
+        ry32, _ = _oracle_conv(orc, inp, prec="f32")
+        check_f32_rel(to_np(y), ry32, 1e-5, "conv f32, 5 heads")
+    assert np.array_equal(to_np(cs), rcs), "conv_state commit must be bit-exact"
+
+
 def test_conv_padded_rows_and_padding_sequence(G, orc):
     inp = syn.prefill_inputs([70, 9, 33], 1, 2, "bf16", seed=102, init_mask=np.array([1, 1, 0]))
     inp["slot_idx"][1] = -1
