@@ -337,7 +337,8 @@ __device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, cons
     if constexpr (MODE == COMMIT) {
       if (tid == 0 && g + 1 < nh) prefetch_state_l2(state + (((int64_t)slot * Hv + h + 1) * D) * D);
     }
-    // state rows of head h: in flight since the previous head's products / commit
+    // state rows of head h: in flight since load_first_state (head 0) or since the
+    // previous head's state write (the others)
     float* Sg = state + (((int64_t)slot * Hv + h) * D) * D;
     __syncthreads();                                      // tables ready
 

@@ -511,15 +511,14 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
   do {                                                    // once; left early on a failed wait
     if (!valid) break;                                    // padding entry or bad slot: no outputs
     bool ok = true;
-    // ---- dot products: warp w takes the pairs w, w + 4, ... of the order
-    // t = 0, 1, ...: (k_t.k_s, s < t) then (q_t.k_s, s <= t); the pairs of the
-    // first T tokens are the first T^2. Lane l holds columns 4l..4l+3 (a product
-    // and three fused multiply-adds), then an xor butterfly 16, 8, 4, 2, 1: the
-    // step kernel's warp dot product.
+    // ---- dot products, in the order t = 0, 1, ...: (k_t.k_s, s < t) then
+    // (q_t.k_s, s <= t); the pairs of the first T tokens are the first T^2. On
+    // the CUDA cores in every variant, formed (with the table below) while the
+    // state is still arriving.
     if constexpr (NT >= 3 || TC) {
       // T >= 3: an 8-lane group per pair (lane holds 16 columns, a product and
       // 15 fused multiply-adds, then an xor butterfly 4, 2, 1), four pairs per
-      // warp at once: the T^2 pairs in one round instead of T^2 / 4 serial ones
+      // warp at once: the T^2 pairs in T^2 / 16 rounds instead of T^2 / 4
       // (these outputs are held to the oracle's tolerance, not to the step
       // kernel's bits, which only T = 1 shares)
       const int sub = lane & 7;
@@ -545,6 +544,9 @@ __global__ void __launch_bounds__(VT, blocks_per_sm<A>())
         if (live && sub == 0) tb[(which ? TAB_OC : TAB_A) + t * MAXT + s] = d;
       }
     } else {
+      // T <= 2: warp w takes the pairs w, w + 4, ...; lane l holds columns
+      // 4l..4l+3 (a product and three fused multiply-adds), then an xor butterfly
+      // 16, 8, 4, 2, 1: the step kernel's warp dot product
 #pragma unroll 1
       for (int i = warp; i < T * T; i += VT / 32) {
         const int t = (i >= 1) + (i >= 4) + (i >= 9) + (i >= 16) + (i >= 25) + (i >= 36) + (i >= 49);
