@@ -294,10 +294,11 @@ __device__ __forceinline__ bool step_pass(const StepArgs& p, const void* x, cons
     if (tid == 0 && nh > 1) prefetch_state_l2(state + (((int64_t)slot * Hv + h0 + 1) * D) * D);
   }
 
-  // ---- phase 2: key/key and query/key dot products (shared by the group)
+  // ---- phase 2: key/key and query/key dot products (shared by the group); only
+  // the pairs the tables use: k_t.k_s for s < t, q_t.k_s for s <= t
   for (int pr = warp; pr < 2 * MAXT * MAXT; pr += STEP_THREADS / 32) {
     const int which = pr / (MAXT * MAXT), t = (pr % (MAXT * MAXT)) / MAXT, s = pr % MAXT;
-    if (t >= n || s >= n) continue;                        // warp-uniform
+    if (t >= n || (which == 0 ? s >= t : s > t)) continue;   // warp-uniform
     if (which == 0) { const float d = warp_dot128(k_s + t * D, k_s + s * D); if (lane == 0) kk_s[t * MAXT + s] = d; }
     else if (OUTPUTS) { const float d = warp_dot128(q_s + t * D, k_s + s * D); if (lane == 0) qk_s[t * MAXT + s] = d; }
   }
